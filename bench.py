@@ -1,0 +1,377 @@
+"""Benchmark of the DeepSeekMoE layer forward on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference] [--no-cpu-baseline]
+
+One step = one pass of the whole hot path over one synthetic batch: route,
+permute, expert FFNs (routed + shared), combine, then the +-gamma bias
+update.  Default workload: the V3-shaped prefill layer (T=8192, d=7168,
+256 routed experts, top-8, 1 shared, intermediate 2048, bf16, seed 2).
+Prints one JSON line.  N > 1 (torchrun) runs independent replicas, one per
+GPU, with no data-path collective; value = all ranks' tokens / max time.
+
+--impl reference times the CPU fp64 oracle (the only reference this method
+has) on a bounded sample of the same workload, on rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from moe_inputs import as_f64, generate, get_config  # noqa: E402
+
+METRIC = "MoE-layer tokens/s at V3 shape"
+L2_NOTE = "inputs larger than L2 (22.5 GB of expert weights read per step)"
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            m = json.load(f)
+        return {"hbm_gbs": m["hbm_gbs"], "bf16_tflops": m["bf16_tflops"],
+                "bf16_tflops_sustained": m.get("bf16_tflops_sustained"),
+                "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0,
+            "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+
+
+def layer_flops(cfg) -> float:
+    A = cfg.T * cfg.top_k
+    return (6.0 * A * cfg.d * cfg.d_ff + 6.0 * cfg.T * cfg.d * cfg.n_shared *
+            cfg.d_ff + 2.0 * cfg.T * cfg.d * cfg.n_routed)
+
+
+def ffn_flops(cfg) -> float:
+    A = cfg.T * cfg.top_k
+    return 6.0 * (A + cfg.T * cfg.n_shared) * cfg.d * cfg.d_ff
+
+
+def ffn_bytes(cfg, counts) -> float:
+    """Algorithmic bytes of the expert-FFN call: weights of the experts that
+    received tokens plus the shared experts (read once), the routed and
+    shared input rows, and the fp32 outputs."""
+    es = 2 if cfg.dtype == "bf16" else 4
+    touched = int((np.asarray(counts) > 0).sum())
+    w = 3.0 * cfg.d * cfg.d_ff * es * (touched + cfg.n_shared)
+    A = cfg.T * cfg.top_k
+    act = A * cfg.d * es + cfg.T * cfg.d * es + (A + cfg.T) * cfg.d * 4
+    return w + act
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled every 200 ms."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,"
+             "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no-smi"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def cpu_baseline(cfg, t, budget_s: float = 15.0, max_tokens: int = 64):
+    """The fp64 oracle, as it stands, on a bounded sample of this workload:
+    the whole routing of sampled tokens plus their routed and shared FFNs.
+    Returns tokens/s and what the sample was."""
+    import oracle.moe as om
+    try:
+        from threadpoolctl import threadpool_info
+        blas = max((i.get("num_threads", 1) for i in threadpool_info()),
+                   default=1)
+    except Exception:
+        blas = os.cpu_count()
+    rng = np.random.default_rng(cfg.seed + 99)
+    order = rng.permutation(cfg.T)
+    E64, b64 = as_f64(t["E"]), as_f64(t["b"])
+    shared = [tuple(as_f64(t[k][s]) for k in ("ws_gate", "ws_up", "ws_down"))
+              for s in range(cfg.n_shared)]
+    host = {}
+
+    def routed(e):
+        return tuple(host[e][k].to(torch.float64).numpy()
+                     for k in range(3))
+    done, spent = 0, 0.0
+    for tok in order[:max_tokens]:
+        u64 = as_f64(t["u"][int(tok):int(tok) + 1])
+        t0 = time.perf_counter()
+        r = om.route(u64, E64, b64, cfg.top_k)
+        spent += time.perf_counter() - t0
+        for e in r["idx"][0].tolist():      # stage weights on the host (untimed)
+            if e not in host:
+                host[e] = tuple(t[k][e].cpu() for k in
+                                ("w_gate", "w_up", "w_down"))
+        t0 = time.perf_counter()
+        om.layer_forward(u64, E64, b64, cfg.top_k, routed, shared)
+        spent += time.perf_counter() - t0
+        done += 1
+        if spent >= budget_s:
+            break
+    return {"value": done / spent, "unit": "tokens/s", "cores": int(blas),
+            "kind": "oracle",
+            "sample": f"{done} of {cfg.T} tokens of {cfg.name} (routing + "
+                      f"routed and shared FFNs, fp64), {spent:.1f} s"}
+
+
+def run_reference(args, cfg):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    torch.manual_seed(0)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = generate(cfg, dev)
+    per_step = []
+    per_tok = max(1, int(args.ref_tokens))
+    for i in range(args.warmup + args.steps):
+        c = cpu_baseline(cfg, t, budget_s=args.ref_budget, max_tokens=per_tok)
+        if i >= args.warmup:
+            per_step.append(c)
+    value = statistics.mean(c["value"] for c in per_step)
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * cfg.T / value,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": cfg.name, "T": cfg.T, "d": cfg.d,
+                       "n_routed": cfg.n_routed, "top_k": cfg.top_k,
+                       "n_shared": cfg.n_shared, "d_ff": cfg.d_ff},
+            "cpu_baseline": dict(per_step[-1], value=value),
+            "e2e": {"value": value, "unit": "tokens/s",
+                    "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, cfg):
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    import mixture_experts_layer_gemms_b300 as moe
+
+    dev = torch.device("cuda", local)
+    t = generate(cfg, dev)
+    layer = moe.MoELayer(t["E"], t["b"].clone(), t["w_gate"], t["w_up"],
+                         t["w_down"], t["ws_gate"], t["ws_up"], t["ws_down"],
+                         top_k=cfg.top_k, h_dtype=torch.float32)
+    u = t["u"]
+    bufs = layer.buffers(cfg.T)
+    sh = layer.shape(cfg.T)
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+
+    def step(i=None):
+        """One step through the C ABI; returns kernels launched."""
+        n = 0
+        moe.route(sh, u, layer.E, layer.bias, bufs.topk_idx, bufs.topk_gate,
+                  bufs.counts, bufs.workspace)
+        n += moe.last_launch_count()
+        moe.permute(sh, u, bufs.topk_idx, bufs.counts, bufs.offsets,
+                    bufs.perm, bufs.inv, bufs.x_perm, bufs.workspace)
+        n += moe.last_launch_count()
+        if i is not None:
+            ev[i][0].record(stream)
+        moe.expert_ffn(sh, bufs.x_perm, bufs.offsets, layer.w_gu,
+                       layer.w_down, u, layer.ws_gu, layer.ws_down,
+                       bufs.y_perm, bufs.y_shared, bufs.workspace)
+        n += moe.last_launch_count()
+        if i is not None:
+            ev[i][1].record(stream)
+        moe.combine(sh, u, bufs.y_perm, bufs.y_shared, bufs.inv,
+                    bufs.topk_gate, bufs.h)
+        n += moe.last_launch_count()
+        moe.update_bias(cfg.n_routed, bufs.counts, cfg.T * cfg.top_k,
+                        cfg.gamma, layer.bias)
+        n += moe.last_launch_count()
+        return n
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    moe.get_device_error()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    launches = 0
+    for i in range(args.steps):
+        launches += step(i)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    moe.get_device_error()
+    ms = t0.elapsed_time(t1)
+    if ws > 1:
+        import torch.distributed as dist
+        x = torch.tensor([ms], device=dev)
+        dist.all_reduce(x, op=dist.ReduceOp.MAX)
+        ms = float(x.item())
+    ffn_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    counts = bufs.counts.cpu().numpy()
+
+    # end to end through the public API with host buffers: H2D of u from
+    # pinned memory, the layer, D2H of h, every step
+    u_host = u.cpu().pin_memory()
+    h_host = torch.empty(bufs.h.shape, dtype=bufs.h.dtype).pin_memory()
+    u_dev = torch.empty_like(u)
+    e_steps = max(2, min(args.steps, 10))
+    torch.cuda.synchronize()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e_steps):
+        u_dev.copy_(u_host, non_blocking=True)
+        h = layer(u_dev, update_bias=True, gamma=cfg.gamma)
+        h_host.copy_(h, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e_ms = e0.elapsed_time(e1) / e_steps
+    if ws > 1:
+        import torch.distributed as dist
+        x = torch.tensor([e_ms], device=dev)
+        dist.all_reduce(x, op=dist.ReduceOp.MAX)
+        e_ms = float(x.item())
+    moe.get_device_error()
+
+    peaks = _peaks()
+    ms_step = ms / args.steps
+    value = ws * cfg.T * args.steps / (ms / 1e3)
+    decode = cfg.T * cfg.top_k <= 48 * cfg.n_routed
+    if decode:
+        ach = ffn_bytes(cfg, counts) / (ffn_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": ach / peaks["hbm_gbs"],
+                "traffic": None,
+                "kernel": "grouped_gemm_kernel<32,8> (gate/up + down launches)",
+                "peak_source": f"{peaks['source']} hbm_gbs"}
+    else:
+        ach = ffn_flops(cfg) / (ffn_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": ach,
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": ach / peaks["bf16_tflops"], "traffic": None,
+                "kernel": "grouped_gemm_kernel<256,4> (gate/up + down launches)",
+                "peak_source": f"{peaks['source']} bf16_tflops (burst)",
+                "frac_of_sustained": (ach / peaks["bf16_tflops_sustained"]
+                                      if peaks["bf16_tflops_sustained"]
+                                      else None)}
+    roof["ms_per_launch_pair"] = ffn_ms
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": ws, "steps": args.steps, "warmup": max(3, args.warmup),
+            "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": cfg.name, "T": cfg.T, "d": cfg.d,
+                       "n_routed": cfg.n_routed, "top_k": cfg.top_k,
+                       "n_shared": cfg.n_shared, "d_ff": cfg.d_ff,
+                       "parallelism": f"replicas x{ws}", "l2": L2_NOTE},
+            "layer_tflops": layer_flops(cfg) / (ms_step / 1e3) / 1e12,
+            "layer_frac_of_bf16_peak": layer_flops(cfg) / (ms_step / 1e3) /
+            1e12 / peaks["bf16_tflops"],
+            "roofline": roof,
+            "clocks": clk,
+            "gpu_launches": launches * ws,
+            "e2e": {"value": ws * cfg.T / (e_ms / 1e3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": u.numel() * u.element_size(),
+                    "d2h_bytes_per_step": bufs.h.numel() *
+                    bufs.h.element_size()}}
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, t, budget_s=args.ref_budget)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="v3_prefill")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-budget", type=float, default=15.0,
+                    help="seconds of oracle work per reference step")
+    ap.add_argument("--ref-tokens", type=int, default=4,
+                    help="tokens per reference step (upper bound)")
+    args = ap.parse_args()
+    cfg = get_config(args.workload)
+    if args.impl == "reference":
+        if args.ref_budget > 10.0:
+            args.ref_budget = 10.0
+        run_reference(args, cfg)
+    else:
+        run_ours(args, cfg)
+
+
+if __name__ == "__main__":
+    main()

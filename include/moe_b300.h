@@ -1,0 +1,170 @@
+/*
+ * moe_b300.h -- C ABI of the DeepSeekMoE layer forward on one B300 (sm_103a).
+ *
+ * The layer (source: "【推理llm論文精讀】DeepSeek V3技術論文", section 2.2
+ * "DeepSeekMoE"; the bias step also "AI新顶流-DeepSeek 技术大揭秘", section
+ * 无辅助损失的负载均衡策略):
+ *
+ *   s_{i,t} = Sigmoid(u_t . e_i)                      affinity equation
+ *   top-K_r experts of token t by s_{i,t} + b_i       biased selection
+ *   g_{i,t} = s_{i,t} on those experts, else 0        routing-weight equation
+ *   h_t = u_t + sum_{s<N_s} FFN^(s)_s(u_t)
+ *             + sum_{i<N_r} g_{i,t} FFN^(r)_i(u_t)    FFN-output equation
+ *   after the step: b_i -= gamma if expert i is overloaded,
+ *                   b_i += gamma if it is underloaded
+ *
+ * FFN(x) = W_down (SiLU(W_gate x) * (W_up x)) (SwiGLU; the pages give no FFN
+ * form).  Ties in the top-K go to the lower expert index.  No gate
+ * renormalisation.
+ *
+ * Conventions for every call:
+ *  - All tensor pointers are DEVICE pointers, row-major, owned by the caller.
+ *    The library allocates nothing; scratch lives in the caller's workspace
+ *    (size from moe_workspace_size).
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the
+ *    legacy default stream).  Argument errors are returned immediately and
+ *    nothing is launched.  Errors found on the device (a pipeline wait that
+ *    timed out, an index out of range) are recorded in a device error word
+ *    and reported by moe_get_device_error.
+ *  - Pointers must be 16-byte aligned.  d and d_ff must be multiples of 64,
+ *    d a multiple of 128; n_routed <= 256 and a multiple of 16 for bf16
+ *    (<= 1024 for fp32); 1 <= top_k <= min(16, n_routed); 0 <= n_shared <= 8.
+ *    Violations return MOE_ERR_UNSUPPORTED (shape) or MOE_ERR_INVALID_ARG.
+ *  - Element type of u, E, weights and x_perm: shape->dtype.  y_perm,
+ *    y_shared, bias and topk_gate are fp32; indices and counts int32.
+ *  - The library never aborts the process.
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* null / misaligned pointer, bad value        */
+  MOE_ERR_UNSUPPORTED = 2,   /* shape outside the supported range           */
+  MOE_ERR_WORKSPACE = 3,     /* workspace missing or too small              */
+  MOE_ERR_CUDA = 4,          /* a CUDA runtime call failed                  */
+  MOE_ERR_TIMEOUT = 5,       /* a device pipeline wait gave up (no hang)    */
+  MOE_ERR_DEVICE_CHECK = 6   /* a device-side bounds check failed           */
+} moe_status;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+
+typedef struct {
+  int T;          /* tokens in the batch                                    */
+  int d;          /* hidden size (length of u_t and e_i)                    */
+  int n_routed;   /* N_r, routed experts                                    */
+  int top_k;      /* K_r, routed experts per token                          */
+  int n_shared;   /* N_s, shared experts (every token, weight 1)            */
+  int d_ff;       /* I, intermediate size of every expert FFN               */
+  moe_dtype dtype;/* element type of activations and weights                */
+} moe_shape;
+
+/* Bytes of workspace every call below needs for this shape (one buffer
+ * serves all calls; it holds per-block histograms and the intermediate
+ * activations H).  No alignment beyond 256 bytes is required.            */
+MOE_API moe_status moe_workspace_size(const moe_shape* shape, size_t* bytes);
+
+/* One-time weight repack (not part of the per-step path).
+ *  w_gate, w_up   [n_routed, d_ff, d]   -> w_gu_packed  [n_routed, 2*d_ff, d]
+ *  ws_gate, ws_up [n_shared, d_ff, d]   -> ws_gu_packed [2*n_shared*d_ff, d]
+ *  ws_down        [n_shared, d, d_ff]   -> ws_down_packed [d, n_shared*d_ff]
+ * Packed gate/up rows come in blocks of 128: 64 gate rows then the 64 up
+ * rows of the same intermediate columns, so one 128-row weight tile yields
+ * 64 columns of SiLU(gate)*up.  The shared experts are concatenated along
+ * the intermediate dimension, so sum_s FFN_s(u) is one wider FFN.
+ * Routed w_down [n_routed, d, d_ff] is used as is.  ws_* may be NULL when
+ * n_shared == 0.                                                          */
+MOE_API moe_status moe_pack_weights(const moe_shape* shape,
+                            const void* w_gate, const void* w_up,
+                            const void* ws_gate, const void* ws_up,
+                            const void* ws_down,
+                            void* w_gu_packed, void* ws_gu_packed,
+                            void* ws_down_packed, void* stream);
+
+/* Routing (affinity equation, biased selection, routing-weight equation).
+ *  u [T, d], centroids E [n_routed, d] (row i = e_i), bias b [n_routed] fp32
+ *  -> topk_idx [T, top_k] int32: the selected experts of each token, by
+ *     s+b descending, lower index first on ties;
+ *     topk_gate [T, top_k] fp32: g = s (never s+b) of those experts;
+ *     counts [n_routed] int32: tokens routed to each expert in this batch.
+ * s = 1/(1+exp(-z)) with z accumulated in fp32 (bf16 inputs: on the tensor
+ * cores; fp32 inputs: fp32 FMA).  The bias only selects.                  */
+MOE_API moe_status moe_route(const moe_shape* shape, const void* u,
+                     const void* centroids, const float* bias,
+                     int32_t* topk_idx, float* topk_gate, int32_t* counts,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/* Dispatch: expert-contiguous copy of the token rows.
+ *  offsets [n_routed+1]: exclusive prefix sum of counts (offsets[N] = T*K);
+ *  perm [T*K]: token filling each slot; slots of expert e are
+ *     [offsets[e], offsets[e+1]) in ascending token order (deterministic);
+ *  inv [T, top_k]: slot of assignment (t, k);
+ *  x_perm [T*K, d]: x_perm[slot] = u[perm[slot]].                         */
+MOE_API moe_status moe_permute(const moe_shape* shape, const void* u,
+                       const int32_t* topk_idx, const int32_t* counts,
+                       int32_t* offsets, int32_t* perm, int32_t* inv,
+                       void* x_perm, void* workspace, size_t workspace_bytes,
+                       void* stream);
+
+/* Expert FFNs (the two sums of the FFN-output equation, before weighting).
+ *  y_perm [T*K, d]: rows [offsets[e], offsets[e+1]) = FFN^(r)_e of those
+ *     x_perm rows, from w_gu_packed and w_down [n_routed, d, d_ff];
+ *  y_shared [T, d] = sum_s FFN^(s)_s(u) (not written when n_shared == 0).
+ * y_perm and y_shared are fp32 for both dtypes.  bf16: tcgen05 tensor-core
+ * GEMMs, fp32 accumulation in TMEM, H = SiLU(gate)*up rounded to bf16 in
+ * the workspace (it is the second GEMM's operand).  fp32: fp32 FMA.       */
+MOE_API moe_status moe_expert_ffn(const moe_shape* shape, const void* x_perm,
+                          const int32_t* offsets, const void* w_gu_packed,
+                          const void* w_down, const void* u,
+                          const void* ws_gu_packed, const void* ws_down_packed,
+                          void* y_perm, void* y_shared, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
+/* Combine (FFN-output equation):
+ *  h[t] = u[t] + y_shared[t] + sum_k topk_gate[t,k] * y_perm[inv[t,k]],
+ * accumulated in fp32 in that order; h is written as h_dtype.  y_shared may
+ * be NULL when n_shared == 0.                                             */
+MOE_API moe_status moe_combine(const moe_shape* shape, const void* u,
+                       const void* y_perm, const void* y_shared,
+                       const int32_t* inv, const float* topk_gate, void* h,
+                       moe_dtype h_dtype, void* stream);
+
+/* Auxiliary-loss-free bias step after a batch (section 2.2 of the notes;
+ * load counted over the whole step):
+ *   counts[i]*n_routed >  total_assign  (overloaded):  b_i = fl32(b_i - gamma)
+ *   counts[i]*n_routed <  total_assign  (underloaded): b_i = fl32(b_i + gamma)
+ *   otherwise unchanged.  total_assign = T*K.  gamma is rounded to fp32.    */
+MOE_API moe_status moe_update_bias(int n_routed, const int32_t* counts,
+                           long long total_assign, float gamma, float* bias,
+                           void* stream);
+
+/* Synchronises `stream`, reads and clears the device error word of the
+ * current device.  MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_CHECK.       */
+MOE_API moe_status moe_get_device_error(void* stream);
+
+/* Static description of a status code; detail of the last host-side error
+ * of the calling thread.                                                  */
+MOE_API const char* moe_status_string(moe_status status);
+MOE_API const char* moe_last_error_detail(void);
+
+/* Number of kernel launches the previous successful call on this thread
+ * issued (for launch accounting).                                         */
+MOE_API int moe_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_B300_H */

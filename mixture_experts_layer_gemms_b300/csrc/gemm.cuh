@@ -1,0 +1,394 @@
+// Grouped expert GEMMs on the 5th-generation tensor cores (tcgen05 + TMEM,
+// operands staged by TMA).  ("【推理llm論文精讀】DeepSeek V3技術論文", section
+// 2.2: FFN^(r)_i of each selected expert and FFN^(s) of every shared expert
+// in the FFN-output equation; SwiGLU form is this library's reading.)
+//
+// Orientation: the weight rows sit on the MMA's M side (128 TMEM lanes) and
+// the tokens on its N side, so a group of M_e tokens pads only to a multiple
+// of 16 (tokens per tile = min(BN, remaining) rounded up to 16).
+//
+//   D[w, n] = sum_k W[a_row + w, k] * X[b_row + n, k]     (w < 128, n < N)
+//
+// Gate/up pass (swiglu = 1): a 128-row packed weight tile holds 64 gate rows
+// then the 64 up rows of the same intermediate columns, so the epilogue
+// emits 64 columns of H = SiLU(gate) * up (bf16, the next GEMM's operand).
+// Down pass (swiglu = 0): 128 output columns of Y, kept in fp32.
+//
+// Work items: (group, weight tile, token chunk) with the chunk index
+// fastest, so the items that share a weight tile run side by side and the
+// tile is fetched from HBM about once.  The shared experts form one extra
+// group that spans all T tokens, scheduled first.  Offsets stay on the
+// device: each CTA derives the item table from them in its prologue.
+//
+// Warp roles (192 threads, one CTA per SM, persistent):
+//   warp 0 lane 0: TMA producer over a STAGES-deep smem ring;
+//   warp 1 lane 0: MMA issuer (also allocates / frees TMEM);
+//   warps 2..5   : epilogue, double-buffered TMEM accumulators so that the
+//                  epilogue of one item overlaps the mainloop of the next.
+#pragma once
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int kGemmBM = 128;    // weight rows per tile (MMA M)
+constexpr int kGemmBK = 64;     // K per pipeline stage (128 B of bf16)
+constexpr int kBoxRows = 32;    // token rows per TMA box
+constexpr int kMaxGroups = 256;
+
+struct GemmParams {
+  const int* offsets;   // routed group row offsets [n_groups+1] (device)
+  int n_groups;         // routed groups (0: none)
+  int w_rows_routed;    // weight rows per routed group
+  int k_routed;         // reduction length of the routed pass
+  long long max_routed_rows;  // rows of the routed B operand / output
+  int shared_rows;      // tokens of the shared group (0: none)
+  int w_rows_shared;    // weight rows of the shared group
+  int k_shared;         // reduction length of the shared pass
+  void* out_routed;     // swiglu: H bf16; else: Y fp32
+  long long ld_routed;
+  void* out_shared;
+  long long ld_shared;
+  int swiglu;
+};
+
+template <int BN, int STAGES>
+struct GemmSmem {
+  static constexpr int a_bytes = kGemmBM * kGemmBK * 2;
+  static constexpr int b_bytes = BN * kGemmBK * 2;
+  static constexpr int a_off = 0;
+  static constexpr int b_off = a_off + STAGES * a_bytes;
+  static constexpr int stg_off = b_off + STAGES * b_bytes;
+  static constexpr int stg_bytes = 128 * 33 * 4;
+  static constexpr int bar_off = stg_off + stg_bytes;
+  static constexpr int n_bars = 2 * STAGES + 5;
+  static constexpr int misc_off = bar_off + n_bars * 8;
+  static constexpr int epok_off = misc_off + 16;
+  static constexpr int tab_off = epok_off + 16;
+  static constexpr int total = tab_off + 2 * (kMaxGroups + 1) * 4;
+  static constexpr int alloc = total + 1024;
+  static constexpr int tmem_cols = 2 * BN < 32 ? 32 : 2 * BN;
+  static_assert(alloc <= 227 * 1024, "shared memory");
+};
+
+struct Tile {
+  int a_row;      // first weight row (in its tensor map)
+  int b_row;      // first token row (in its tensor map and output)
+  int n_valid;    // tokens in this tile
+  int n_mma;      // n_valid rounded up to 16
+  int k;          // reduction length
+  int wt;         // weight tile index inside the group
+  int shared;     // 1: shared group
+};
+
+template <int BN>
+__device__ __forceinline__ Tile decode_item(int item, const GemmParams& p,
+                                            int n_items_s, int nch_s,
+                                            const int* off_s,
+                                            const int* chunk_pre) {
+  Tile t;
+  if (item < n_items_s) {
+    const int wt = item / nch_s, ch = item % nch_s;
+    t.shared = 1;
+    t.wt = wt;
+    t.a_row = wt * kGemmBM;
+    t.b_row = ch * BN;
+    t.n_valid = min(BN, p.shared_rows - t.b_row);
+    t.k = p.k_shared;
+  } else {
+    const int wt_r = p.w_rows_routed / kGemmBM;
+    const int j = item - n_items_s;
+    // largest e with chunk_pre[e] * wt_r <= j
+    int lo = 0, hi = p.n_groups;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (chunk_pre[mid] * wt_r <= j) lo = mid; else hi = mid;
+    }
+    const int e = lo;
+    const int ce = chunk_pre[e + 1] - chunk_pre[e];
+    const int local = j - chunk_pre[e] * wt_r;
+    const int wt = local / ce, ch = local % ce;
+    t.shared = 0;
+    t.wt = wt;
+    t.a_row = e * p.w_rows_routed + wt * kGemmBM;
+    t.b_row = off_s[e] + ch * BN;
+    t.n_valid = min(BN, off_s[e + 1] - t.b_row);
+    t.k = p.k_routed;
+  }
+  t.n_mma = (t.n_valid + 15) & ~15;
+  return t;
+}
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(192, 1)
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA_r,
+                    const __grid_constant__ CUtensorMap tmB_r,
+                    const __grid_constant__ CUtensorMap tmA_s,
+                    const __grid_constant__ CUtensorMap tmB_s,
+                    const GemmParams p) {
+  using L = GemmSmem<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar_full = sbase + L::bar_off;
+  const uint32_t bar_empty = bar_full + 8 * STAGES;
+  const uint32_t bar_tfull = bar_empty + 8 * STAGES;    // [2]
+  const uint32_t bar_tempty = bar_tfull + 16;           // [2]
+  const uint32_t bar_final = bar_tempty + 16;
+  volatile uint32_t* tmem_slot =
+      reinterpret_cast<volatile uint32_t*>(smem + L::misc_off);
+  volatile int* abort_flag =
+      reinterpret_cast<volatile int*>(smem + L::misc_off + 4);
+  volatile int* bad_flag =
+      reinterpret_cast<volatile int*>(smem + L::misc_off + 8);
+  volatile int* ep_ok = reinterpret_cast<volatile int*>(smem + L::epok_off);
+  int* off_s = reinterpret_cast<int*>(smem + L::tab_off);        // [G+1]
+  int* chunk_pre = off_s + (kMaxGroups + 1);                     // [G+1]
+  float* stg = reinterpret_cast<float*>(smem + L::stg_off);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = p.n_groups;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(bar_tfull + 8 * a, 1);
+      mbar_init(bar_tempty + 8 * a, 128);
+    }
+    mbar_init(bar_final, 1);
+    *abort_flag = 0;
+    *bad_flag = 0;
+    fence_mbar_init();
+    if (G > 0) {
+      tma_prefetch_desc(&tmA_r);
+      tma_prefetch_desc(&tmB_r);
+    }
+    if (p.shared_rows > 0) {
+      tma_prefetch_desc(&tmA_s);
+      tma_prefetch_desc(&tmB_s);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(sbase + L::misc_off, L::tmem_cols);
+    tmem_relinquish();
+  }
+  // Item table: offsets (checked) and the prefix of token chunks per group.
+  if (G > 0)
+    for (int e = threadIdx.x; e <= G; e += blockDim.x) off_s[e] = p.offsets[e];
+  __syncthreads();
+  for (int e = threadIdx.x; e < G; e += blockDim.x) {
+    const int m = off_s[e + 1] - off_s[e];
+    if (m < 0 || off_s[e] < 0) *bad_flag = 1;
+    chunk_pre[e + 1] = m > 0 ? (m + BN - 1) / BN : 0;
+  }
+  if (threadIdx.x == 0) {
+    chunk_pre[0] = 0;
+    if (G > 0 && static_cast<long long>(off_s[G]) > p.max_routed_rows)
+      *bad_flag = 1;
+  }
+  __syncthreads();
+  if (warp == 0) {   // inclusive scan of chunk counts, 32 at a time
+    int carry = 0;
+    for (int base = 1; base <= G; base += 32) {
+      const int i = base + lane;
+      int v = (i <= G) ? chunk_pre[i] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += y;
+      }
+      if (i <= G) chunk_pre[i] = v + carry;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const bool bad = *bad_flag != 0;
+  if (bad && threadIdx.x == 0) report_error(ERR_CHECK, KID_GEMM, 0);
+
+  const int nch_s = p.shared_rows > 0 ? (p.shared_rows + BN - 1) / BN : 0;
+  const int n_items_s = nch_s * (p.w_rows_shared / kGemmBM);
+  const int n_items = bad ? 0
+                          : n_items_s + (G > 0 ? chunk_pre[G] *
+                                                     (p.w_rows_routed / kGemmBM)
+                                               : 0);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      for (int item = blockIdx.x; item < n_items && !*abort_flag;
+           item += gridDim.x) {
+        const Tile t = decode_item<BN>(item, p, n_items_s, nch_s, off_s,
+                                       chunk_pre);
+        const CUtensorMap* mA = t.shared ? &tmA_s : &tmA_r;
+        const CUtensorMap* mB = t.shared ? &tmB_s : &tmB_r;
+        const int nbox = (t.n_mma + kBoxRows - 1) / kBoxRows;
+        const uint32_t bytes = L::a_bytes + nbox * kBoxRows * kGemmBK * 2;
+        const int nk = t.k / kGemmBK;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag,
+                         KID_GEMM, 1))
+            break;
+          const uint32_t fb = bar_full + 8 * stage;
+          mbar_arrive_expect_tx(fb, bytes);
+          tma_load_2d(sbase + L::a_off + stage * L::a_bytes, mA, kb * kGemmBK,
+                      t.a_row, fb);
+          const uint32_t bdst = sbase + L::b_off + stage * L::b_bytes;
+          for (int bx = 0; bx < nbox; ++bx)
+            tma_load_2d(bdst + bx * kBoxRows * kGemmBK * 2, mB, kb * kGemmBK,
+                        t.b_row + bx * kBoxRows, fb);
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (*abort_flag) {   // let loads in flight land before smem is freed
+        for (int j = 0; j < STAGES && j < issued; ++j) {
+          int st = stage - 1 - j;
+          uint32_t ph = phase;
+          if (st < 0) {
+            st += STAGES;
+            ph ^= 1;
+          }
+          mbar_drain(bar_full + 8 * st, ph);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      for (int item = blockIdx.x; item < n_items && !*abort_flag;
+           item += gridDim.x) {
+        const Tile t = decode_item<BN>(item, p, n_items_s, nch_s, off_s,
+                                       chunk_pre);
+        if (!mbar_wait(bar_tempty + 8 * acc, acc_phase ^ 1, abort_flag,
+                       KID_GEMM, 2))
+          break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + acc * BN;
+        const uint32_t idesc = idesc_bf16_f32(kGemmBM, t.n_mma);
+        const int nk = t.k / kGemmBK;
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag, KID_GEMM,
+                         3)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = sbase + L::a_off + stage * L::a_bytes;
+          const uint32_t b0 = sbase + L::b_off + stage * L::b_bytes;
+#pragma unroll
+          for (int kk = 0; kk < kGemmBK / 16; ++kk)
+            mma_bf16(d_tmem, sdesc_k128(a0 + kk * 32),
+                     sdesc_k128(b0 + kk * 32), idesc, (kb | kk) != 0);
+          mma_commit(bar_empty + 8 * stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        mma_commit(bar_tfull + 8 * acc);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
+      }
+      // every MMA issued above is complete once this fires
+      mma_commit(bar_final);
+      mbar_drain(bar_final, 0);
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5) ----------------
+    const int ep = warp - 2;          // column group of the store phase
+    const int q = warp & 3;           // TMEM sub-partition this warp may read
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+      const Tile t = decode_item<BN>(item, p, n_items_s, nch_s, off_s,
+                                     chunk_pre);
+      // The four epilogue warps share named barrier 1, so they leave the
+      // loop together: each posts its verdict, all read all four.
+      const bool ok = mbar_wait(bar_tfull + 8 * acc, acc_phase, abort_flag,
+                                KID_GEMM, 4);
+      const bool wok = __all_sync(0xffffffffu, ok);
+      if (lane == 0) ep_ok[ep] = wok ? 1 : 0;
+      named_bar_sync(1, 128);
+      if (!(ep_ok[0] && ep_ok[1] && ep_ok[2] && ep_ok[3])) break;
+      tc_fence_after();
+      void* out = t.shared ? p.out_shared : p.out_routed;
+      const long long ld = t.shared ? p.ld_shared : p.ld_routed;
+      for (int n0 = 0; n0 < t.n_valid; n0 += 32) {
+        uint32_t r[32];
+        tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + n0,
+                  r);
+        tmem_ld_wait();
+        float* srow = stg + (q * 32 + lane) * 33;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) srow[j] = __uint_as_float(r[j]);
+        named_bar_sync(1, 128);
+        const int n = n0 + lane;
+        if (n < t.n_valid) {
+          const size_t row = static_cast<size_t>(t.b_row + n) * ld;
+          if (p.swiglu) {
+            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(out) + row;
+            // H columns wt*64 + ep*16 + [0, 16)
+            uint32_t pk[8];
+#pragma unroll
+            for (int i = 0; i < 16; i += 2) {
+              const int c = ep * 16 + i;
+              const float g0 = stg[c * 33 + lane], u0 = stg[(64 + c) * 33 + lane];
+              const float g1 = stg[(c + 1) * 33 + lane],
+                          u1 = stg[(65 + c) * 33 + lane];
+              pk[i / 2] = pack_bf16x2(silu_f32(g0) * u0, silu_f32(g1) * u1);
+            }
+            uint4* d4 = reinterpret_cast<uint4*>(dst + t.wt * 64 + ep * 16);
+            d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          } else {
+            // Y columns wt*128 + ep*32 + [0, 32), fp32
+            float* dst = static_cast<float*>(out) + row + t.wt * 128 + ep * 32;
+            float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              d4[i] = make_float4(stg[(ep * 32 + 4 * i) * 33 + lane],
+                                  stg[(ep * 32 + 4 * i + 1) * 33 + lane],
+                                  stg[(ep * 32 + 4 * i + 2) * 33 + lane],
+                                  stg[(ep * 32 + 4 * i + 3) * 33 + lane]);
+          }
+        }
+        named_bar_sync(1, 128);
+      }
+      tc_fence_before();
+      mbar_arrive(bar_tempty + 8 * acc);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, L::tmem_cols);
+  }
+}
+
+}  // namespace moe

@@ -1,0 +1,617 @@
+// C ABI of the MoE layer forward (declared in include/moe_b300.h):
+// argument validation, workspace layout, TMA descriptors and kernel
+// launches on the caller's stream.  One translation unit holds every kernel.
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "common.cuh"
+#include "elementwise.cuh"
+#include "gemm.cuh"
+#include "permute.cuh"
+#include "route.cuh"
+#include "moe_b300.h"
+
+using namespace moe;
+
+namespace {
+
+thread_local std::string g_detail;
+thread_local int g_launches = 0;
+
+moe_status fail(moe_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_detail = buf;
+  return st;
+}
+
+#define MOE_CHECK_CUDA(call)                                                 \
+  do {                                                                       \
+    cudaError_t e_ = (call);                                                 \
+    if (e_ != cudaSuccess)                                                   \
+      return fail(MOE_ERR_CUDA, "%s: %s (%s:%d)", #call,                      \
+                  cudaGetErrorString(e_), __FILE__, __LINE__);               \
+  } while (0)
+
+#define MOE_CHECK_LAUNCH()                                                   \
+  do {                                                                       \
+    cudaError_t e_ = cudaGetLastError();                                     \
+    if (e_ != cudaSuccess)                                                   \
+      return fail(MOE_ERR_CUDA, "launch: %s (%s:%d)", cudaGetErrorString(e_), \
+                  __FILE__, __LINE__);                                       \
+    ++g_launches;                                                            \
+  } while (0)
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool init = false;
+  int sm_count = 0;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+template <typename K>
+cudaError_t allow_smem(K kernel, int bytes) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              bytes);
+}
+
+// Per-device one-time set-up: SM count and the dynamic shared-memory limits
+// of the TMA/tcgen05 kernels.
+moe_status device_setup(int* sm_count) {
+  int dev = 0;
+  MOE_CHECK_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kMaxDevices)
+    return fail(MOE_ERR_UNSUPPORTED, "device index %d", dev);
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& di = g_dev[dev];
+  if (!di.init) {
+    MOE_CHECK_CUDA(cudaDeviceGetAttribute(&di.sm_count,
+                                          cudaDevAttrMultiProcessorCount, dev));
+    MOE_CHECK_CUDA(allow_smem(route_tc_kernel, RouteTcSmemLayout::alloc));
+    MOE_CHECK_CUDA(allow_smem(grouped_gemm_kernel<256, 4>,
+                              GemmSmem<256, 4>::alloc));
+    MOE_CHECK_CUDA(allow_smem(grouped_gemm_kernel<32, 8>,
+                              GemmSmem<32, 8>::alloc));
+    di.init = true;
+  }
+  *sm_count = di.sm_count;
+  return MOE_OK;
+}
+
+moe_status get_encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (g_encode == nullptr)
+    return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  return MOE_OK;
+}
+
+// 2-D bf16 K-major operand [rows, cols] (cols contiguous), 128-byte swizzle,
+// box {64, box_rows}; out-of-range rows read as zero.
+moe_status make_map(CUtensorMap* m, const void* ptr, long long rows,
+                    long long cols, int box_rows) {
+  moe_status st = get_encoder();
+  if (st != MOE_OK) return st;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols),
+                        static_cast<cuuint64_t>(rows > 0 ? rows : 1)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                        const_cast<void*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) rows=%lld "
+                "cols=%lld box_rows=%d", static_cast<int>(r), rows, cols,
+                box_rows);
+  return MOE_OK;
+}
+
+size_t elem_size(moe_dtype dt) { return dt == MOE_BF16 ? 2 : 4; }
+
+bool aligned16(const void* p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+inline long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
+inline size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+moe_status check_shape(const moe_shape* s) {
+  if (s == nullptr) return fail(MOE_ERR_INVALID_ARG, "shape is NULL");
+  if (s->dtype != MOE_F32 && s->dtype != MOE_BF16)
+    return fail(MOE_ERR_INVALID_ARG, "dtype %d", static_cast<int>(s->dtype));
+  if (s->T < 0 || s->d <= 0 || s->n_routed <= 0 || s->top_k <= 0 ||
+      s->n_shared < 0 || s->d_ff <= 0)
+    return fail(MOE_ERR_INVALID_ARG, "non-positive size in shape");
+  if (s->d % 128 != 0)
+    return fail(MOE_ERR_UNSUPPORTED, "d=%d must be a multiple of 128", s->d);
+  if (s->d_ff % 64 != 0)
+    return fail(MOE_ERR_UNSUPPORTED, "d_ff=%d must be a multiple of 64",
+                s->d_ff);
+  if (s->top_k > kTopKMax || s->top_k > s->n_routed)
+    return fail(MOE_ERR_UNSUPPORTED, "top_k=%d (max %d, <= n_routed)",
+                s->top_k, kTopKMax);
+  if (s->n_shared > 8)
+    return fail(MOE_ERR_UNSUPPORTED, "n_shared=%d (max 8)", s->n_shared);
+  if (s->dtype == MOE_BF16) {
+    if (s->n_routed > 256 || s->n_routed % 16 != 0)
+      return fail(MOE_ERR_UNSUPPORTED,
+                  "bf16 n_routed=%d must be a multiple of 16, <= 256",
+                  s->n_routed);
+  } else {
+    if (s->n_routed > 1024)
+      return fail(MOE_ERR_UNSUPPORTED, "fp32 n_routed=%d (max 1024)",
+                  s->n_routed);
+    if (static_cast<long long>(s->T) * s->top_k > 65535LL * 4)
+      return fail(MOE_ERR_UNSUPPORTED, "fp32 path: T*top_k too large");
+  }
+  const long long A = static_cast<long long>(s->T) * s->top_k;
+  if (A > (1LL << 31) - 1 || static_cast<long long>(s->T) * s->d > (1LL << 40))
+    return fail(MOE_ERR_UNSUPPORTED, "problem too large");
+  return MOE_OK;
+}
+
+struct WsLayout {
+  size_t route_hist, perm_hist, h_routed, h_shared, total;
+};
+
+WsLayout ws_layout(const moe_shape* s) {
+  WsLayout w;
+  const size_t es = elem_size(s->dtype);
+  const long long nblk = cdiv(s->T, kRouteTile);
+  const long long A = static_cast<long long>(s->T) * s->top_k;
+  size_t off = 0;
+  w.route_hist = off;
+  off = round256(off + static_cast<size_t>(nblk) * s->n_routed * 4);
+  w.perm_hist = off;
+  off = round256(off + static_cast<size_t>(cdiv(s->T, kPermChunk)) *
+                           s->n_routed * 4);
+  w.h_routed = off;
+  off = round256(off + static_cast<size_t>(A) * s->d_ff * es);
+  w.h_shared = off;
+  off = round256(off + static_cast<size_t>(s->T) * s->n_shared * s->d_ff * es);
+  w.total = off;
+  return w;
+}
+
+moe_status check_ws(const moe_shape* s, void* ws, size_t bytes) {
+  const WsLayout w = ws_layout(s);
+  if (ws == nullptr && w.total > 0)
+    return fail(MOE_ERR_WORKSPACE, "workspace is NULL");
+  if (bytes < w.total)
+    return fail(MOE_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", bytes,
+                w.total);
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+    return fail(MOE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  return MOE_OK;
+}
+
+#define NEED_PTR(p)                                                     \
+  do {                                                                  \
+    if ((p) == nullptr) return fail(MOE_ERR_INVALID_ARG, #p " is NULL"); \
+    if (!aligned16(p))                                                  \
+      return fail(MOE_ERR_INVALID_ARG, #p " not 16-byte aligned");      \
+  } while (0)
+
+inline cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+// grid of the fp32 FFN kernels: 64 columns x 4 rows per 256-thread block
+inline dim3 grid2(long long cols, long long rows) {
+  return dim3(static_cast<unsigned>(cdiv(cols, 64)),
+              static_cast<unsigned>(cdiv(rows, 4)));
+}
+
+}  // namespace
+
+namespace {
+
+template <int BN, int STAGES>
+moe_status launch_gemm(const CUtensorMap& a_r, const CUtensorMap& b_r,
+                       const CUtensorMap& a_s, const CUtensorMap& b_s,
+                       const GemmParams& p, int sms, cudaStream_t cs) {
+  long long items = 0;
+  if (p.shared_rows > 0)
+    items += cdiv(p.shared_rows, BN) * (p.w_rows_shared / kGemmBM);
+  if (p.n_groups > 0)
+    items += (cdiv(p.max_routed_rows, BN) + p.n_groups) *
+             (p.w_rows_routed / kGemmBM);
+  if (items == 0) return MOE_OK;
+  const int grid = static_cast<int>(items < sms ? items : sms);
+  grouped_gemm_kernel<BN, STAGES><<<grid, 192, GemmSmem<BN, STAGES>::alloc,
+                                    cs>>>(a_r, b_r, a_s, b_s, p);
+  MOE_CHECK_LAUNCH();
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_workspace_size(const moe_shape* shape, size_t* bytes) {
+  moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if (bytes == nullptr) return fail(MOE_ERR_INVALID_ARG, "bytes is NULL");
+  *bytes = ws_layout(shape).total;
+  return MOE_OK;
+}
+
+moe_status moe_pack_weights(const moe_shape* s, const void* w_gate,
+                            const void* w_up, const void* ws_gate,
+                            const void* ws_up, const void* ws_down,
+                            void* w_gu_packed, void* ws_gu_packed,
+                            void* ws_down_packed, void* stream) {
+  g_launches = 0;
+  moe_status st = check_shape(s);
+  if (st != MOE_OK) return st;
+  NEED_PTR(w_gate);
+  NEED_PTR(w_up);
+  NEED_PTR(w_gu_packed);
+  if (s->n_shared > 0) {
+    NEED_PTR(ws_gate);
+    NEED_PTR(ws_up);
+    NEED_PTR(ws_down);
+    NEED_PTR(ws_gu_packed);
+    NEED_PTR(ws_down_packed);
+  }
+  const int es = static_cast<int>(elem_size(s->dtype));
+  const int rvec = s->d * es / 16;
+  cudaStream_t cs = as_stream(stream);
+  const long long rows_r = 2LL * s->n_routed * s->d_ff;
+  pack_gate_up_kernel<<<static_cast<int>(rows_r < 65536 ? rows_r : 65536), 128,
+                        0, cs>>>(
+      static_cast<const uint4*>(w_gate), static_cast<const uint4*>(w_up),
+      s->n_routed, 1, s->d_ff, rvec, static_cast<uint4*>(w_gu_packed));
+  MOE_CHECK_LAUNCH();
+  if (s->n_shared > 0) {
+    const long long rows_s = 2LL * s->n_shared * s->d_ff;
+    pack_gate_up_kernel<<<static_cast<int>(rows_s < 65536 ? rows_s : 65536),
+                          128, 0, cs>>>(
+        static_cast<const uint4*>(ws_gate), static_cast<const uint4*>(ws_up), 1,
+        s->n_shared, s->d_ff, rvec, static_cast<uint4*>(ws_gu_packed));
+    MOE_CHECK_LAUNCH();
+    const long long rows_d = static_cast<long long>(s->n_shared) * s->d;
+    pack_shared_down_kernel<<<static_cast<int>(rows_d < 65536 ? rows_d : 65536),
+                              128, 0, cs>>>(
+        static_cast<const uint4*>(ws_down), s->n_shared, s->d,
+        s->d_ff * es / 16, static_cast<uint4*>(ws_down_packed));
+    MOE_CHECK_LAUNCH();
+  }
+  return MOE_OK;
+}
+
+moe_status moe_route(const moe_shape* s, const void* u, const void* centroids,
+                     const float* bias, int32_t* topk_idx, float* topk_gate,
+                     int32_t* counts, void* ws, size_t ws_bytes, void* stream) {
+  g_launches = 0;
+  moe_status st = check_shape(s);
+  if (st != MOE_OK) return st;
+  if (s->T > 0) {
+    NEED_PTR(u);
+    NEED_PTR(topk_idx);
+    NEED_PTR(topk_gate);
+  }
+  NEED_PTR(centroids);
+  NEED_PTR(bias);
+  NEED_PTR(counts);
+  st = check_ws(s, ws, ws_bytes);
+  if (st != MOE_OK) return st;
+  int sms = 0;
+  st = device_setup(&sms);
+  if (st != MOE_OK) return st;
+  const WsLayout w = ws_layout(s);
+  int* hist = reinterpret_cast<int*>(static_cast<char*>(ws) + w.route_hist);
+  const int nblk = static_cast<int>(cdiv(s->T, kRouteTile));
+  cudaStream_t cs = as_stream(stream);
+  if (nblk > 0) {
+    if (s->dtype == MOE_BF16) {
+      CUtensorMap tm_u, tm_e;
+      st = make_map(&tm_u, u, s->T, s->d, kRouteTile);
+      if (st != MOE_OK) return st;
+      st = make_map(&tm_e, centroids, s->n_routed, s->d, s->n_routed);
+      if (st != MOE_OK) return st;
+      route_tc_kernel<<<nblk, 128, RouteTcSmemLayout::alloc, cs>>>(
+          tm_u, tm_e, bias, s->T, s->d, s->n_routed, s->top_k, topk_idx,
+          topk_gate, hist);
+      MOE_CHECK_LAUNCH();
+    } else {
+      route_f32_kernel<<<nblk, 128, 4 * s->n_routed * sizeof(float), cs>>>(
+          static_cast<const float*>(u), static_cast<const float*>(centroids),
+          bias, s->T, s->d, s->n_routed, s->top_k, topk_idx, topk_gate, hist);
+      MOE_CHECK_LAUNCH();
+    }
+  }
+  route_hist_reduce_kernel<<<static_cast<int>(cdiv(s->n_routed, 256)), 256, 0,
+                             cs>>>(hist, nblk, s->n_routed, counts);
+  MOE_CHECK_LAUNCH();
+  return MOE_OK;
+}
+
+moe_status moe_permute(const moe_shape* s, const void* u,
+                       const int32_t* topk_idx, const int32_t* counts,
+                       int32_t* offsets, int32_t* perm, int32_t* inv,
+                       void* x_perm, void* ws, size_t ws_bytes, void* stream) {
+  g_launches = 0;
+  moe_status st = check_shape(s);
+  if (st != MOE_OK) return st;
+  if (s->T > 0) {
+    NEED_PTR(u);
+    NEED_PTR(topk_idx);
+    NEED_PTR(perm);
+    NEED_PTR(inv);
+    NEED_PTR(x_perm);
+  }
+  NEED_PTR(counts);
+  NEED_PTR(offsets);
+  st = check_ws(s, ws, ws_bytes);
+  if (st != MOE_OK) return st;
+  const WsLayout w = ws_layout(s);
+  int* chist = reinterpret_cast<int*>(static_cast<char*>(ws) + w.perm_hist);
+  const int nch = static_cast<int>(cdiv(s->T, kPermChunk));
+  cudaStream_t cs = as_stream(stream);
+  if (nch > 0) {
+    permute_chunk_hist_kernel<<<nch, 256, 0, cs>>>(topk_idx, s->T, s->top_k,
+                                                   s->n_routed, chist);
+    MOE_CHECK_LAUNCH();
+  }
+  permute_slots_kernel<<<nch > 0 ? nch : 1, 256, 0, cs>>>(
+      topk_idx, counts, chist, s->T, s->top_k, s->n_routed, offsets, perm, inv);
+  MOE_CHECK_LAUNCH();
+  if (s->T > 0) {
+    const int nvec = static_cast<int>(s->d * elem_size(s->dtype) / 16);
+    int sms = 0;
+    st = device_setup(&sms);
+    if (st != MOE_OK) return st;
+    const long long want = cdiv(s->T, 8);
+    const int grid = static_cast<int>(want < sms * 8LL ? want : sms * 8LL);
+    permute_gather_kernel<<<grid, 256, 0, cs>>>(
+        static_cast<const uint4*>(u), inv, s->T, s->top_k, nvec,
+        static_cast<long long>(s->T) * s->top_k, static_cast<uint4*>(x_perm));
+    MOE_CHECK_LAUNCH();
+  }
+  return MOE_OK;
+}
+
+
+moe_status moe_expert_ffn(const moe_shape* s, const void* x_perm,
+                          const int32_t* offsets, const void* w_gu_packed,
+                          const void* w_down, const void* u,
+                          const void* ws_gu_packed, const void* ws_down_packed,
+                          void* y_perm, void* y_shared, void* ws,
+                          size_t ws_bytes, void* stream) {
+  g_launches = 0;
+  moe_status st = check_shape(s);
+  if (st != MOE_OK) return st;
+  NEED_PTR(offsets);
+  NEED_PTR(w_gu_packed);
+  NEED_PTR(w_down);
+  if (s->T > 0) {
+    NEED_PTR(x_perm);
+    NEED_PTR(y_perm);
+  }
+  const bool has_shared = s->n_shared > 0 && s->T > 0;
+  if (has_shared) {
+    NEED_PTR(u);
+    NEED_PTR(ws_gu_packed);
+    NEED_PTR(ws_down_packed);
+    NEED_PTR(y_shared);
+  }
+  st = check_ws(s, ws, ws_bytes);
+  if (st != MOE_OK) return st;
+  if (s->T == 0) return MOE_OK;
+  int sms = 0;
+  st = device_setup(&sms);
+  if (st != MOE_OK) return st;
+  const WsLayout w = ws_layout(s);
+  void* h_r = static_cast<char*>(ws) + w.h_routed;
+  void* h_s = static_cast<char*>(ws) + w.h_shared;
+  const long long A = static_cast<long long>(s->T) * s->top_k;
+  const int N = s->n_routed, d = s->d, I = s->d_ff, SI = s->n_shared * s->d_ff;
+  cudaStream_t cs = as_stream(stream);
+
+  if (s->dtype == MOE_F32) {
+    const float* xp = static_cast<const float*>(x_perm);
+    float* hr = static_cast<float*>(h_r);
+    float* hs = static_cast<float*>(h_s);
+    ffn_f32_gate_up_kernel<<<grid2(I, A), 256, 0, cs>>>(
+        xp, static_cast<int>(A), offsets, N,
+        static_cast<const float*>(w_gu_packed), I, d, hr);
+    MOE_CHECK_LAUNCH();
+    ffn_f32_down_kernel<<<grid2(d, A), 256, 0, cs>>>(
+        hr, static_cast<int>(A), offsets, N, static_cast<const float*>(w_down),
+        I, d, static_cast<float*>(y_perm));
+    MOE_CHECK_LAUNCH();
+    if (has_shared) {
+      ffn_f32_gate_up_kernel<<<grid2(SI, s->T), 256, 0, cs>>>(
+          static_cast<const float*>(u), s->T, nullptr, 1,
+          static_cast<const float*>(ws_gu_packed), SI, d, hs);
+      MOE_CHECK_LAUNCH();
+      ffn_f32_down_kernel<<<grid2(d, s->T), 256, 0, cs>>>(
+          hs, s->T, nullptr, 1, static_cast<const float*>(ws_down_packed), SI,
+          d, static_cast<float*>(y_shared));
+      MOE_CHECK_LAUNCH();
+    }
+    return MOE_OK;
+  }
+
+  // bf16: tcgen05 grouped GEMMs.  Small average group size -> 32-token
+  // chunks and a deeper ring (weight streaming); else 256-token chunks.
+  const bool small = A <= 48LL * N;
+  CUtensorMap a_r, b_r, a_s, b_s;
+  const int box = kBoxRows;
+  GemmParams p{};
+  // pass 1: gate/up + SwiGLU -> H
+  if ((st = make_map(&a_r, w_gu_packed, 2LL * N * I, d, kGemmBM)) != MOE_OK)
+    return st;
+  if ((st = make_map(&b_r, x_perm, A, d, box)) != MOE_OK) return st;
+  if (has_shared) {
+    if ((st = make_map(&a_s, ws_gu_packed, 2LL * SI, d, kGemmBM)) != MOE_OK)
+      return st;
+    if ((st = make_map(&b_s, u, s->T, d, box)) != MOE_OK) return st;
+  } else {
+    a_s = a_r;
+    b_s = b_r;
+  }
+  p.offsets = offsets;
+  p.n_groups = N;
+  p.w_rows_routed = 2 * I;
+  p.k_routed = d;
+  p.max_routed_rows = A;
+  p.shared_rows = has_shared ? s->T : 0;
+  p.w_rows_shared = 2 * SI;
+  p.k_shared = d;
+  p.out_routed = h_r;
+  p.ld_routed = I;
+  p.out_shared = h_s;
+  p.ld_shared = SI;
+  p.swiglu = 1;
+  st = small ? launch_gemm<32, 8>(a_r, b_r, a_s, b_s, p, sms, cs)
+             : launch_gemm<256, 4>(a_r, b_r, a_s, b_s, p, sms, cs);
+  if (st != MOE_OK) return st;
+  // pass 2: down -> y
+  if ((st = make_map(&a_r, w_down, static_cast<long long>(N) * d, I,
+                     kGemmBM)) != MOE_OK)
+    return st;
+  if ((st = make_map(&b_r, h_r, A, I, box)) != MOE_OK) return st;
+  if (has_shared) {
+    if ((st = make_map(&a_s, ws_down_packed, d, SI, kGemmBM)) != MOE_OK)
+      return st;
+    if ((st = make_map(&b_s, h_s, s->T, SI, box)) != MOE_OK) return st;
+  } else {
+    a_s = a_r;
+    b_s = b_r;
+  }
+  p.w_rows_routed = d;
+  p.k_routed = I;
+  p.w_rows_shared = d;
+  p.k_shared = SI;
+  p.out_routed = y_perm;
+  p.ld_routed = d;
+  p.out_shared = y_shared;
+  p.ld_shared = d;
+  p.swiglu = 0;
+  const int before = g_launches;
+  st = small ? launch_gemm<32, 8>(a_r, b_r, a_s, b_s, p, sms, cs)
+             : launch_gemm<256, 4>(a_r, b_r, a_s, b_s, p, sms, cs);
+  (void)before;
+  return st;
+}
+
+moe_status moe_combine(const moe_shape* s, const void* u, const void* y_perm,
+                       const void* y_shared, const int32_t* inv,
+                       const float* topk_gate, void* h, moe_dtype h_dtype,
+                       void* stream) {
+  g_launches = 0;
+  moe_status st = check_shape(s);
+  if (st != MOE_OK) return st;
+  if (h_dtype != MOE_F32 && h_dtype != MOE_BF16)
+    return fail(MOE_ERR_INVALID_ARG, "h_dtype %d", static_cast<int>(h_dtype));
+  if (s->T == 0) return MOE_OK;
+  NEED_PTR(u);
+  NEED_PTR(y_perm);
+  NEED_PTR(inv);
+  NEED_PTR(topk_gate);
+  NEED_PTR(h);
+  if (s->n_shared > 0) NEED_PTR(y_shared);
+  const void* ys = s->n_shared > 0 ? y_shared : nullptr;
+  const long long A = static_cast<long long>(s->T) * s->top_k;
+  cudaStream_t cs = as_stream(stream);
+  const float* y = static_cast<const float*>(y_perm);
+  const float* z = static_cast<const float*>(ys);
+  if (s->dtype == MOE_BF16) {
+    const __nv_bfloat16* a = static_cast<const __nv_bfloat16*>(u);
+    if (h_dtype == MOE_F32)
+      combine_kernel<__nv_bfloat16, float><<<s->T, 128, 0, cs>>>(
+          a, y, z, inv, topk_gate, s->T, s->d, s->top_k, A,
+          static_cast<float*>(h));
+    else
+      combine_kernel<__nv_bfloat16, __nv_bfloat16><<<s->T, 128, 0, cs>>>(
+          a, y, z, inv, topk_gate, s->T, s->d, s->top_k, A,
+          static_cast<__nv_bfloat16*>(h));
+  } else {
+    const float* a = static_cast<const float*>(u);
+    if (h_dtype == MOE_F32)
+      combine_kernel<float, float><<<s->T, 128, 0, cs>>>(
+          a, y, z, inv, topk_gate, s->T, s->d, s->top_k, A,
+          static_cast<float*>(h));
+    else
+      combine_kernel<float, __nv_bfloat16><<<s->T, 128, 0, cs>>>(
+          a, y, z, inv, topk_gate, s->T, s->d, s->top_k, A,
+          static_cast<__nv_bfloat16*>(h));
+  }
+  MOE_CHECK_LAUNCH();
+  return MOE_OK;
+}
+
+moe_status moe_update_bias(int n_routed, const int32_t* counts,
+                           long long total_assign, float gamma, float* bias,
+                           void* stream) {
+  g_launches = 0;
+  if (n_routed <= 0 || total_assign < 0)
+    return fail(MOE_ERR_INVALID_ARG, "n_routed=%d total_assign=%lld", n_routed,
+                total_assign);
+  if (!(gamma >= 0.f) || gamma > 1e30f)
+    return fail(MOE_ERR_INVALID_ARG, "gamma must be finite and >= 0");
+  NEED_PTR(counts);
+  NEED_PTR(bias);
+  update_bias_kernel<<<static_cast<int>(cdiv(n_routed, 256)), 256, 0,
+                       as_stream(stream)>>>(counts, n_routed, total_assign,
+                                            gamma, bias);
+  MOE_CHECK_LAUNCH();
+  return MOE_OK;
+}
+
+moe_status moe_get_device_error(void* stream) {
+  MOE_CHECK_CUDA(cudaStreamSynchronize(as_stream(stream)));
+  unsigned word = 0, info[2] = {0, 0};
+  MOE_CHECK_CUDA(cudaMemcpyFromSymbol(&word, g_err_word, sizeof(word)));
+  if (word == 0) return MOE_OK;
+  MOE_CHECK_CUDA(cudaMemcpyFromSymbol(info, g_err_info, sizeof(info)));
+  const unsigned zero[3] = {0, 0, 0};
+  MOE_CHECK_CUDA(cudaMemcpyToSymbol(g_err_word, zero, sizeof(unsigned)));
+  MOE_CHECK_CUDA(cudaMemcpyToSymbol(g_err_info, zero, 2 * sizeof(unsigned)));
+  if (word & ERR_TIMEOUT)
+    return fail(MOE_ERR_TIMEOUT, "device wait timed out (kernel %u, site %u)",
+                info[0], info[1]);
+  return fail(MOE_ERR_DEVICE_CHECK, "device bounds check (kernel %u, at %u)",
+              info[0], info[1]);
+}
+
+const char* moe_status_string(moe_status st) {
+  switch (st) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape";
+    case MOE_ERR_WORKSPACE: return "workspace missing or too small";
+    case MOE_ERR_CUDA: return "CUDA runtime error";
+    case MOE_ERR_TIMEOUT: return "device pipeline wait timed out";
+    case MOE_ERR_DEVICE_CHECK: return "device bounds check failed";
+  }
+  return "unknown status";
+}
+
+const char* moe_last_error_detail(void) { return g_detail.c_str(); }
+
+int moe_last_launch_count(void) { return g_launches; }
+
+}  // extern "C"

@@ -1,0 +1,120 @@
+"""DeepSeekMoE layer forward on one B300 through the C ABI.
+
+``MoELayer`` owns the (packed) weights and the per-batch buffers, all torch
+device tensors, and runs one forward as four library calls on one stream:
+
+    route -> permute -> expert_ffn -> combine   [-> update_bias]
+
+h = u + sum_s FFN^(s)(u) + sum_i g_i FFN^(r)_i(u)
+("【推理llm論文精讀】DeepSeek V3技術論文", section 2.2, FFN-output equation),
+with the auxiliary-loss-free bias step after the batch when asked.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import Dict, Optional
+
+import torch
+
+from . import _lib
+
+
+@dataclass
+class Buffers:
+    T: int
+    topk_idx: torch.Tensor
+    topk_gate: torch.Tensor
+    counts: torch.Tensor
+    offsets: torch.Tensor
+    perm: torch.Tensor
+    inv: torch.Tensor
+    x_perm: torch.Tensor
+    y_perm: torch.Tensor
+    y_shared: Optional[torch.Tensor]
+    h: torch.Tensor
+    workspace: torch.Tensor
+
+
+class MoELayer:
+    def __init__(self, E: torch.Tensor, bias: torch.Tensor,
+                 w_gate: torch.Tensor, w_up: torch.Tensor, w_down: torch.Tensor,
+                 ws_gate: Optional[torch.Tensor] = None,
+                 ws_up: Optional[torch.Tensor] = None,
+                 ws_down: Optional[torch.Tensor] = None, top_k: int = 8,
+                 h_dtype: torch.dtype = torch.float32, stream=None):
+        if not E.is_cuda:
+            raise ValueError("MoELayer needs CUDA tensors")
+        self.dtype = E.dtype
+        self.N, self.d = E.shape
+        self.I = w_gate.shape[1]
+        self.S = 0 if ws_gate is None else ws_gate.shape[0]
+        self.K = int(top_k)
+        self.h_dtype = h_dtype
+        self.E, self.bias, self.w_down = E, bias, w_down
+        dev, dt = E.device, E.dtype
+        self.w_gu = torch.empty((self.N, 2 * self.I, self.d), dtype=dt,
+                                device=dev)
+        if self.S:
+            self.ws_gu = torch.empty((2 * self.S * self.I, self.d), dtype=dt,
+                                     device=dev)
+            self.ws_down = torch.empty((self.d, self.S * self.I), dtype=dt,
+                                       device=dev)
+        else:
+            self.ws_gu = self.ws_down = None
+        _lib.pack_weights(self.shape(1), w_gate, w_up, ws_gate, ws_up, ws_down,
+                          self.w_gu, self.ws_gu, self.ws_down, stream)
+        self._bufs: Dict[int, Buffers] = {}
+
+    def shape(self, T: int) -> _lib.MoeShape:
+        return _lib.make_shape(T, self.d, self.N, self.K, self.S, self.I,
+                               self.dtype)
+
+    def buffers(self, T: int) -> Buffers:
+        b = self._bufs.get(T)
+        if b is not None:
+            return b
+        dev, dt, K = self.E.device, self.dtype, self.K
+        A = T * K
+        i32 = dict(dtype=torch.int32, device=dev)
+        ws = _lib.workspace_size(self.shape(T))
+        b = Buffers(
+            T=T,
+            topk_idx=torch.empty((T, K), **i32),
+            topk_gate=torch.empty((T, K), dtype=torch.float32, device=dev),
+            counts=torch.empty((self.N,), **i32),
+            offsets=torch.empty((self.N + 1,), **i32),
+            perm=torch.empty((max(A, 1),), **i32),
+            inv=torch.empty((T, K), **i32),
+            x_perm=torch.empty((max(A, 1), self.d), dtype=dt, device=dev),
+            y_perm=torch.empty((max(A, 1), self.d), dtype=torch.float32,
+                               device=dev),
+            y_shared=(torch.empty((T, self.d), dtype=torch.float32,
+                                  device=dev) if self.S else None),
+            h=torch.empty((T, self.d), dtype=self.h_dtype, device=dev),
+            workspace=torch.empty((max(ws, 256),), dtype=torch.uint8,
+                                  device=dev),
+        )
+        self._bufs[T] = b
+        return b
+
+    def forward(self, u: torch.Tensor, update_bias: bool = False,
+                gamma: float = 1e-3, stream=None) -> torch.Tensor:
+        """h for u[T, d]; the result lives in this layer's buffer for T."""
+        T = u.shape[0]
+        b = self.buffers(T)
+        sh = self.shape(T)
+        _lib.route(sh, u, self.E, self.bias, b.topk_idx, b.topk_gate, b.counts,
+                   b.workspace, stream)
+        _lib.permute(sh, u, b.topk_idx, b.counts, b.offsets, b.perm, b.inv,
+                     b.x_perm, b.workspace, stream)
+        _lib.expert_ffn(sh, b.x_perm, b.offsets, self.w_gu, self.w_down, u,
+                        self.ws_gu, self.ws_down, b.y_perm, b.y_shared,
+                        b.workspace, stream)
+        _lib.combine(sh, u, b.y_perm, b.y_shared, b.inv, b.topk_gate, b.h,
+                     stream)
+        if update_bias:
+            _lib.update_bias(self.N, b.counts, T * self.K, gamma, self.bias,
+                             stream)
+        return b.h
+
+    __call__ = forward

@@ -1,0 +1,131 @@
+"""Host-only checks of the C ABI (no GPU): the library loads, exports every
+function the header declares, and rejects bad arguments with a status code
+before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_b300.h")
+
+
+@pytest.fixture(scope="module")
+def moe():
+    from mixture_experts_layer_gemms_b300 import build
+    build.build()
+    import mixture_experts_layer_gemms_b300 as m
+    return m
+
+
+def declared_functions():
+    txt = open(HEADER).read()
+    return sorted(set(re.findall(r"MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(", txt)))
+
+
+def test_header_declares_the_calls():
+    names = declared_functions()
+    for core in ("moe_route", "moe_permute", "moe_expert_ffn", "moe_combine",
+                 "moe_update_bias"):
+        assert core in names
+
+
+def test_library_exports_every_declared_symbol(moe):
+    lib = ctypes.CDLL(moe.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+    assert set(declared_functions()) == set(moe.EXPORTED)
+
+
+def _shape(moe, **kw):
+    base = dict(T=64, d=256, n_routed=16, top_k=4, n_shared=1, d_ff=128,
+                dtype=moe.MOE_F32)
+    base.update(kw)
+    return moe.MoeShape(*[base[k] for k in ("T", "d", "n_routed", "top_k",
+                                            "n_shared", "d_ff", "dtype")])
+
+
+def _ws(moe, shape):
+    n = ctypes.c_size_t()
+    st = moe.LIB.moe_workspace_size(ctypes.byref(shape), ctypes.byref(n))
+    return st, n.value
+
+
+def test_workspace_size(moe):
+    st, n = _ws(moe, _shape(moe))
+    assert st == 0 and n > 0 and n % 256 == 0
+    # T*K*I elements of H plus histograms, monotone in T
+    st2, n2 = _ws(moe, _shape(moe, T=128))
+    assert st2 == 0 and n2 > n
+    st0, n0 = _ws(moe, _shape(moe, T=0))
+    assert st0 == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d=200), 2),                 # d % 128
+    (dict(d_ff=100), 2),              # d_ff % 64
+    (dict(top_k=17, n_routed=32), 2),
+    (dict(top_k=20), 2),              # > n_routed
+    (dict(n_shared=9), 2),
+    (dict(dtype=1, n_routed=24), 2),  # bf16 needs n_routed % 16 == 0
+    (dict(dtype=1, n_routed=512), 2),
+    (dict(T=-1), 1),
+    (dict(top_k=0), 1),
+    (dict(dtype=7), 1),
+])
+def test_bad_shapes_rejected(moe, kw, code):
+    st, _ = _ws(moe, _shape(moe, **kw))
+    assert st == code
+    assert moe.LIB.moe_status_string(st)
+    assert moe.LIB.moe_last_error_detail()
+
+
+def test_null_and_misaligned_pointers(moe):
+    sh = _shape(moe)
+    _, n = _ws(moe, sh)
+    P = ctypes.c_void_p
+    ws = P(4096)          # never dereferenced: validation fails first
+    st = moe.LIB.moe_route(ctypes.byref(sh), None, P(256), P(512), P(768),
+                           P(1024), P(1280), ws, n, None)
+    assert st == 1
+    st = moe.LIB.moe_route(ctypes.byref(sh), P(8), P(256), P(512), P(768),
+                           P(1024), P(1280), ws, n, None)   # misaligned u
+    assert st == 1
+    assert b"aligned" in moe.LIB.moe_last_error_detail()
+
+
+def test_workspace_too_small(moe):
+    sh = _shape(moe)
+    _, n = _ws(moe, sh)
+    P = ctypes.c_void_p
+    st = moe.LIB.moe_permute(ctypes.byref(sh), P(256), P(512), P(768),
+                             P(1024), P(1280), P(1536), P(1792), P(4096),
+                             n - 256, None)
+    assert st == 3
+    st = moe.LIB.moe_route(ctypes.byref(sh), P(256), P(512), P(768), P(1024),
+                           P(1280), P(1536), None, n, None)
+    assert st == 3
+
+
+def test_update_bias_validation(moe):
+    P = ctypes.c_void_p
+    assert moe.LIB.moe_update_bias(0, P(256), 8, ctypes.c_float(1e-3), P(512),
+                                   None) == 1
+    assert moe.LIB.moe_update_bias(4, None, 8, ctypes.c_float(1e-3), P(512),
+                                   None) == 1
+    assert moe.LIB.moe_update_bias(4, P(256), 8, ctypes.c_float(float("nan")),
+                                   P(512), None) == 1
+
+
+def test_combine_bad_dtype(moe):
+    sh = _shape(moe)
+    P = ctypes.c_void_p
+    st = moe.LIB.moe_combine(ctypes.byref(sh), P(256), P(512), P(768),
+                             P(1024), P(1280), P(1536), 5, None)
+    assert st == 1
+
+
+def test_status_strings(moe):
+    for code in range(7):
+        assert moe.LIB.moe_status_string(code)

@@ -164,6 +164,33 @@ MOE_API const char* moe_last_error_detail(void);
  * issued (for launch accounting).                                         */
 MOE_API int moe_last_launch_count(void);
 
+/* moe_route without a workspace, for callers that cannot allocate device
+ * memory at the point of the call: for example a plugin inside an inference
+ * engine that is handed only its input and output buffers and may not
+ * allocate while the engine runs (cudaMalloc can synchronise the device and
+ * break the engine's memory plan), or code running where allocating CUDA
+ * calls are not allowed at all.  The layer equations have no counterpart of
+ * this call; it exists only for such callers.
+ *
+ * Arguments and results are those of moe_route (same kernels).  The router's
+ * per-block histograms go to a library-owned array in device memory of
+ * MOE_ROUTE_NOALLOC_MAX_ENTRIES int32 (1 MiB), which every GPU that loads
+ * the library holds until the process exits.  A call needs
+ * ceil(T/128) * n_routed entries (for example T up to 131072 tokens with 256
+ * experts); larger shapes return MOE_ERR_UNSUPPORTED and launch nothing.
+ * The call allocates nothing (no cudaMalloc, no cudaFree).  Its first call
+ * on a device looks up that array's device address (cudaGetSymbolAddress)
+ * with the device current; make that first call before any stream capture.
+ * All calls share the one array and it keeps the last call's contents:
+ * each call writes every entry it later reads, so nothing needs clearing,
+ * but calls that overlap on the GPU (other streams, other threads) race on
+ * it and must be serialised by the caller.                                */
+#define MOE_ROUTE_NOALLOC_MAX_ENTRIES (1 << 18)
+MOE_API moe_status moe_route_noalloc(const moe_shape* shape, const void* u,
+                                     const void* centroids, const float* bias,
+                                     int32_t* topk_idx, float* topk_gate,
+                                     int32_t* counts, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -2,13 +2,28 @@
 
 Calls (same names as the C ABI without the ``moe_`` prefix): ``route``,
 ``permute``, ``expert_ffn``, ``combine``, ``update_bias``, plus
-``pack_weights``, ``workspace_size`` and ``get_device_error``.  ``MoELayer``
-chains them for one forward.  Importing fails if ``libmoe_b300.so`` has not
-been built (``python -m mixture_experts_layer_gemms_b300.build``).
+``pack_weights``, ``workspace_size``, ``get_device_error`` and
+``route_noalloc``.  ``MoELayer`` chains them for one forward.
+
+The shared library is loaded on first use of any of these names; if
+``libmoe_b300.so`` has not been built
+(``python -m mixture_experts_layer_gemms_b300.build``) that use raises
+ImportError -- there is no fallback.
 """
-from ._lib import (  # noqa: F401
-    EXPORTED, LIB, LIB_PATH, MOE_BF16, MOE_F32, MoEError, MoeShape, combine,
-    expert_ffn, get_device_error, last_launch_count, make_shape, pack_weights,
-    permute, route, update_bias, workspace_size,
-)
-from .layer import Buffers, MoELayer  # noqa: F401
+from importlib import import_module
+
+_FROM_LIB = ("EXPORTED", "LIB", "LIB_PATH", "MOE_BF16", "MOE_F32", "MoEError",
+             "MoeShape", "combine", "expert_ffn", "get_device_error",
+             "last_launch_count", "make_shape", "pack_weights", "permute",
+             "route", "route_noalloc", "update_bias", "workspace_size")
+_FROM_LAYER = ("Buffers", "MoELayer")
+
+__all__ = list(_FROM_LIB + _FROM_LAYER)
+
+
+def __getattr__(name):
+    if name in _FROM_LIB:
+        return getattr(import_module("._lib", __name__), name)
+    if name in _FROM_LAYER:
+        return getattr(import_module(".layer", __name__), name)
+    raise AttributeError(name)

@@ -25,7 +25,8 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 EXPORTED = ("moe_workspace_size", "moe_pack_weights", "moe_route",
             "moe_permute", "moe_expert_ffn", "moe_combine", "moe_update_bias",
             "moe_get_device_error", "moe_status_string",
-            "moe_last_error_detail", "moe_last_launch_count")
+            "moe_last_error_detail", "moe_last_launch_count",
+            "moe_route_noalloc")
 
 
 class MoEError(RuntimeError):
@@ -61,6 +62,7 @@ def _load() -> ctypes.CDLL:
         "moe_status_string": [I],
         "moe_last_error_detail": [],
         "moe_last_launch_count": [],
+        "moe_route_noalloc": [SP, P, P, P, P, P, P, V],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -133,6 +135,16 @@ def route(shape, u, centroids, bias, topk_idx, topk_gate, counts, workspace,
                          _ptr(counts), _ptr(workspace),
                          workspace.numel() * workspace.element_size(),
                          _stream(stream)), "moe_route")
+
+
+def route_noalloc(shape, u, centroids, bias, topk_idx, topk_gate, counts,
+                  stream=None) -> None:
+    """moe_route without a workspace (library-owned 1 MiB scratch); see
+    include/moe_b300.h for who needs it and its limits."""
+    _check(LIB.moe_route_noalloc(ctypes.byref(shape), _ptr(u),
+                                 _ptr(centroids), _ptr(bias), _ptr(topk_idx),
+                                 _ptr(topk_gate), _ptr(counts),
+                                 _stream(stream)), "moe_route_noalloc")
 
 
 def permute(shape, u, topk_idx, counts, offsets, perm, inv, x_perm, workspace,

@@ -615,3 +615,96 @@ const char* moe_last_error_detail(void) { return g_detail.c_str(); }
 int moe_last_launch_count(void) { return g_launches; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Workspace-free routing.  The per-block histograms of the router live in
+// this file-scope device array instead of the caller's workspace.  Host code
+// must not pass `g_route_noalloc_scratch` itself to a kernel: on the host
+// that name is a stand-in, not a device address.  The device address is
+// looked up once per device (cudaGetSymbolAddress, with that device current)
+// and cached.
+static __device__ __align__(256) int
+    g_route_noalloc_scratch[MOE_ROUTE_NOALLOC_MAX_ENTRIES];
+
+namespace {
+int* g_noalloc_ptr[kMaxDevices] = {nullptr};
+std::mutex g_noalloc_mu;
+
+moe_status noalloc_scratch(int** out) {
+  int dev = 0;
+  MOE_CHECK_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kMaxDevices)
+    return fail(MOE_ERR_UNSUPPORTED, "device index %d", dev);
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_route_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr)
+      return fail(MOE_ERR_CUDA, "cudaGetSymbolAddress(route scratch): %s",
+                  cudaGetErrorString(e));
+    g_noalloc_ptr[dev] = static_cast<int*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return MOE_OK;
+}
+}  // namespace
+
+extern "C" {
+
+moe_status moe_route_noalloc(const moe_shape* s, const void* u,
+                             const void* centroids, const float* bias,
+                             int32_t* topk_idx, float* topk_gate,
+                             int32_t* counts, void* stream) {
+  g_launches = 0;
+  moe_status st = check_shape(s);
+  if (st != MOE_OK) return st;
+  if (s->T > 0) {
+    NEED_PTR(u);
+    NEED_PTR(topk_idx);
+    NEED_PTR(topk_gate);
+  }
+  NEED_PTR(centroids);
+  NEED_PTR(bias);
+  NEED_PTR(counts);
+  const long long nblk = cdiv(s->T, kRouteTile);
+  const long long need = nblk * s->n_routed;
+  if (need > MOE_ROUTE_NOALLOC_MAX_ENTRIES)
+    return fail(MOE_ERR_UNSUPPORTED,
+                "moe_route_noalloc: ceil(T/128)*n_routed = %lld histogram "
+                "entries exceeds the static scratch of %d; use moe_route "
+                "with a workspace",
+                need, MOE_ROUTE_NOALLOC_MAX_ENTRIES);
+  int sms = 0;
+  st = device_setup(&sms);
+  if (st != MOE_OK) return st;
+  int* hist = nullptr;
+  st = noalloc_scratch(&hist);
+  if (st != MOE_OK) return st;
+  cudaStream_t cs = as_stream(stream);
+  if (nblk > 0) {
+    if (s->dtype == MOE_BF16) {
+      CUtensorMap tm_u, tm_e;
+      st = make_map(&tm_u, u, s->T, s->d, kRouteTile);
+      if (st != MOE_OK) return st;
+      st = make_map(&tm_e, centroids, s->n_routed, s->d, s->n_routed);
+      if (st != MOE_OK) return st;
+      route_tc_kernel<<<static_cast<int>(nblk), 128, RouteTcSmemLayout::alloc,
+                        cs>>>(tm_u, tm_e, bias, s->T, s->d, s->n_routed,
+                              s->top_k, topk_idx, topk_gate, hist);
+      MOE_CHECK_LAUNCH();
+    } else {
+      route_f32_kernel<<<static_cast<int>(nblk), 128,
+                         4 * s->n_routed * sizeof(float), cs>>>(
+          static_cast<const float*>(u), static_cast<const float*>(centroids),
+          bias, s->T, s->d, s->n_routed, s->top_k, topk_idx, topk_gate, hist);
+      MOE_CHECK_LAUNCH();
+    }
+  }
+  route_hist_reduce_kernel<<<static_cast<int>(cdiv(s->n_routed, 256)), 256, 0,
+                             cs>>>(hist, static_cast<int>(nblk), s->n_routed,
+                                   counts);
+  MOE_CHECK_LAUNCH();
+  return MOE_OK;
+}
+
+}  // extern "C"

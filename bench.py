@@ -363,8 +363,17 @@ def main():
                     help="seconds of oracle work per reference step")
     ap.add_argument("--ref-tokens", type=int, default=4,
                     help="tokens per reference step (upper bound)")
+    ap.add_argument("--set", action="append", default=[], metavar="KEY=VAL",
+                    help="override a workload field (profiling of a smaller "
+                         "case of the same kernels; not a bench line)")
     args = ap.parse_args()
     cfg = get_config(args.workload)
+    if args.set:
+        over = {}
+        for kv in args.set:
+            k, v = kv.split("=", 1)
+            over[k] = type(getattr(cfg, k))(v)
+        cfg = cfg.with_(name=cfg.name + "+" + ",".join(args.set), **over)
     if args.impl == "reference":
         if args.ref_budget > 10.0:
             args.ref_budget = 10.0

@@ -100,6 +100,10 @@ combine_kernel(const TI* __restrict__ u, const float* __restrict__ y_perm,
   }
 }
 
+__global__ void zero_i32_kernel(int* __restrict__ p, int n) {
+  for (int i = threadIdx.x; i < n; i += blockDim.x) p[i] = 0;
+}
+
 // b_i <- fl32(b_i - gamma) when counts[i]*N > total_assign, fl32(b_i + gamma)
 // when counts[i]*N < total_assign, unchanged otherwise.
 __global__ void update_bias_kernel(const int* __restrict__ counts, int N,

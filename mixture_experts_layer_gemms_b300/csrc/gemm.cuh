@@ -15,13 +15,15 @@
 // Down pass (swiglu = 0): 128 output columns of Y, kept in fp32.
 //
 // Work items: (group, weight tile, token chunk) with the chunk index
-// fastest, so the items that share a weight tile run side by side and the
-// tile is fetched from HBM about once.  The shared experts form one extra
-// group that spans all T tokens, scheduled first.  Offsets stay on the
-// device: each CTA derives the item table from them in its prologue.
+// fastest.  CTAs claim items in index order from a global counter, so the
+// items that share a weight tile run side by side and the tile is fetched
+// from HBM about once; the producer also prefetches the weight stream into
+// L2 a dozen k-blocks ahead to hide DRAM latency.  The shared experts form
+// one extra group that spans all T tokens, scheduled first.  Offsets stay on
+// the device: each CTA derives the item table from them in its prologue.
 //
 // Warp roles (192 threads, one CTA per SM, persistent):
-//   warp 0 lane 0: TMA producer over a STAGES-deep smem ring;
+//   warp 0 lane 0: scheduler + TMA producer over a STAGES-deep smem ring;
 //   warp 1 lane 0: MMA issuer (also allocates / frees TMEM);
 //   warps 2..5   : epilogue, double-buffered TMEM accumulators so that the
 //                  epilogue of one item overlaps the mainloop of the next.
@@ -34,6 +36,8 @@ constexpr int kGemmBM = 128;    // weight rows per tile (MMA M)
 constexpr int kGemmBK = 64;     // K per pipeline stage (128 B of bf16)
 constexpr int kBoxRows = 32;    // token rows per TMA box
 constexpr int kMaxGroups = 256;
+constexpr int kSchedDepth = 4;      // claimed items queued producer -> consumers
+constexpr int kPrefetchAhead = 12;  // weight k-blocks prefetched into L2 ahead
 
 struct GemmParams {
   const int* offsets;   // routed group row offsets [n_groups+1] (device)
@@ -49,6 +53,7 @@ struct GemmParams {
   void* out_shared;
   long long ld_shared;
   int swiglu;
+  int* item_counter;    // zeroed before the launch; CTAs claim items from it
 };
 
 template <int BN, int STAGES>
@@ -60,10 +65,11 @@ struct GemmSmem {
   static constexpr int stg_off = b_off + STAGES * b_bytes;
   static constexpr int stg_bytes = 128 * 33 * 4;
   static constexpr int bar_off = stg_off + stg_bytes;
-  static constexpr int n_bars = 2 * STAGES + 5;
+  static constexpr int n_bars = 2 * STAGES + 5 + 2 * kSchedDepth;
   static constexpr int misc_off = bar_off + n_bars * 8;
   static constexpr int epok_off = misc_off + 16;
-  static constexpr int tab_off = epok_off + 16;
+  static constexpr int sched_off = epok_off + 16;
+  static constexpr int tab_off = sched_off + 4 * kSchedDepth;
   static constexpr int total = tab_off + 2 * (kMaxGroups + 1) * 4;
   static constexpr int alloc = total + 1024;
   static constexpr int tmem_cols = 2 * BN < 32 ? 32 : 2 * BN;
@@ -118,6 +124,62 @@ __device__ __forceinline__ Tile decode_item(int item, const GemmParams& p,
   return t;
 }
 
+// Epilogue of one work item, run by the four epilogue warps (128 threads,
+// named barrier 1).  `taddr` is this warp's TMEM lane quarter at the item's
+// accumulator; TMEM row = weight row of the tile, column = token.  Tokens go
+// 32 at a time through a padded staging buffer so that each thread then
+// owns one token and writes a contiguous run of its output row:
+//   swiglu: H[b_row + n][col0 + ep*16 + c] = SiLU(D[c][n]) * D[64 + c][n]
+//           (bf16, 16 columns per thread), or
+//   down:   Y[b_row + n][col0 + ep*32 + r] = D[ep*32 + r][n] (fp32).
+__device__ __forceinline__ void epilogue_store(uint32_t taddr, int n_valid,
+                                               int b_row, void* out,
+                                               long long ld, int col0,
+                                               bool swiglu, float* stg, int q,
+                                               int ep, int lane) {
+  for (int n0 = 0; n0 < n_valid; n0 += 32) {
+    uint32_t r[32];
+    tmem_ld32(taddr + n0, r);
+    tmem_ld_wait();
+    float* srow = stg + (q * 32 + lane) * 33;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) srow[j] = __uint_as_float(r[j]);
+    named_bar_sync(1, 128);
+    const int n = n0 + lane;
+    if (n < n_valid) {
+      const size_t row = static_cast<size_t>(b_row + n) * ld;
+      if (swiglu) {
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(out) + row;
+        uint32_t pk[8];
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {
+          const int c = ep * 16 + i;
+          const float g0 = stg[c * 33 + lane], u0 = stg[(64 + c) * 33 + lane];
+          const float g1 = stg[(c + 1) * 33 + lane],
+                      u1 = stg[(65 + c) * 33 + lane];
+          pk[i / 2] = pack_bf16x2(silu_f32(g0) * u0, silu_f32(g1) * u1);
+        }
+        uint4* d4 = reinterpret_cast<uint4*>(dst + col0 + ep * 16);
+        d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+      } else {
+        float* dst = static_cast<float*>(out) + row + col0 + ep * 32;
+        float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          d4[i] = make_float4(stg[(ep * 32 + 4 * i) * 33 + lane],
+                              stg[(ep * 32 + 4 * i + 1) * 33 + lane],
+                              stg[(ep * 32 + 4 * i + 2) * 33 + lane],
+                              stg[(ep * 32 + 4 * i + 3) * 33 + lane]);
+      }
+    }
+    named_bar_sync(1, 128);
+  }
+}
+
+// K-block visited at step i of an item (plain ascending order).
+__device__ __forceinline__ int k_block(const Tile&, int i, int) { return i; }
+
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(192, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA_r,
@@ -159,6 +221,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA_r,
       mbar_init(bar_tempty + 8 * a, 128);
     }
     mbar_init(bar_final, 1);
+    for (int i = 0; i < kSchedDepth; ++i) {
+      mbar_init(bar_final + 8 + 8 * i, 1);                    // sched full
+      mbar_init(bar_final + 8 + 8 * kSchedDepth + 8 * i, 5);  // sched empty:
+    }                                   // MMA thread + one per epilogue warp
     *abort_flag = 0;
     *bad_flag = 0;
     fence_mbar_init();
@@ -217,40 +283,87 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA_r,
                           : n_items_s + (G > 0 ? chunk_pre[G] *
                                                      (p.w_rows_routed / kGemmBM)
                                                : 0);
+  // Dynamic schedule: the producer claims items from a global counter (so
+  // the items that share a weight tile run side by side on neighbouring
+  // SMs) and hands each claimed item to the MMA and epilogue warps through a
+  // small ring in shared memory; an item >= n_items tells them to stop.
+  const uint32_t bar_sfull = bar_final + 8;                 // [kSchedDepth]
+  const uint32_t bar_sempty = bar_sfull + 8 * kSchedDepth;  // [kSchedDepth]
+  volatile int* sched = reinterpret_cast<volatile int*>(smem + L::sched_off);
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------- TMA producer ----------------
+      // ---------------- TMA producer + scheduler ----------------
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
-      for (int item = blockIdx.x; item < n_items && !*abort_flag;
-           item += gridDim.x) {
-        const Tile t = decode_item<BN>(item, p, n_items_s, nch_s, off_s,
-                                       chunk_pre);
+      int slot = 0;
+      uint32_t sph = 0;
+      int item = bad ? n_items : atomicAdd(p.item_counter, 1);
+      Tile t{};
+      if (item < n_items) {
+        t = decode_item<BN>(item, p, n_items_s, nch_s, off_s, chunk_pre);
+        const CUtensorMap* mA = t.shared ? &tmA_s : &tmA_r;
+        const int nk = t.k / kGemmBK;
+        for (int i = 0; i < kPrefetchAhead && i < nk; ++i)
+          tma_prefetch_l2_2d(mA, k_block(t, i, nk) * kGemmBK, t.a_row);
+      }
+      while (!*abort_flag) {
+        if (!mbar_wait(bar_sempty + 8 * slot, sph ^ 1, abort_flag, KID_GEMM, 5))
+          break;
+        sched[slot] = item;
+        mbar_arrive(bar_sfull + 8 * slot);
+        if (++slot == kSchedDepth) {
+          slot = 0;
+          sph ^= 1;
+        }
+        if (item >= n_items) break;
+        const int next = atomicAdd(p.item_counter, 1);
+        Tile tn{};
+        int nk_next = 0;
+        if (next < n_items) {
+          tn = decode_item<BN>(next, p, n_items_s, nch_s, off_s, chunk_pre);
+          nk_next = tn.k / kGemmBK;
+        }
         const CUtensorMap* mA = t.shared ? &tmA_s : &tmA_r;
         const CUtensorMap* mB = t.shared ? &tmB_s : &tmB_r;
+        const CUtensorMap* mA_next = tn.shared ? &tmA_s : &tmA_r;
         const int nbox = (t.n_mma + kBoxRows - 1) / kBoxRows;
         const uint32_t bytes = L::a_bytes + nbox * kBoxRows * kGemmBK * 2;
         const int nk = t.k / kGemmBK;
-        for (int kb = 0; kb < nk; ++kb) {
+        bool ok = true;
+        for (int i = 0; i < nk; ++i) {
           if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag,
-                         KID_GEMM, 1))
+                         KID_GEMM, 1)) {
+            ok = false;
             break;
+          }
+          const int kx = k_block(t, i, nk) * kGemmBK;
           const uint32_t fb = bar_full + 8 * stage;
           mbar_arrive_expect_tx(fb, bytes);
-          tma_load_2d(sbase + L::a_off + stage * L::a_bytes, mA, kb * kGemmBK,
-                      t.a_row, fb);
+          tma_load_2d(sbase + L::a_off + stage * L::a_bytes, mA, kx, t.a_row,
+                      fb);
           const uint32_t bdst = sbase + L::b_off + stage * L::b_bytes;
           for (int bx = 0; bx < nbox; ++bx)
-            tma_load_2d(bdst + bx * kBoxRows * kGemmBK * 2, mB, kb * kGemmBK,
+            tma_load_2d(bdst + bx * kBoxRows * kGemmBK * 2, mB, kx,
                         t.b_row + bx * kBoxRows, fb);
+          // keep the weight stream kPrefetchAhead k-blocks ahead in L2,
+          // running on into the next item's tile
+          const int pi = i + kPrefetchAhead;
+          if (pi < nk)
+            tma_prefetch_l2_2d(mA, k_block(t, pi, nk) * kGemmBK, t.a_row);
+          else if (pi - nk < nk_next)
+            tma_prefetch_l2_2d(mA_next, k_block(tn, pi - nk, nk_next) * kGemmBK,
+                               tn.a_row);
           ++issued;
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
           }
         }
+        if (!ok) break;
+        item = next;
+        t = tn;
       }
       if (*abort_flag) {   // let loads in flight land before smem is freed
         for (int j = 0; j < STAGES && j < issued; ++j) {
@@ -271,8 +384,18 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA_r,
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
-      for (int item = blockIdx.x; item < n_items && !*abort_flag;
-           item += gridDim.x) {
+      int slot = 0;
+      uint32_t sph = 0;
+      while (!*abort_flag) {
+        if (!mbar_wait(bar_sfull + 8 * slot, sph, abort_flag, KID_GEMM, 6))
+          break;
+        const int item = sched[slot];
+        mbar_arrive(bar_sempty + 8 * slot);
+        if (++slot == kSchedDepth) {
+          slot = 0;
+          sph ^= 1;
+        }
+        if (item >= n_items) break;
         const Tile t = decode_item<BN>(item, p, n_items_s, nch_s, off_s,
                                        chunk_pre);
         if (!mbar_wait(bar_tempty + 8 * acc, acc_phase ^ 1, abort_flag,
@@ -283,7 +406,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA_r,
         const uint32_t idesc = idesc_bf16_f32(kGemmBM, t.n_mma);
         const int nk = t.k / kGemmBK;
         bool ok = true;
-        for (int kb = 0; kb < nk; ++kb) {
+        for (int i = 0; i < nk; ++i) {
           if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag, KID_GEMM,
                          3)) {
             ok = false;
@@ -295,7 +418,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA_r,
 #pragma unroll
           for (int kk = 0; kk < kGemmBK / 16; ++kk)
             mma_bf16(d_tmem, sdesc_k128(a0 + kk * 32),
-                     sdesc_k128(b0 + kk * 32), idesc, (kb | kk) != 0);
+                     sdesc_k128(b0 + kk * 32), idesc, (i | kk) != 0);
           mma_commit(bar_empty + 8 * stage);
           if (++stage == STAGES) {
             stage = 0;
@@ -319,61 +442,38 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA_r,
     const int q = warp & 3;           // TMEM sub-partition this warp may read
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-      const Tile t = decode_item<BN>(item, p, n_items_s, nch_s, off_s,
-                                     chunk_pre);
+    int slot = 0;
+    uint32_t sph = 0;
+    while (true) {
+      const bool got = mbar_wait(bar_sfull + 8 * slot, sph, abort_flag,
+                                 KID_GEMM, 7);
+      const int item = got ? sched[slot] : n_items;
+      __syncwarp();
+      if (got && lane == 0) mbar_arrive(bar_sempty + 8 * slot);
+      if (++slot == kSchedDepth) {
+        slot = 0;
+        sph ^= 1;
+      }
+      bool ok = got;
+      if (got && item < n_items)
+        ok = mbar_wait(bar_tfull + 8 * acc, acc_phase, abort_flag, KID_GEMM,
+                       4);
       // The four epilogue warps share named barrier 1, so they leave the
       // loop together: each posts its verdict, all read all four.
-      const bool ok = mbar_wait(bar_tfull + 8 * acc, acc_phase, abort_flag,
-                                KID_GEMM, 4);
       const bool wok = __all_sync(0xffffffffu, ok);
       if (lane == 0) ep_ok[ep] = wok ? 1 : 0;
       named_bar_sync(1, 128);
       if (!(ep_ok[0] && ep_ok[1] && ep_ok[2] && ep_ok[3])) break;
+      if (item >= n_items) break;
+      const Tile t = decode_item<BN>(item, p, n_items_s, nch_s, off_s,
+                                     chunk_pre);
       tc_fence_after();
       void* out = t.shared ? p.out_shared : p.out_routed;
       const long long ld = t.shared ? p.ld_shared : p.ld_routed;
-      for (int n0 = 0; n0 < t.n_valid; n0 += 32) {
-        uint32_t r[32];
-        tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + n0,
-                  r);
-        tmem_ld_wait();
-        float* srow = stg + (q * 32 + lane) * 33;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) srow[j] = __uint_as_float(r[j]);
-        named_bar_sync(1, 128);
-        const int n = n0 + lane;
-        if (n < t.n_valid) {
-          const size_t row = static_cast<size_t>(t.b_row + n) * ld;
-          if (p.swiglu) {
-            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(out) + row;
-            // H columns wt*64 + ep*16 + [0, 16)
-            uint32_t pk[8];
-#pragma unroll
-            for (int i = 0; i < 16; i += 2) {
-              const int c = ep * 16 + i;
-              const float g0 = stg[c * 33 + lane], u0 = stg[(64 + c) * 33 + lane];
-              const float g1 = stg[(c + 1) * 33 + lane],
-                          u1 = stg[(65 + c) * 33 + lane];
-              pk[i / 2] = pack_bf16x2(silu_f32(g0) * u0, silu_f32(g1) * u1);
-            }
-            uint4* d4 = reinterpret_cast<uint4*>(dst + t.wt * 64 + ep * 16);
-            d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-          } else {
-            // Y columns wt*128 + ep*32 + [0, 32), fp32
-            float* dst = static_cast<float*>(out) + row + t.wt * 128 + ep * 32;
-            float4* d4 = reinterpret_cast<float4*>(dst);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              d4[i] = make_float4(stg[(ep * 32 + 4 * i) * 33 + lane],
-                                  stg[(ep * 32 + 4 * i + 1) * 33 + lane],
-                                  stg[(ep * 32 + 4 * i + 2) * 33 + lane],
-                                  stg[(ep * 32 + 4 * i + 3) * 33 + lane]);
-          }
-        }
-        named_bar_sync(1, 128);
-      }
+      epilogue_store(tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * BN,
+                     t.n_valid, t.b_row, out, ld,
+                     p.swiglu ? t.wt * 64 : t.wt * 128, p.swiglu != 0, stg,
+                     q, ep, lane);
       tc_fence_before();
       mbar_arrive(bar_tempty + 8 * acc);
       if (++acc == 2) {

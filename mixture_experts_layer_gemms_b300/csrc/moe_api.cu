@@ -12,6 +12,7 @@
 #include "common.cuh"
 #include "elementwise.cuh"
 #include "gemm.cuh"
+#include "gemm2sm.cuh"
 #include "permute.cuh"
 #include "route.cuh"
 #include "moe_b300.h"
@@ -55,6 +56,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceInfo {
   bool init = false;
   int sm_count = 0;
+  int pair_clusters = 0;   // co-resident clusters of the CTA-pair GEMM
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -85,10 +87,26 @@ moe_status device_setup(int* sm_count) {
                               GemmSmem<256, 4>::alloc));
     MOE_CHECK_CUDA(allow_smem(grouped_gemm_kernel<32, 8>,
                               GemmSmem<32, 8>::alloc));
+    MOE_CHECK_CUDA(allow_smem(grouped_gemm_pair_kernel, PairSmem::alloc));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (di.sm_count / 2));
+    cfg.blockDim = dim3(192);
+    cfg.dynamicSmemBytes = PairSmem::alloc;
+    int clusters = 0;
+    MOE_CHECK_CUDA(cudaOccupancyMaxActiveClusters(
+        &clusters, grouped_gemm_pair_kernel, &cfg));
+    di.pair_clusters = clusters;
     di.init = true;
   }
   *sm_count = di.sm_count;
   return MOE_OK;
+}
+
+int pair_clusters() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return 0;
+  return g_dev[dev].pair_clusters;
 }
 
 moe_status get_encoder() {
@@ -173,7 +191,7 @@ moe_status check_shape(const moe_shape* s) {
 }
 
 struct WsLayout {
-  size_t route_hist, perm_hist, h_routed, h_shared, total;
+  size_t sched, route_hist, perm_hist, h_routed, h_shared, total;
 };
 
 WsLayout ws_layout(const moe_shape* s) {
@@ -182,6 +200,8 @@ WsLayout ws_layout(const moe_shape* s) {
   const long long nblk = cdiv(s->T, kRouteTile);
   const long long A = static_cast<long long>(s->T) * s->top_k;
   size_t off = 0;
+  w.sched = off;                      // item counters of the GEMM passes
+  off = round256(off + 2 * sizeof(int));
   w.route_hist = off;
   off = round256(off + static_cast<size_t>(nblk) * s->n_routed * 4);
   w.perm_hist = off;
@@ -240,6 +260,26 @@ moe_status launch_gemm(const CUtensorMap& a_r, const CUtensorMap& b_r,
   const int grid = static_cast<int>(items < sms ? items : sms);
   grouped_gemm_kernel<BN, STAGES><<<grid, 192, GemmSmem<BN, STAGES>::alloc,
                                     cs>>>(a_r, b_r, a_s, b_s, p);
+  MOE_CHECK_LAUNCH();
+  return MOE_OK;
+}
+
+moe_status launch_gemm_pair(const CUtensorMap& a_r, const CUtensorMap& b_r,
+                            const CUtensorMap& a_s, const CUtensorMap& b_s,
+                            const GemmParams& p, cudaStream_t cs) {
+  long long items = 0;
+  if (p.shared_rows > 0)
+    items += cdiv(p.shared_rows, kPairBN) * (p.w_rows_shared / kPairBM);
+  if (p.n_groups > 0)
+    items += (cdiv(p.max_routed_rows, kPairBN) + p.n_groups) *
+             (p.w_rows_routed / kPairBM);
+  if (items == 0) return MOE_OK;
+  const long long clusters = pair_clusters();
+  if (clusters <= 0)
+    return fail(MOE_ERR_CUDA, "CTA-pair GEMM cannot be resident on this GPU");
+  const long long n = items < clusters ? items : clusters;
+  grouped_gemm_pair_kernel<<<static_cast<int>(2 * n), 192, PairSmem::alloc,
+                             cs>>>(a_r, b_r, a_s, b_s, p);
   MOE_CHECK_LAUNCH();
   return MOE_OK;
 }
@@ -457,6 +497,12 @@ moe_status moe_expert_ffn(const moe_shape* s, const void* x_perm,
   // bf16: tcgen05 grouped GEMMs.  Small average group size -> 32-token
   // chunks and a deeper ring (weight streaming); else 256-token chunks.
   const bool small = A <= 48LL * N;
+  // CTA pairs (256 weight rows per item) when every weight group splits
+  // into 256-row tiles; else the single-SM kernel.
+  const bool pair = !small && d % 256 == 0 && I % 128 == 0;
+  int* ctr = reinterpret_cast<int*>(static_cast<char*>(ws) + w.sched);
+  zero_i32_kernel<<<1, 32, 0, cs>>>(ctr, 2);
+  MOE_CHECK_LAUNCH();
   CUtensorMap a_r, b_r, a_s, b_s;
   const int box = kBoxRows;
   GemmParams p{};
@@ -485,8 +531,10 @@ moe_status moe_expert_ffn(const moe_shape* s, const void* x_perm,
   p.out_shared = h_s;
   p.ld_shared = SI;
   p.swiglu = 1;
-  st = small ? launch_gemm<32, 8>(a_r, b_r, a_s, b_s, p, sms, cs)
-             : launch_gemm<256, 4>(a_r, b_r, a_s, b_s, p, sms, cs);
+  p.item_counter = ctr;
+  st = pair ? launch_gemm_pair(a_r, b_r, a_s, b_s, p, cs)
+       : small ? launch_gemm<32, 8>(a_r, b_r, a_s, b_s, p, sms, cs)
+               : launch_gemm<256, 4>(a_r, b_r, a_s, b_s, p, sms, cs);
   if (st != MOE_OK) return st;
   // pass 2: down -> y
   if ((st = make_map(&a_r, w_down, static_cast<long long>(N) * d, I,
@@ -510,10 +558,10 @@ moe_status moe_expert_ffn(const moe_shape* s, const void* x_perm,
   p.out_shared = y_shared;
   p.ld_shared = d;
   p.swiglu = 0;
-  const int before = g_launches;
-  st = small ? launch_gemm<32, 8>(a_r, b_r, a_s, b_s, p, sms, cs)
-             : launch_gemm<256, 4>(a_r, b_r, a_s, b_s, p, sms, cs);
-  (void)before;
+  p.item_counter = ctr + 1;
+  st = pair ? launch_gemm_pair(a_r, b_r, a_s, b_s, p, cs)
+       : small ? launch_gemm<32, 8>(a_r, b_r, a_s, b_s, p, sms, cs)
+               : launch_gemm<256, 4>(a_r, b_r, a_s, b_s, p, sms, cs);
   return st;
 }
 

@@ -10,53 +10,51 @@ namespace moe {
 constexpr int kRouteTile = 128;   // tokens per CTA (both router variants)
 constexpr int kTopKMax = 16;
 
-// Running top-K of (beta, index) pairs, best first.  A pair ranks above
-// another when its beta is larger, or equal with a lower index -- so the
-// lowest index wins a tie, whatever order candidates arrive in.
+// Running top-KT of (beta, index) pairs, best first, in registers (KT is a
+// compile-time size >= K; the first K entries are the top-K).  A pair ranks
+// above another when its beta is larger, or equal with a lower index -- so
+// the lowest index wins a tie, whatever order candidates arrive in.
+template <int KT>
 struct TopK {
-  float b[kTopKMax];
-  float s[kTopKMax];
-  int i[kTopKMax];
-  float kth;  // beta of the K-th entry (-inf until K entries are held)
+  float b[KT];
+  float s[KT];
+  int i[KT];
 
   __device__ __forceinline__ void reset() {
 #pragma unroll
-    for (int j = 0; j < kTopKMax; ++j) {
+    for (int j = 0; j < KT; ++j) {
       b[j] = -INFINITY;
       s[j] = 0.f;
       i[j] = 0x7fffffff;
     }
-    kth = -INFINITY;
   }
-  // Candidates must arrive in ascending index order for the `beta >= kth`
-  // shortcut to be exact: an equal beta with a higher index never enters.
-  __device__ __forceinline__ void push(float beta, float sv, int idx, int K) {
-    if (!(beta > kth)) return;
+  // Candidates arrive in ascending index order, so a candidate whose beta
+  // only equals the current last entry never enters (the earlier index
+  // keeps its place).
+  __device__ __forceinline__ void push(float beta, float sv, int idx) {
+    if (!(beta > b[KT - 1])) return;
     float cb = beta, cs = sv;
     int ci = idx;
 #pragma unroll
-    for (int j = 0; j < kTopKMax; ++j) {
-      if (j < K) {
-        const bool better = (cb > b[j]) || (cb == b[j] && ci < i[j]);
-        if (better) {
-          float tb = b[j], ts = s[j];
-          int ti = i[j];
-          b[j] = cb; s[j] = cs; i[j] = ci;
-          cb = tb; cs = ts; ci = ti;
-        }
-      }
+    for (int j = 0; j < KT; ++j) {
+      const bool better = (cb > b[j]) || (cb == b[j] && ci < i[j]);
+      const float tb = b[j], ts = s[j];
+      const int ti = i[j];
+      b[j] = better ? cb : tb;
+      s[j] = better ? cs : ts;
+      i[j] = better ? ci : ti;
+      cb = better ? tb : cb;
+      cs = better ? ts : cs;
+      ci = better ? ti : ci;
     }
-#pragma unroll
-    for (int j = 0; j < kTopKMax; ++j)
-      if (j == K - 1) kth = b[j];
   }
-  // Writes token t's selection and counts it in the CTA histogram.  A slot
-  // left empty (only possible with non-finite affinities) is written as -1
-  // and reported; it is never used as an index.
+  // Writes token t's first K entries and counts them in the CTA histogram.
+  // A slot left empty (only possible with non-finite affinities) is written
+  // as -1 and reported; it is never used as an index.
   __device__ __forceinline__ void store(int t, int K, int N, int* topk_idx,
                                         float* topk_gate, int* hist) const {
 #pragma unroll
-    for (int j = 0; j < kTopKMax; ++j) {
+    for (int j = 0; j < KT; ++j) {
       if (j < K) {
         int e = i[j];
         if (e < 0 || e >= N) {
@@ -71,6 +69,35 @@ struct TopK {
     }
   }
 };
+
+// Biased top-K of one token from its affinities s[e * stride] (e < N), fp32:
+// beta = s + b, candidates in ascending expert order.
+template <int KT>
+__device__ __forceinline__ void select_token(const float* s, int stride,
+                                             const float* bias, int N, int K,
+                                             int t, int* topk_idx,
+                                             float* topk_gate, int* hist) {
+  TopK<KT> top;
+  top.reset();
+#pragma unroll 4
+  for (int e = 0; e < N; ++e) {
+    const float sv = s[e * stride];
+    top.push(__fadd_rn(sv, bias[e]), sv, e);
+  }
+  top.store(t, K, N, topk_idx, topk_gate, hist);
+}
+
+__device__ __forceinline__ void select_token_any(const float* s, int stride,
+                                                 const float* bias, int N,
+                                                 int K, int t, int* topk_idx,
+                                                 float* topk_gate, int* hist) {
+  if (K <= 4)
+    select_token<4>(s, stride, bias, N, K, t, topk_idx, topk_gate, hist);
+  else if (K <= 8)
+    select_token<8>(s, stride, bias, N, K, t, topk_idx, topk_gate, hist);
+  else
+    select_token<16>(s, stride, bias, N, K, t, topk_idx, topk_gate, hist);
+}
 
 // ------------------------------------------------------------------------
 // bf16 router on the tensor cores.  One CTA = 128 tokens x all N experts:
@@ -152,11 +179,15 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tm_u,
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0 && lane == 0) {
-    // TMA producer
+    // TMA producer.  Each CTA walks d from its own starting block (rotated
+    // order), so the CTAs do not all fetch the same centroid block from the
+    // same L2 slices at the same moment.
     int issued = 0;
-    for (int kb = 0; kb < nk; ++kb) {
-      const int s = kb % kRtStages;
-      const uint32_t ph = (kb / kRtStages) & 1;
+    const int kb0 = (tile * 5) % nk;
+    for (int i = 0; i < nk; ++i) {
+      const int s = i % kRtStages;
+      const uint32_t ph = (i / kRtStages) & 1;
+      const int kb = (kb0 + i) % nk;
       if (!mbar_wait(bar_empty + 8 * s, ph ^ 1, abort_flag, KID_ROUTE_TC, 1))
         break;
       ++issued;
@@ -172,33 +203,35 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tm_u,
   } else if (warp == 1 && lane == 0) {
     // MMA issuer
     const uint32_t idesc = idesc_bf16_f32(128, N);
-    for (int kb = 0; kb < nk; ++kb) {
-      const int s = kb % kRtStages;
-      const uint32_t ph = (kb / kRtStages) & 1;
+    for (int i = 0; i < nk; ++i) {
+      const int s = i % kRtStages;
+      const uint32_t ph = (i / kRtStages) & 1;
       if (!mbar_wait(bar_full + 8 * s, ph, abort_flag, KID_ROUTE_TC, 2))
         break;
       tc_fence_after();
       const uint32_t a0 = sbase + L::a_off + s * L::a_bytes;
       const uint32_t b0 = sbase + L::b_off + s * L::b_bytes_max;
-      const uint32_t d_acc = tmem + (kb % n_acc) * acc_cols;
+      const uint32_t d_acc = tmem + (i % n_acc) * acc_cols;
 #pragma unroll
       for (int kk = 0; kk < kRtBK / 16; ++kk)
         mma_bf16(d_acc, sdesc_k128(a0 + kk * 32), sdesc_k128(b0 + kk * 32),
-                 idesc, (kb >= n_acc || kk > 0) ? 1u : 0u);
+                 idesc, (i >= n_acc || kk > 0) ? 1u : 0u);
       mma_commit(bar_empty + 8 * s);
     }
     mma_commit(bar_done);   // also fires when the loop stopped early
   }
   __syncwarp();
 
-  // Epilogue: every thread owns one token (TMEM lane).
+  // Epilogue: every thread owns one token (TMEM lane).  Its affinities go
+  // to shared memory (the pipeline buffers are free by now), row-major with
+  // a padded stride so a warp's accesses hit distinct banks, then a plain
+  // loop selects the top-K.
   const bool done_ok = mbar_wait(bar_done, 0, abort_flag, KID_ROUTE_TC, 3);
   tc_fence_after();
   const bool go = __all_sync(0xffffffffu, done_ok && !*abort_flag);
   const int row = warp * 32 + lane;
   const int t = tile * kRouteTile + row;
-  TopK top;
-  top.reset();
+  float* srow = reinterpret_cast<float*>(smem) + row * (N + 1);
   if (go) {
     const int used = min(n_acc, nk);
     for (int c0 = 0; c0 < N; c0 += 32) {
@@ -216,15 +249,11 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tm_u,
         for (int j = 0; j < 32; ++j) z[j] += __uint_as_float(r[j]);
       }
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int e = c0 + j;
-        if (e < N) {
-          const float sv = sigmoid_f32(z[j]);
-          top.push(__fadd_rn(sv, bias_s[e]), sv, e, K);
-        }
-      }
+      for (int j = 0; j < 32; ++j)
+        if (c0 + j < N) srow[c0 + j] = sigmoid_f32(z[j]);
     }
-    if (t < T) top.store(t, K, N, topk_idx, topk_gate, hist);
+    if (t < T)
+      select_token_any(srow, 1, bias_s, N, K, t, topk_idx, topk_gate, hist);
   }
   tc_fence_before();
   __syncthreads();
@@ -263,15 +292,10 @@ route_f32_kernel(const float* __restrict__ u, const float* __restrict__ E,
       if (lane == 0) z[e] = acc;
     }
     __syncwarp();
-    if (lane == 0) {
-      TopK top;
-      top.reset();
-      for (int e = 0; e < N; ++e) {
-        const float sv = sigmoid_f32(z[e]);
-        top.push(__fadd_rn(sv, bias[e]), sv, e, K);
-      }
-      top.store(t, K, N, topk_idx, topk_gate, hist);
-    }
+    for (int e = lane; e < N; e += 32) z[e] = sigmoid_f32(z[e]);
+    __syncwarp();
+    if (lane == 0)
+      select_token_any(z, 1, bias, N, K, t, topk_idx, topk_gate, hist);
     __syncwarp();
   }
   __syncthreads();

@@ -311,6 +311,9 @@ LAYER_CASES = {
                              "d_ff": 128}),
     "v3dims_T200_N64": ("v3_prefill", {"T": 200, "n_routed": 64}),
     "ragged_T37": ("mid", {"T": 37}),
+    # d % 256 != 0 and I % 128 != 0: the single-SM grouped GEMM
+    "single_sm_d384_I192": ("mid", {"T": 400, "d": 384, "d_ff": 192,
+                                    "n_routed": 16, "top_k": 4}),
 }
 
 

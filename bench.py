@@ -310,7 +310,7 @@ def run_ours(args, cfg):
         roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": ach / peaks["hbm_gbs"],
                 "traffic": None,
-                "kernel": "grouped_gemm_kernel<32,8> (gate/up + down launches)",
+                "kernel": "grouped_gemm_kernel<32,10> (gate/up + down launches)",
                 "peak_source": f"{peaks['source']} hbm_gbs"}
     else:
         ach = ffn_flops(cfg) / (ffn_ms / 1e3) / 1e12

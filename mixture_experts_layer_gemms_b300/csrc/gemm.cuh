@@ -63,7 +63,7 @@ struct GemmSmem {
   static constexpr int a_off = 0;
   static constexpr int b_off = a_off + STAGES * a_bytes;
   static constexpr int stg_off = b_off + STAGES * b_bytes;
-  static constexpr int stg_bytes = 128 * 33 * 4;
+  static constexpr int stg_bytes = 4 * 32 * 17 * 4;   // epilogue exchange
   static constexpr int bar_off = stg_off + stg_bytes;
   static constexpr int n_bars = 2 * STAGES + 5 + 2 * kSchedDepth;
   static constexpr int misc_off = bar_off + n_bars * 8;
@@ -126,52 +126,55 @@ __device__ __forceinline__ Tile decode_item(int item, const GemmParams& p,
 
 // Epilogue of one work item, run by the four epilogue warps (128 threads,
 // named barrier 1).  `taddr` is this warp's TMEM lane quarter at the item's
-// accumulator; TMEM row = weight row of the tile, column = token.  Tokens go
-// 32 at a time through a padded staging buffer so that each thread then
-// owns one token and writes a contiguous run of its output row:
-//   swiglu: H[b_row + n][col0 + ep*16 + c] = SiLU(D[c][n]) * D[64 + c][n]
-//           (bf16, 16 columns per thread), or
-//   down:   Y[b_row + n][col0 + ep*32 + r] = D[ep*32 + r][n] (fp32).
+// accumulator; TMEM row = weight row of the tile, column = token.  Thread
+// (q, lane) owns weight row q*32 + lane and, per 32-token chunk, reads that
+// row's 32 values with one tcgen05.ld.
+//   down (swiglu = 0): row r is output column col0 + r of Y (fp32).  For each
+//     token the warp stores 32 consecutive floats (128 B), straight from
+//     registers -- no shared memory.
+//   gate/up (swiglu = 1): rows 0..63 are gate and rows 64..127 the up values
+//     of H columns col0 + 0..63.  Warp q (gate) and warp q+2 (up) swap half
+//     of their tokens through `xchg`: the gate warp finishes tokens 0..15,
+//     the up warp tokens 16..31, each storing 32 consecutive bf16 per token.
+//   xchg: 4 warps x 32 lanes x 17 floats (padded against bank conflicts).
 __device__ __forceinline__ void epilogue_store(uint32_t taddr, int n_valid,
                                                int b_row, void* out,
                                                long long ld, int col0,
-                                               bool swiglu, float* stg, int q,
+                                               bool swiglu, float* xchg, int q,
                                                int ep, int lane) {
+  (void)ep;
   for (int n0 = 0; n0 < n_valid; n0 += 32) {
     uint32_t r[32];
     tmem_ld32(taddr + n0, r);
     tmem_ld_wait();
-    float* srow = stg + (q * 32 + lane) * 33;
+    const int nleft = n_valid - n0;   // tokens of this chunk that exist
+    if (!swiglu) {
+      float* dst = static_cast<float*>(out) +
+                   static_cast<size_t>(b_row + n0) * ld + col0 + q * 32 + lane;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) srow[j] = __uint_as_float(r[j]);
+      for (int j = 0; j < 32; ++j)
+        if (j < nleft) dst[static_cast<size_t>(j) * ld] = __uint_as_float(r[j]);
+      continue;
+    }
+    const bool gate_warp = q < 2;
+    const int pair_q = q & 1;               // warps q and q+2 form a pair
+    // publish the half the partner warp finishes
+    float* mine = xchg + ((q * 32) + lane) * 17;
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      mine[j] = __uint_as_float(r[gate_warp ? 16 + j : j]);
     named_bar_sync(1, 128);
-    const int n = n0 + lane;
-    if (n < n_valid) {
-      const size_t row = static_cast<size_t>(b_row + n) * ld;
-      if (swiglu) {
-        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(out) + row;
-        uint32_t pk[8];
+    const float* theirs = xchg + (((gate_warp ? q + 2 : q - 2) * 32) + lane) * 17;
+    const int jbase = gate_warp ? 0 : 16;
+    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(out) +
+                         static_cast<size_t>(b_row + n0 + jbase) * ld + col0 +
+                         pair_q * 32 + lane;
 #pragma unroll
-        for (int i = 0; i < 16; i += 2) {
-          const int c = ep * 16 + i;
-          const float g0 = stg[c * 33 + lane], u0 = stg[(64 + c) * 33 + lane];
-          const float g1 = stg[(c + 1) * 33 + lane],
-                      u1 = stg[(65 + c) * 33 + lane];
-          pk[i / 2] = pack_bf16x2(silu_f32(g0) * u0, silu_f32(g1) * u1);
-        }
-        uint4* d4 = reinterpret_cast<uint4*>(dst + col0 + ep * 16);
-        d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-      } else {
-        float* dst = static_cast<float*>(out) + row + col0 + ep * 32;
-        float4* d4 = reinterpret_cast<float4*>(dst);
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          d4[i] = make_float4(stg[(ep * 32 + 4 * i) * 33 + lane],
-                              stg[(ep * 32 + 4 * i + 1) * 33 + lane],
-                              stg[(ep * 32 + 4 * i + 2) * 33 + lane],
-                              stg[(ep * 32 + 4 * i + 3) * 33 + lane]);
-      }
+    for (int j = 0; j < 16; ++j) {
+      const float g = gate_warp ? __uint_as_float(r[j]) : theirs[j];
+      const float u = gate_warp ? theirs[j] : __uint_as_float(r[16 + j]);
+      if (jbase + j < nleft)
+        dst[static_cast<size_t>(j) * ld] = __float2bfloat16_rn(silu_f32(g) * u);
     }
     named_bar_sync(1, 128);
   }

@@ -42,7 +42,7 @@ struct PairSmem {
   static constexpr int a_off = 0;
   static constexpr int b_off = a_off + kPairStages * a_bytes;
   static constexpr int stg_off = b_off + kPairStages * b_bytes;
-  static constexpr int stg_bytes = 128 * 33 * 4;
+  static constexpr int stg_bytes = 4 * 32 * 17 * 4;   // epilogue exchange
   static constexpr int bar_off = stg_off + stg_bytes;
   static constexpr int n_bars = 2 * kPairStages + 5 + 2 * kSchedDepth;
   static constexpr int misc_off = bar_off + n_bars * 8;

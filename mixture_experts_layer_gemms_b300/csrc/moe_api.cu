@@ -85,8 +85,8 @@ moe_status device_setup(int* sm_count) {
     MOE_CHECK_CUDA(allow_smem(route_tc_kernel, RouteTcSmemLayout::alloc));
     MOE_CHECK_CUDA(allow_smem(grouped_gemm_kernel<256, 4>,
                               GemmSmem<256, 4>::alloc));
-    MOE_CHECK_CUDA(allow_smem(grouped_gemm_kernel<32, 8>,
-                              GemmSmem<32, 8>::alloc));
+    MOE_CHECK_CUDA(allow_smem(grouped_gemm_kernel<32, 10>,
+                              GemmSmem<32, 10>::alloc));
     MOE_CHECK_CUDA(allow_smem(grouped_gemm_pair_kernel, PairSmem::alloc));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (di.sm_count / 2));
@@ -533,7 +533,7 @@ moe_status moe_expert_ffn(const moe_shape* s, const void* x_perm,
   p.swiglu = 1;
   p.item_counter = ctr;
   st = pair ? launch_gemm_pair(a_r, b_r, a_s, b_s, p, cs)
-       : small ? launch_gemm<32, 8>(a_r, b_r, a_s, b_s, p, sms, cs)
+       : small ? launch_gemm<32, 10>(a_r, b_r, a_s, b_s, p, sms, cs)
                : launch_gemm<256, 4>(a_r, b_r, a_s, b_s, p, sms, cs);
   if (st != MOE_OK) return st;
   // pass 2: down -> y
@@ -560,7 +560,7 @@ moe_status moe_expert_ffn(const moe_shape* s, const void* x_perm,
   p.swiglu = 0;
   p.item_counter = ctr + 1;
   st = pair ? launch_gemm_pair(a_r, b_r, a_s, b_s, p, cs)
-       : small ? launch_gemm<32, 8>(a_r, b_r, a_s, b_s, p, sms, cs)
+       : small ? launch_gemm<32, 10>(a_r, b_r, a_s, b_s, p, sms, cs)
                : launch_gemm<256, 4>(a_r, b_r, a_s, b_s, p, sms, cs);
   return st;
 }

@@ -97,6 +97,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA_r,
                          const __grid_constant__ CUtensorMap tmB_r,
                          const __grid_constant__ CUtensorMap tmA_s,
                          const __grid_constant__ CUtensorMap tmB_s,
+                         const __grid_constant__ CUtensorMap tmB_r128,
+                         const __grid_constant__ CUtensorMap tmB_s128,
                          const GemmParams p) {
   using L = PairSmem;
   constexpr int ST = kPairStages;
@@ -245,6 +247,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA_r,
                                         chunk_pre);
         const CUtensorMap* mA = t.shared ? &tmA_s : &tmA_r;
         const CUtensorMap* mB = t.shared ? &tmB_s : &tmB_r;
+        // a full half (128 token rows) goes in one 128-row box
+        const CUtensorMap* mB128 = t.shared ? &tmB_s128 : &tmB_r128;
         const int half = t.n_mma >> 1;                 // token rows per CTA
         const int nbox = (half + kBoxRows - 1) / kBoxRows;
         const int a_row = t.a_row + static_cast<int>(rank) * 128;
@@ -267,9 +271,13 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA_r,
           tma_load_2d_pair(sbase + L::a_off + stage * L::a_bytes, mA, kx, a_row,
                            fb);
           const uint32_t bdst = sbase + L::b_off + stage * L::b_bytes;
-          for (int bx = 0; bx < nbox; ++bx)
-            tma_load_2d_pair(bdst + bx * kBoxRows * kGemmBK * 2, mB, kx,
-                             b_row + bx * kBoxRows, fb);
+          if (half == kPairHalfRows) {
+            tma_load_2d_pair(bdst, mB128, kx, b_row, fb);
+          } else {
+            for (int bx = 0; bx < nbox; ++bx)
+              tma_load_2d_pair(bdst + bx * kBoxRows * kGemmBK * 2, mB, kx,
+                               b_row + bx * kBoxRows, fb);
+          }
           if (i + kPrefetchAhead < nk)
             tma_prefetch_l2_2d(mA, (i + kPrefetchAhead) * kGemmBK, a_row);
           ++issued;

@@ -17,8 +17,9 @@
 // Work items: (group, weight tile, token chunk) with the chunk index
 // fastest.  CTAs claim items in index order from a global counter, so the
 // items that share a weight tile run side by side and the tile is fetched
-// from HBM about once; the producer also prefetches the weight stream into
-// L2 a dozen k-blocks ahead to hide DRAM latency.  The shared experts form
+// from HBM about once.  (An L2 prefetch of the weight stream ahead of the
+// TMA ring measured slower: the extra TMA instructions cost more than the
+// latency they hide.)  The shared experts form
 // one extra group that spans all T tokens, scheduled first.  Offsets stay on
 // the device: each CTA derives the item table from them in its prologue.
 //
@@ -36,8 +37,7 @@ constexpr int kGemmBM = 128;    // weight rows per tile (MMA M)
 constexpr int kGemmBK = 64;     // K per pipeline stage (128 B of bf16)
 constexpr int kBoxRows = 32;    // token rows per TMA box
 constexpr int kMaxGroups = 256;
-constexpr int kSchedDepth = 4;      // claimed items queued producer -> consumers
-constexpr int kPrefetchAhead = 12;  // weight k-blocks prefetched into L2 ahead
+constexpr int kSchedDepth = 6;      // claimed items queued producer -> consumers
 
 struct GemmParams {
   const int* offsets;   // routed group row offsets [n_groups+1] (device)
@@ -304,13 +304,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA_r,
       uint32_t sph = 0;
       int item = bad ? n_items : atomicAdd(p.item_counter, 1);
       Tile t{};
-      if (item < n_items) {
+      if (item < n_items)
         t = decode_item<BN>(item, p, n_items_s, nch_s, off_s, chunk_pre);
-        const CUtensorMap* mA = t.shared ? &tmA_s : &tmA_r;
-        const int nk = t.k / kGemmBK;
-        for (int i = 0; i < kPrefetchAhead && i < nk; ++i)
-          tma_prefetch_l2_2d(mA, k_block(t, i, nk) * kGemmBK, t.a_row);
-      }
       while (!*abort_flag) {
         if (!mbar_wait(bar_sempty + 8 * slot, sph ^ 1, abort_flag, KID_GEMM, 5))
           break;
@@ -323,14 +318,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA_r,
         if (item >= n_items) break;
         const int next = atomicAdd(p.item_counter, 1);
         Tile tn{};
-        int nk_next = 0;
-        if (next < n_items) {
+        if (next < n_items)
           tn = decode_item<BN>(next, p, n_items_s, nch_s, off_s, chunk_pre);
-          nk_next = tn.k / kGemmBK;
-        }
         const CUtensorMap* mA = t.shared ? &tmA_s : &tmA_r;
         const CUtensorMap* mB = t.shared ? &tmB_s : &tmB_r;
-        const CUtensorMap* mA_next = tn.shared ? &tmA_s : &tmA_r;
         const int nbox = (t.n_mma + kBoxRows - 1) / kBoxRows;
         const uint32_t bytes = L::a_bytes + nbox * kBoxRows * kGemmBK * 2;
         const int nk = t.k / kGemmBK;
@@ -350,14 +341,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA_r,
           for (int bx = 0; bx < nbox; ++bx)
             tma_load_2d(bdst + bx * kBoxRows * kGemmBK * 2, mB, kx,
                         t.b_row + bx * kBoxRows, fb);
-          // keep the weight stream kPrefetchAhead k-blocks ahead in L2,
-          // running on into the next item's tile
-          const int pi = i + kPrefetchAhead;
-          if (pi < nk)
-            tma_prefetch_l2_2d(mA, k_block(t, pi, nk) * kGemmBK, t.a_row);
-          else if (pi - nk < nk_next)
-            tma_prefetch_l2_2d(mA_next, k_block(tn, pi - nk, nk_next) * kGemmBK,
-                               tn.a_row);
           ++issued;
           if (++stage == STAGES) {
             stage = 0;

@@ -256,8 +256,6 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA_r,
         const uint32_t pair_bytes =
             2u * (L::a_bytes + nbox * kBoxRows * kGemmBK * 2);
         const int nk = t.k / kGemmBK;
-        for (int i = 0; i < kPrefetchAhead && i < nk; ++i)
-          tma_prefetch_l2_2d(mA, i * kGemmBK, a_row);
         bool ok = true;
         for (int i = 0; i < nk; ++i) {
           if (!mbar_wait_cl(bar_empty + 8 * stage, phase ^ 1, abort_flag,
@@ -278,8 +276,6 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA_r,
               tma_load_2d_pair(bdst + bx * kBoxRows * kGemmBK * 2, mB, kx,
                                b_row + bx * kBoxRows, fb);
           }
-          if (i + kPrefetchAhead < nk)
-            tma_prefetch_l2_2d(mA, (i + kPrefetchAhead) * kGemmBK, a_row);
           ++issued;
           if (++stage == ST) {
             stage = 0;

@@ -97,6 +97,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA_r,
                          const __grid_constant__ CUtensorMap tmB_r,
                          const __grid_constant__ CUtensorMap tmA_s,
                          const __grid_constant__ CUtensorMap tmB_s,
+                         const __grid_constant__ CUtensorMap tmB_r64,
+                         const __grid_constant__ CUtensorMap tmB_s64,
                          const __grid_constant__ CUtensorMap tmB_r128,
                          const __grid_constant__ CUtensorMap tmB_s128,
                          const GemmParams p) {
@@ -246,15 +248,19 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA_r,
         const Tile t = decode_pair_item(item, p, n_items_s, nch_s, off_s,
                                         chunk_pre);
         const CUtensorMap* mA = t.shared ? &tmA_s : &tmA_r;
-        const CUtensorMap* mB = t.shared ? &tmB_s : &tmB_r;
-        // a full half (128 token rows) goes in one 128-row box
-        const CUtensorMap* mB128 = t.shared ? &tmB_s128 : &tmB_r128;
+        // The CTA's token half-tile comes in ONE TMA box of 32, 64 or 128
+        // rows (the smallest that covers it; rows past the half are loaded
+        // and ignored): the TMA instruction count per stage, not the bytes,
+        // is what costs here.
         const int half = t.n_mma >> 1;                 // token rows per CTA
-        const int nbox = (half + kBoxRows - 1) / kBoxRows;
+        const int box = half <= 32 ? 32 : (half <= 64 ? 64 : 128);
+        const CUtensorMap* mB =
+            box == 32 ? (t.shared ? &tmB_s : &tmB_r)
+                      : (box == 64 ? (t.shared ? &tmB_s64 : &tmB_r64)
+                                   : (t.shared ? &tmB_s128 : &tmB_r128));
         const int a_row = t.a_row + static_cast<int>(rank) * 128;
         const int b_row = t.b_row + static_cast<int>(rank) * half;
-        const uint32_t pair_bytes =
-            2u * (L::a_bytes + nbox * kBoxRows * kGemmBK * 2);
+        const uint32_t pair_bytes = 2u * (L::a_bytes + box * kGemmBK * 2);
         const int nk = t.k / kGemmBK;
         bool ok = true;
         for (int i = 0; i < nk; ++i) {
@@ -268,14 +274,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA_r,
           const int kx = i * kGemmBK;
           tma_load_2d_pair(sbase + L::a_off + stage * L::a_bytes, mA, kx, a_row,
                            fb);
-          const uint32_t bdst = sbase + L::b_off + stage * L::b_bytes;
-          if (half == kPairHalfRows) {
-            tma_load_2d_pair(bdst, mB128, kx, b_row, fb);
-          } else {
-            for (int bx = 0; bx < nbox; ++bx)
-              tma_load_2d_pair(bdst + bx * kBoxRows * kGemmBK * 2, mB, kx,
-                               b_row + bx * kBoxRows, fb);
-          }
+          tma_load_2d_pair(sbase + L::b_off + stage * L::b_bytes, mB, kx,
+                           b_row, fb);
           ++issued;
           if (++stage == ST) {
             stage = 0;

@@ -266,6 +266,7 @@ moe_status launch_gemm(const CUtensorMap& a_r, const CUtensorMap& b_r,
 
 moe_status launch_gemm_pair(const CUtensorMap& a_r, const CUtensorMap& b_r,
                             const CUtensorMap& a_s, const CUtensorMap& b_s,
+                            const CUtensorMap& b_r64, const CUtensorMap& b_s64,
                             const CUtensorMap& b_r128,
                             const CUtensorMap& b_s128, const GemmParams& p,
                             cudaStream_t cs) {
@@ -281,7 +282,8 @@ moe_status launch_gemm_pair(const CUtensorMap& a_r, const CUtensorMap& b_r,
     return fail(MOE_ERR_CUDA, "CTA-pair GEMM cannot be resident on this GPU");
   const long long n = items < clusters ? items : clusters;
   grouped_gemm_pair_kernel<<<static_cast<int>(2 * n), 192, PairSmem::alloc,
-                             cs>>>(a_r, b_r, a_s, b_s, b_r128, b_s128, p);
+                             cs>>>(a_r, b_r, a_s, b_s, b_r64, b_s64, b_r128,
+                                   b_s128, p);
   MOE_CHECK_LAUNCH();
   return MOE_OK;
 }
@@ -511,17 +513,22 @@ moe_status moe_expert_ffn(const moe_shape* s, const void* x_perm,
   // pass 1: gate/up + SwiGLU -> H
   if ((st = make_map(&a_r, w_gu_packed, 2LL * N * I, d, kGemmBM)) != MOE_OK)
     return st;
-  CUtensorMap b_r128, b_s128;   // 128-row token boxes (CTA-pair kernel)
+  // token maps with 32-, 64- and 128-row boxes (the CTA-pair kernel loads a
+  // token half-tile with the smallest box that covers it)
+  CUtensorMap b_r64, b_s64, b_r128, b_s128;
   if ((st = make_map(&b_r, x_perm, A, d, box)) != MOE_OK) return st;
+  if ((st = make_map(&b_r64, x_perm, A, d, 64)) != MOE_OK) return st;
   if ((st = make_map(&b_r128, x_perm, A, d, 128)) != MOE_OK) return st;
   if (has_shared) {
     if ((st = make_map(&a_s, ws_gu_packed, 2LL * SI, d, kGemmBM)) != MOE_OK)
       return st;
     if ((st = make_map(&b_s, u, s->T, d, box)) != MOE_OK) return st;
+    if ((st = make_map(&b_s64, u, s->T, d, 64)) != MOE_OK) return st;
     if ((st = make_map(&b_s128, u, s->T, d, 128)) != MOE_OK) return st;
   } else {
     a_s = a_r;
     b_s = b_r;
+    b_s64 = b_r64;
     b_s128 = b_r128;
   }
   p.offsets = offsets;
@@ -538,7 +545,8 @@ moe_status moe_expert_ffn(const moe_shape* s, const void* x_perm,
   p.ld_shared = SI;
   p.swiglu = 1;
   p.item_counter = ctr;
-  st = pair ? launch_gemm_pair(a_r, b_r, a_s, b_s, b_r128, b_s128, p, cs)
+  st = pair ? launch_gemm_pair(a_r, b_r, a_s, b_s, b_r64, b_s64, b_r128,
+                               b_s128, p, cs)
        : small ? launch_gemm<32, 10>(a_r, b_r, a_s, b_s, p, sms, cs)
                : launch_gemm<256, 4>(a_r, b_r, a_s, b_s, p, sms, cs);
   if (st != MOE_OK) return st;
@@ -547,15 +555,18 @@ moe_status moe_expert_ffn(const moe_shape* s, const void* x_perm,
                      kGemmBM)) != MOE_OK)
     return st;
   if ((st = make_map(&b_r, h_r, A, I, box)) != MOE_OK) return st;
+  if ((st = make_map(&b_r64, h_r, A, I, 64)) != MOE_OK) return st;
   if ((st = make_map(&b_r128, h_r, A, I, 128)) != MOE_OK) return st;
   if (has_shared) {
     if ((st = make_map(&a_s, ws_down_packed, d, SI, kGemmBM)) != MOE_OK)
       return st;
     if ((st = make_map(&b_s, h_s, s->T, SI, box)) != MOE_OK) return st;
+    if ((st = make_map(&b_s64, h_s, s->T, SI, 64)) != MOE_OK) return st;
     if ((st = make_map(&b_s128, h_s, s->T, SI, 128)) != MOE_OK) return st;
   } else {
     a_s = a_r;
     b_s = b_r;
+    b_s64 = b_r64;
     b_s128 = b_r128;
   }
   p.w_rows_routed = d;
@@ -568,7 +579,8 @@ moe_status moe_expert_ffn(const moe_shape* s, const void* x_perm,
   p.ld_shared = d;
   p.swiglu = 0;
   p.item_counter = ctr + 1;
-  st = pair ? launch_gemm_pair(a_r, b_r, a_s, b_s, b_r128, b_s128, p, cs)
+  st = pair ? launch_gemm_pair(a_r, b_r, a_s, b_s, b_r64, b_s64, b_r128,
+                               b_s128, p, cs)
        : small ? launch_gemm<32, 10>(a_r, b_r, a_s, b_s, p, sms, cs)
                : launch_gemm<256, 4>(a_r, b_r, a_s, b_s, p, sms, cs);
   return st;

@@ -81,11 +81,17 @@ __device__ __forceinline__ Tile decode_pair_item(int item, const GemmParams& p,
     const int ce = chunk_pre[e + 1] - chunk_pre[e];
     const int local = j - chunk_pre[e] * wt_r;
     const int wt = local / ce, ch = local % ce;
+    // ce = ceil(m / 256) chunks of equal size (rounded up to 16): two
+    // balanced chunks each keep their MMAs busy while the weight tile
+    // streams, where 256 + a few tokens would leave the second item with
+    // almost no MMA work (measured ~1.5% faster at the V3 prefill shape).
+    const int m = off_s[e + 1] - off_s[e];
+    const int sz = (((m + ce - 1) / ce) + 15) & ~15;
     t.shared = 0;
     t.wt = wt;
     t.a_row = e * p.w_rows_routed + wt * kPairBM;
-    t.b_row = off_s[e] + ch * kPairBN;
-    t.n_valid = min(kPairBN, off_s[e + 1] - t.b_row);
+    t.b_row = off_s[e] + ch * sz;
+    t.n_valid = min(sz, off_s[e + 1] - t.b_row);
     t.k = p.k_routed;
   }
   t.n_mma = (t.n_valid + 15) & ~15;

@@ -32,6 +32,11 @@ import torch  # noqa: E402
 from moe_inputs import as_f64, generate, get_config  # noqa: E402
 
 METRIC = "MoE-layer tokens/s at V3 shape"
+# DRAM bytes (read + write) of one expert-FFN call (the grouped GEMM's two
+# launches) from an ncu capture of the same kernel on a smaller case of the
+# same shape, scaled by the units processed (see profiles/
+# grouped_gemm_pair_small_v3dims.md).  None where no capture exists.
+MEASURED_TRAFFIC = {"v3_prefill": 26.5e9}
 L2_NOTE = "inputs larger than L2 (22.5 GB of expert weights read per step)"
 
 
@@ -195,6 +200,65 @@ def run_reference(args, cfg):
     print(json.dumps(line), flush=True)
 
 
+def run_skew(args, cfg, moe, dev, ws, rank, local):
+    """The skewed-load bias loop: cfg.steps steps, each with a fresh batch,
+    every one followed by the +-gamma bias update.  Reports throughput and
+    the max/mean expert load of every step."""
+    from moe_inputs import step_tokens
+    t = generate(cfg, dev)
+    steps = cfg.steps
+    us = [step_tokens(cfg, s, dev) for s in range(steps)]
+    bias0 = t["b"].clone()
+    layer = moe.MoELayer(t["E"], t["b"].clone(), t["w_gate"], t["w_up"],
+                         t["w_down"], t["ws_gate"], t["ws_up"], t["ws_down"],
+                         top_k=cfg.top_k, h_dtype=torch.float32)
+    bufs = layer.buffers(cfg.T)
+    loads = torch.empty((steps, cfg.n_routed), dtype=torch.int32, device=dev)
+    for s in range(max(3, args.warmup)):          # warm-up on a scratch bias
+        layer(us[s % steps], update_bias=True, gamma=cfg.gamma)
+    torch.cuda.synchronize()
+    layer.bias.copy_(bias0)
+    moe.get_device_error()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for s in range(steps):
+        layer(us[s], update_bias=True, gamma=cfg.gamma)
+        loads[s].copy_(bufs.counts)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    moe.get_device_error()
+    ms = t0.elapsed_time(t1)
+    c = loads.cpu().numpy().astype(np.float64)
+    mean = cfg.T * cfg.top_k / cfg.n_routed
+    mm = (c.max(axis=1) / mean).tolist()
+    peaks = _peaks()
+    line = {"metric": METRIC, "value": ws * cfg.T * steps / (ms / 1e3),
+            "unit": "tokens/s", "n_gpus": ws, "steps": steps,
+            "warmup": max(3, args.warmup), "ms_per_step": ms / steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": cfg.name, "T": cfg.T, "d": cfg.d,
+                       "n_routed": cfg.n_routed, "top_k": cfg.top_k,
+                       "n_shared": cfg.n_shared, "d_ff": cfg.d_ff,
+                       "gamma": cfg.gamma, "zipf": cfg.zipf,
+                       "parallelism": f"replicas x{ws}", "l2": L2_NOTE},
+            "layer_tflops": layer_flops(cfg) / (ms / steps / 1e3) / 1e12,
+            "layer_frac_of_bf16_peak": layer_flops(cfg) / (ms / steps / 1e3) /
+            1e12 / peaks["bf16_tflops"],
+            "load_max_over_mean": {"first": mm[0], "last": mm[-1],
+                                   "per_step": [round(x, 3) for x in mm]},
+            "clocks": clk}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def run_ours(args, cfg):
     ws, rank, local = _dist()
     torch.cuda.set_device(local)
@@ -204,6 +268,12 @@ def run_ours(args, cfg):
     import mixture_experts_layer_gemms_b300 as moe
 
     dev = torch.device("cuda", local)
+    if cfg.steps > 1:
+        run_skew(args, cfg, moe, dev, ws, rank, local)
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
     t = generate(cfg, dev)
     layer = moe.MoELayer(t["E"], t["b"].clone(), t["w_gate"], t["w_up"],
                          t["w_down"], t["ws_gate"], t["ws_up"], t["ws_down"],
@@ -310,14 +380,17 @@ def run_ours(args, cfg):
         roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": ach / peaks["hbm_gbs"],
                 "traffic": None,
-                "kernel": "grouped_gemm_kernel<32,10> (gate/up + down launches)",
+                "kernel": "grouped_gemm_kernel<32,10> (gate/up + down launches "
+                          "of one expert-FFN call)",
                 "peak_source": f"{peaks['source']} hbm_gbs"}
     else:
         ach = ffn_flops(cfg) / (ffn_ms / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": ach,
                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": ach / peaks["bf16_tflops"], "traffic": None,
-                "kernel": "grouped_gemm_kernel<256,4> (gate/up + down launches)",
+                "frac": ach / peaks["bf16_tflops"],
+                "traffic": MEASURED_TRAFFIC.get(cfg.name),
+                "kernel": "grouped_gemm_pair_kernel (gate/up + down launches "
+                          "of one expert-FFN call)",
                 "peak_source": f"{peaks['source']} bf16_tflops (burst)",
                 "frac_of_sustained": (ach / peaks["bf16_tflops_sustained"]
                                       if peaks["bf16_tflops_sustained"]

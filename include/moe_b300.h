@@ -155,6 +155,15 @@ MOE_API moe_status moe_update_bias(int n_routed, const int32_t* counts,
  * current device.  MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_CHECK.       */
 MOE_API moe_status moe_get_device_error(void* stream);
 
+/* Self-test of the device-side failure detection: launches one kernel whose
+ * single thread waits on a barrier that nothing signals, with a limit of
+ * limit_us microseconds (1 .. 1000000) instead of the pipelines' 2 s.  The
+ * wait gives up, records a timeout in the device error word and the kernel
+ * returns, so the next moe_get_device_error(stream) returns MOE_ERR_TIMEOUT
+ * and the context stays usable.  Every pipeline wait of the library uses
+ * the same bounded-wait routine.                                          */
+MOE_API moe_status moe_selftest_wait_timeout(unsigned limit_us, void* stream);
+
 /* Static description of a status code; detail of the last host-side error
  * of the calling thread.                                                  */
 MOE_API const char* moe_status_string(moe_status status);

@@ -15,7 +15,8 @@ from importlib import import_module
 _FROM_LIB = ("EXPORTED", "LIB", "LIB_PATH", "MOE_BF16", "MOE_F32", "MoEError",
              "MoeShape", "combine", "expert_ffn", "get_device_error",
              "last_launch_count", "make_shape", "pack_weights", "permute",
-             "route", "route_noalloc", "update_bias", "workspace_size")
+             "route", "route_noalloc", "selftest_wait_timeout", "update_bias",
+             "workspace_size")
 _FROM_LAYER = ("Buffers", "MoELayer")
 
 __all__ = list(_FROM_LIB + _FROM_LAYER)

@@ -26,7 +26,7 @@ EXPORTED = ("moe_workspace_size", "moe_pack_weights", "moe_route",
             "moe_permute", "moe_expert_ffn", "moe_combine", "moe_update_bias",
             "moe_get_device_error", "moe_status_string",
             "moe_last_error_detail", "moe_last_launch_count",
-            "moe_route_noalloc")
+            "moe_route_noalloc", "moe_selftest_wait_timeout")
 
 
 class MoEError(RuntimeError):
@@ -63,6 +63,7 @@ def _load() -> ctypes.CDLL:
         "moe_last_error_detail": [],
         "moe_last_launch_count": [],
         "moe_route_noalloc": [SP, P, P, P, P, P, P, V],
+        "moe_selftest_wait_timeout": [ctypes.c_uint, V],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -178,6 +179,12 @@ def update_bias(n_routed, counts, total_assign, gamma, bias,
     _check(LIB.moe_update_bias(int(n_routed), _ptr(counts), int(total_assign),
                                float(gamma), _ptr(bias), _stream(stream)),
            "moe_update_bias")
+
+
+def selftest_wait_timeout(limit_us: int = 20000, stream=None) -> None:
+    """Launch a kernel whose bounded wait must give up (see the header)."""
+    _check(LIB.moe_selftest_wait_timeout(int(limit_us), _stream(stream)),
+           "moe_selftest_wait_timeout")
 
 
 def get_device_error(stream=None) -> None:

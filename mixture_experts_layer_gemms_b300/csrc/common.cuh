@@ -73,9 +73,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Bounded wait for the phase with parity `parity` to complete.  Returns
 // false (and records ERR_TIMEOUT) when the limit passes, or at once when
 // another thread of the CTA already gave up (*abort != 0).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
-                                          volatile int* abort, unsigned kernel,
-                                          unsigned where) {
+__device__ __forceinline__ bool mbar_wait(
+    uint32_t bar, uint32_t parity, volatile int* abort, unsigned kernel,
+    unsigned where, unsigned long long limit_ns = kWaitLimitNs) {
 #pragma unroll 1
   for (int i = 0; i < 64; ++i)
     if (mbar_try_wait(bar, parity)) return true;
@@ -84,7 +84,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (abort != nullptr && *abort) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       if (abort != nullptr) *abort = 1;
       report_error(ERR_TIMEOUT, kernel, where);
       return false;
@@ -374,6 +374,20 @@ __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) {
 enum KernelId : unsigned {
   KID_ROUTE_TC = 1,
   KID_GEMM = 2,
+  KID_SELFTEST = 99,
 };
+
+// Self-test of the bounded wait: one thread waits on an mbarrier that no
+// one arrives on.  The wait gives up after `limit_ns`, records
+// ERR_TIMEOUT in the error word and the kernel returns normally.
+__global__ void wait_timeout_selftest_kernel(unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    const uint32_t b = smem_u32(&bar);
+    mbar_init(b, 1);
+    fence_mbar_init();
+    mbar_wait(b, 0, nullptr, KID_SELFTEST, 1, limit_ns);
+  }
+}
 
 }  // namespace moe

@@ -666,6 +666,16 @@ moe_status moe_get_device_error(void* stream) {
               info[0], info[1]);
 }
 
+moe_status moe_selftest_wait_timeout(unsigned limit_us, void* stream) {
+  g_launches = 0;
+  if (limit_us == 0 || limit_us > 1000000u)
+    return fail(MOE_ERR_INVALID_ARG, "limit_us must be in [1, 1000000]");
+  wait_timeout_selftest_kernel<<<1, 32, 0, as_stream(stream)>>>(
+      1000ull * limit_us);
+  MOE_CHECK_LAUNCH();
+  return MOE_OK;
+}
+
 const char* moe_status_string(moe_status st) {
   switch (st) {
     case MOE_OK: return "ok";

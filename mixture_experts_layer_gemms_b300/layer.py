@@ -118,3 +118,19 @@ class MoELayer:
         return b.h
 
     __call__ = forward
+
+    # --- checkpoint of the routing bias (the layer's only changing state) --
+    def save_state(self, path: str, step: int) -> None:
+        """Write the current bias and the index of the next step."""
+        from .checkpoint import save_bias
+        torch.cuda.current_stream().synchronize()
+        save_bias(path, self.bias, step)
+
+    def load_state(self, path: str) -> int:
+        """Restore the bias in place; returns the step to resume at."""
+        from .checkpoint import load_bias
+        b, step = load_bias(path)
+        if b.size != self.N:
+            raise ValueError(f"checkpoint has {b.size} experts, layer {self.N}")
+        self.bias.copy_(torch.from_numpy(b))
+        return step

@@ -433,3 +433,54 @@ def test_bias_loop_teacher_forced(moe):
                       cfg.top_k)
         want = om.update_bias(b_in, c, cfg.T * cfg.top_k, cfg.gamma)
         assert bias.cpu().numpy().tobytes() == want.tobytes(), step
+
+
+def test_bias_loop_resume_bit_exact(moe, tmp_path):
+    """Checkpoint/resume of the bias loop: 3 steps, save, a fresh bias
+    tensor restored from the file, 3 more steps == 6 uninterrupted steps."""
+    from mixture_experts_layer_gemms_b300.checkpoint import load_bias, save_bias
+    cfg = get_config("skew").with_(T=384, steps=6)
+    t = generate(cfg, "cpu", experts=False)
+    E = t["E"].cuda()
+    sh = _shape(moe, cfg)
+    ws = _ws(moe, sh)
+    idx = torch.empty((cfg.T, cfg.top_k), dtype=torch.int32, device="cuda")
+    gate = torch.empty((cfg.T, cfg.top_k), device="cuda")
+    counts = torch.empty(cfg.n_routed, dtype=torch.int32, device="cuda")
+    us = [step_tokens(cfg, s).cuda() for s in range(cfg.steps)]
+
+    def run(bias, steps):
+        for s in steps:
+            moe.route(sh, us[s], E, bias, idx, gate, counts, ws)
+            moe.update_bias(cfg.n_routed, counts, cfg.T * cfg.top_k,
+                            cfg.gamma, bias)
+        torch.cuda.synchronize()
+        moe.get_device_error()
+    b_full = torch.zeros(cfg.n_routed, device="cuda")
+    run(b_full, range(6))
+    b_half = torch.zeros(cfg.n_routed, device="cuda")
+    run(b_half, range(3))
+    path = str(tmp_path / "bias.ckpt")
+    save_bias(path, b_half, 3)
+    b_loaded, step = load_bias(path)
+    assert step == 3
+    b_resumed = torch.from_numpy(b_loaded.copy()).cuda()
+    run(b_resumed, range(step, 6))
+    assert b_resumed.cpu().numpy().tobytes() == b_full.cpu().numpy().tobytes()
+    assert (b_full.cpu().numpy() != 0).any()
+
+
+def test_wait_timeout_is_reported_and_context_survives(moe):
+    """A bounded device wait that nothing satisfies gives up, is reported as
+    MOE_ERR_TIMEOUT, and the next calls on the same context still work."""
+    moe.get_device_error()                      # start clean
+    moe.selftest_wait_timeout(20000)            # 20 ms limit
+    with pytest.raises(moe.MoEError) as ei:
+        moe.get_device_error()
+    assert ei.value.status == 5
+    moe.get_device_error()                      # cleared
+    cfg = get_config("mid").with_(T=256)
+    t = generate(cfg, "cpu", experts=False)
+    idx, gate, counts = _route_gpu(moe, cfg, t["u"].cuda(), t["E"].cuda(),
+                                   t["b"].cuda())
+    assert counts.sum() == cfg.T * cfg.top_k

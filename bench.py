@@ -36,7 +36,7 @@ METRIC = "MoE-layer tokens/s at V3 shape"
 # launches) from an ncu capture of the same kernel on a smaller case of the
 # same shape, scaled by the units processed (see profiles/
 # grouped_gemm_pair_small_v3dims.md).  None where no capture exists.
-MEASURED_TRAFFIC = {"v3_prefill": 26.5e9}
+MEASURED_TRAFFIC = {}
 L2_NOTE = "inputs larger than L2 (22.5 GB of expert weights read per step)"
 
 
@@ -68,10 +68,11 @@ def ffn_bytes(cfg, counts) -> float:
     received tokens plus the shared experts (read once), the routed and
     shared input rows, and the fp32 outputs."""
     es = 2 if cfg.dtype == "bf16" else 4
+    ys = 2 if cfg.dtype == "bf16" else 4      # expert outputs fp16 / fp32
     touched = int((np.asarray(counts) > 0).sum())
     w = 3.0 * cfg.d * cfg.d_ff * es * (touched + cfg.n_shared)
     A = cfg.T * cfg.top_k
-    act = A * cfg.d * es + cfg.T * cfg.d * es + (A + cfg.T) * cfg.d * 4
+    act = A * cfg.d * es + cfg.T * cfg.d * es + (A + cfg.T) * cfg.d * ys
     return w + act
 
 

@@ -30,8 +30,9 @@
  *    d a multiple of 128; n_routed <= 256 and a multiple of 16 for bf16
  *    (<= 1024 for fp32); 1 <= top_k <= min(16, n_routed); 0 <= n_shared <= 8.
  *    Violations return MOE_ERR_UNSUPPORTED (shape) or MOE_ERR_INVALID_ARG.
- *  - Element type of u, E, weights and x_perm: shape->dtype.  y_perm,
- *    y_shared, bias and topk_gate are fp32; indices and counts int32.
+ *  - Element type of u, E, weights and x_perm: shape->dtype.  y_perm and
+ *    y_shared are fp16 when dtype is bf16 and fp32 when dtype is fp32.
+ *    bias and topk_gate are fp32; indices and counts int32.
  *  - The library never aborts the process.
  */
 #ifndef MOE_B300_H
@@ -123,9 +124,12 @@ MOE_API moe_status moe_permute(const moe_shape* shape, const void* u,
  *  y_perm [T*K, d]: rows [offsets[e], offsets[e+1]) = FFN^(r)_e of those
  *     x_perm rows, from w_gu_packed and w_down [n_routed, d, d_ff];
  *  y_shared [T, d] = sum_s FFN^(s)_s(u) (not written when n_shared == 0).
- * y_perm and y_shared are fp32 for both dtypes.  bf16: tcgen05 tensor-core
- * GEMMs, fp32 accumulation in TMEM, H = SiLU(gate)*up rounded to bf16 in
- * the workspace (it is the second GEMM's operand).  fp32: fp32 FMA.       */
+ * bf16: tcgen05 tensor-core GEMMs, fp32 accumulation in TMEM, H =
+ * SiLU(gate)*up rounded to bf16 in the workspace (the second GEMM's
+ * operand), y rounded once to fp16 (11 significant bits); an output
+ * outside the fp16 range is reported as MOE_ERR_DEVICE_CHECK by
+ * moe_get_device_error, never stored silently as inf.  fp32: fp32 FMA and
+ * fp32 y.                                                                 */
 MOE_API moe_status moe_expert_ffn(const moe_shape* shape, const void* x_perm,
                           const int32_t* offsets, const void* w_gu_packed,
                           const void* w_down, const void* u,

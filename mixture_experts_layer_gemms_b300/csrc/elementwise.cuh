@@ -32,23 +32,33 @@ struct Vec<float> {
   }
 };
 
-// Loads V consecutive fp32 values (V = 4 or 8) as float4s.
+// Loads V consecutive expert outputs (fp32 or fp16; V = 4 or 8) as fp32.
 template <int V>
-__device__ __forceinline__ void load_f32(const float* p, float* f) {
+__device__ __forceinline__ void load_y(const float* p, float* f) {
 #pragma unroll
   for (int i = 0; i < V; i += 4) {
     const float4 v = __ldg(reinterpret_cast<const float4*>(p + i));
     f[i] = v.x; f[i + 1] = v.y; f[i + 2] = v.z; f[i + 3] = v.w;
   }
 }
+template <int V>
+__device__ __forceinline__ void load_y(const __half* p, float* f) {
+#pragma unroll
+  for (int i = 0; i < V; i += 4) {
+    const uint2 v = __ldg(reinterpret_cast<const uint2*>(p + i));
+    const __half2* h = reinterpret_cast<const __half2*>(&v);
+    const float2 a = __half22float2(h[0]), b = __half22float2(h[1]);
+    f[i] = a.x; f[i + 1] = a.y; f[i + 2] = b.x; f[i + 3] = b.y;
+  }
+}
 
 // h[t] = u[t] + y_shared[t] + sum_k gate[t,k] * y_perm[inv[t,k]], fp32 in
-// that order (y_perm, y_shared are fp32).  One CTA per token, 16-byte
-// vectors of u along d.
-template <typename TI, typename TO>
+// that order (y_perm, y_shared are TY: fp16 or fp32).  One CTA per token,
+// 16-byte vectors of u along d.
+template <typename TI, typename TY, typename TO>
 __global__ void __launch_bounds__(128)
-combine_kernel(const TI* __restrict__ u, const float* __restrict__ y_perm,
-               const float* __restrict__ y_shared, const int* __restrict__ inv,
+combine_kernel(const TI* __restrict__ u, const TY* __restrict__ y_perm,
+               const TY* __restrict__ y_shared, const int* __restrict__ inv,
                const float* __restrict__ gate, int T, int d, int K,
                long long total_slots, TO* __restrict__ h) {
   constexpr int V = Vec<TI>::n;
@@ -70,7 +80,7 @@ combine_kernel(const TI* __restrict__ u, const float* __restrict__ y_perm,
     float acc[V], tmp[V];
     Vec<TI>::load(u + static_cast<size_t>(t) * d + v * V, acc);
     if (y_shared != nullptr) {
-      load_f32<V>(y_shared + static_cast<size_t>(t) * d + v * V, tmp);
+      load_y<V>(y_shared + static_cast<size_t>(t) * d + v * V, tmp);
 #pragma unroll
       for (int i = 0; i < V; ++i) acc[i] += tmp[i];
     }
@@ -78,7 +88,7 @@ combine_kernel(const TI* __restrict__ u, const float* __restrict__ y_perm,
       const int s = slot_s[k];
       if (s < 0) continue;
       const float g = gate_s[k];
-      load_f32<V>(y_perm + static_cast<size_t>(s) * d + v * V, tmp);
+      load_y<V>(y_perm + static_cast<size_t>(s) * d + v * V, tmp);
 #pragma unroll
       for (int i = 0; i < V; ++i) acc[i] = fmaf(g, tmp[i], acc[i]);
     }

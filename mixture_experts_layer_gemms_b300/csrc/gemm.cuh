@@ -53,6 +53,7 @@ struct GemmParams {
   void* out_shared;
   long long ld_shared;
   int swiglu;
+  int y_fp16;           // down pass: store Y as fp16 (else fp32)
   int* item_counter;    // zeroed before the launch; CTAs claim items from it
 };
 
@@ -141,19 +142,35 @@ __device__ __forceinline__ void epilogue_store(uint32_t taddr, int n_valid,
                                                int b_row, void* out,
                                                long long ld, int col0,
                                                bool swiglu, float* xchg, int q,
-                                               int ep, int lane) {
+                                               int ep, int lane,
+                                               bool y_fp16 = false) {
   (void)ep;
+  bool overflow = false;
   for (int n0 = 0; n0 < n_valid; n0 += 32) {
     uint32_t r[32];
     tmem_ld32(taddr + n0, r);
     tmem_ld_wait();
     const int nleft = n_valid - n0;   // tokens of this chunk that exist
     if (!swiglu) {
-      float* dst = static_cast<float*>(out) +
-                   static_cast<size_t>(b_row + n0) * ld + col0 + q * 32 + lane;
+      const size_t off =
+          static_cast<size_t>(b_row + n0) * ld + col0 + q * 32 + lane;
+      if (y_fp16) {
+        // fp16 keeps 11 significant bits (8x finer than bf16); values
+        // beyond its range are reported, never written silently as inf
+        __half* dst = static_cast<__half*>(out) + off;
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (j < nleft) dst[static_cast<size_t>(j) * ld] = __uint_as_float(r[j]);
+        for (int j = 0; j < 32; ++j)
+          if (j < nleft) {
+            const float v = __uint_as_float(r[j]);
+            overflow |= !(fabsf(v) <= 65504.f);
+            dst[static_cast<size_t>(j) * ld] = __float2half_rn(v);
+          }
+      } else {
+        float* dst = static_cast<float*>(out) + off;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j < nleft) dst[static_cast<size_t>(j) * ld] = __uint_as_float(r[j]);
+      }
       continue;
     }
     const bool gate_warp = q < 2;
@@ -178,6 +195,7 @@ __device__ __forceinline__ void epilogue_store(uint32_t taddr, int n_valid,
     }
     named_bar_sync(1, 128);
   }
+  if (overflow) report_error(ERR_CHECK, KID_GEMM, 200);
 }
 
 // K-block visited at step i of an item (plain ascending order).
@@ -459,7 +477,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA_r,
       epilogue_store(tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * BN,
                      t.n_valid, t.b_row, out, ld,
                      p.swiglu ? t.wt * 64 : t.wt * 128, p.swiglu != 0, stg,
-                     q, ep, lane);
+                     q, ep, lane, p.y_fp16 != 0);
       tc_fence_before();
       mbar_arrive(bar_tempty + 8 * acc);
       if (++acc == 2) {

@@ -578,6 +578,7 @@ moe_status moe_expert_ffn(const moe_shape* s, const void* x_perm,
   p.out_shared = y_shared;
   p.ld_shared = d;
   p.swiglu = 0;
+  p.y_fp16 = 1;
   p.item_counter = ctr + 1;
   st = pair ? launch_gemm_pair(a_r, b_r, a_s, b_s, b_r64, b_s64, b_r128,
                                b_s128, p, cs)
@@ -605,26 +606,29 @@ moe_status moe_combine(const moe_shape* s, const void* u, const void* y_perm,
   const void* ys = s->n_shared > 0 ? y_shared : nullptr;
   const long long A = static_cast<long long>(s->T) * s->top_k;
   cudaStream_t cs = as_stream(stream);
-  const float* y = static_cast<const float*>(y_perm);
-  const float* z = static_cast<const float*>(ys);
   if (s->dtype == MOE_BF16) {
+    // bf16 layers keep the expert outputs in fp16
     const __nv_bfloat16* a = static_cast<const __nv_bfloat16*>(u);
+    const __half* y = static_cast<const __half*>(y_perm);
+    const __half* z = static_cast<const __half*>(ys);
     if (h_dtype == MOE_F32)
-      combine_kernel<__nv_bfloat16, float><<<s->T, 128, 0, cs>>>(
+      combine_kernel<__nv_bfloat16, __half, float><<<s->T, 128, 0, cs>>>(
           a, y, z, inv, topk_gate, s->T, s->d, s->top_k, A,
           static_cast<float*>(h));
     else
-      combine_kernel<__nv_bfloat16, __nv_bfloat16><<<s->T, 128, 0, cs>>>(
-          a, y, z, inv, topk_gate, s->T, s->d, s->top_k, A,
-          static_cast<__nv_bfloat16*>(h));
+      combine_kernel<__nv_bfloat16, __half, __nv_bfloat16>
+          <<<s->T, 128, 0, cs>>>(a, y, z, inv, topk_gate, s->T, s->d,
+                                 s->top_k, A, static_cast<__nv_bfloat16*>(h));
   } else {
     const float* a = static_cast<const float*>(u);
+    const float* y = static_cast<const float*>(y_perm);
+    const float* z = static_cast<const float*>(ys);
     if (h_dtype == MOE_F32)
-      combine_kernel<float, float><<<s->T, 128, 0, cs>>>(
+      combine_kernel<float, float, float><<<s->T, 128, 0, cs>>>(
           a, y, z, inv, topk_gate, s->T, s->d, s->top_k, A,
           static_cast<float*>(h));
     else
-      combine_kernel<float, __nv_bfloat16><<<s->T, 128, 0, cs>>>(
+      combine_kernel<float, float, __nv_bfloat16><<<s->T, 128, 0, cs>>>(
           a, y, z, inv, topk_gate, s->T, s->d, s->top_k, A,
           static_cast<__nv_bfloat16*>(h));
   }

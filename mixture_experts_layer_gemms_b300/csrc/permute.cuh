@@ -69,8 +69,11 @@ static __device__ void block_exclusive_scan(const int* v, int* out, int n,
 
 // Slots of chunk c.  offsets = exclusive scan of counts (every CTA computes
 // it; CTA 0 writes it).  Expert e's slots for this chunk start at
-// offsets[e] + sum_{c'<c} chunk_hist[c'][e]; inside the chunk, thread e walks
-// the chunk's assignments in (token, k) order, so slots follow token order.
+// offsets[e] + sum_{c'<c} chunk_hist[c'][e].  Inside the chunk, warp 0 walks
+// the assignments in (token, k) order 32 at a time: lanes holding the same
+// expert find each other with __match_any_sync, take consecutive slots in
+// lane order, and the first of them advances that expert's running slot --
+// so slots follow token order and nothing depends on atomics.
 __global__ void __launch_bounds__(256)
 permute_slots_kernel(const int* __restrict__ topk_idx,
                      const int* __restrict__ counts,
@@ -79,7 +82,7 @@ permute_slots_kernel(const int* __restrict__ topk_idx,
                      int* __restrict__ inv) {
   __shared__ int cnt[1024];
   __shared__ int offs[1025];
-  __shared__ int base[1024];
+  __shared__ int run[1024];
   __shared__ int idx_s[kPermChunk * 16];
   __shared__ int warp_tot[8];
   for (int e = threadIdx.x; e < N; e += blockDim.x) cnt[e] = counts[e];
@@ -91,7 +94,7 @@ permute_slots_kernel(const int* __restrict__ topk_idx,
   for (int e = threadIdx.x; e < N; e += blockDim.x) {
     int b = offs[e];
     for (int cc = 0; cc < c; ++cc) b += chunk_hist[static_cast<size_t>(cc) * N + e];
-    base[e] = b;
+    run[e] = b;
   }
   const int t0 = c * kPermChunk;
   const int nt = min(kPermChunk, T - t0);
@@ -101,18 +104,30 @@ permute_slots_kernel(const int* __restrict__ topk_idx,
   __syncthreads();
   // slots never exceed the T*K assignments, whatever counts say
   const int total = min(offs[N], T * K);
-  for (int e = threadIdx.x; e < N; e += blockDim.x) {
-    int slot = base[e];
-    for (int a = 0; a < na; ++a) {
-      if (idx_s[a] == e) {
-        if (slot < total) {
-          inv[static_cast<size_t>(t0) * K + a] = slot;
-          perm[slot] = t0 + a / K;
-        } else {
-          report_error(ERR_CHECK, 11, static_cast<unsigned>(slot));
-        }
-        ++slot;
+  if (threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
+  const unsigned lt = (1u << lane) - 1u;
+  for (int a0 = 0; a0 < na; a0 += 32) {
+    const int a = a0 + lane;
+    const bool valid = a < na;
+    const int e = valid ? idx_s[a] : -1;
+    const bool good = valid && e >= 0 && e < N;
+    const unsigned m = __match_any_sync(0xffffffffu, good ? e : N + lane);
+    const int rank = __popc(m & lt);
+    const int base = good ? run[e] : 0;
+    __syncwarp();
+    if (good && rank == 0) run[e] = base + __popc(m);
+    __syncwarp();
+    if (good) {
+      const int slot = base + rank;
+      if (slot < total) {
+        inv[static_cast<size_t>(t0) * K + a] = slot;
+        perm[slot] = t0 + a / K;
+      } else {
+        report_error(ERR_CHECK, 11, static_cast<unsigned>(slot));
       }
+    } else if (valid) {
+      report_error(ERR_CHECK, 13, static_cast<unsigned>(t0 * K + a));
     }
   }
 }

@@ -50,6 +50,9 @@ class MoELayer:
         self.S = 0 if ws_gate is None else ws_gate.shape[0]
         self.K = int(top_k)
         self.h_dtype = h_dtype
+        # expert outputs: fp16 for bf16 layers, fp32 for fp32 layers
+        self.y_dtype = torch.float16 if E.dtype == torch.bfloat16 \
+            else torch.float32
         self.E, self.bias, self.w_down = E, bias, w_down
         dev, dt = E.device, E.dtype
         self.w_gu = torch.empty((self.N, 2 * self.I, self.d), dtype=dt,
@@ -86,9 +89,9 @@ class MoELayer:
             perm=torch.empty((max(A, 1),), **i32),
             inv=torch.empty((T, K), **i32),
             x_perm=torch.empty((max(A, 1), self.d), dtype=dt, device=dev),
-            y_perm=torch.empty((max(A, 1), self.d), dtype=torch.float32,
+            y_perm=torch.empty((max(A, 1), self.d), dtype=self.y_dtype,
                                device=dev),
-            y_shared=(torch.empty((T, self.d), dtype=torch.float32,
+            y_shared=(torch.empty((T, self.d), dtype=self.y_dtype,
                                   device=dev) if self.S else None),
             h=torch.empty((T, self.d), dtype=self.h_dtype, device=dev),
             workspace=torch.empty((max(ws, 256),), dtype=torch.uint8,

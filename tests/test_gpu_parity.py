@@ -246,9 +246,10 @@ def test_combine_parity(moe, dtype, hdt):
     off, perm, inv = om.permute(idx, counts)
     dt = torch.float32 if dtype == "f32" else torch.bfloat16
     gen = torch.Generator().manual_seed(1)
+    ydt = torch.float16 if dtype == "bf16" else torch.float32
     u = torch.randn((T, d), generator=gen).to(dt)
-    y = torch.randn((T * K, d), generator=gen)
-    ys = torch.randn((T, d), generator=gen)
+    y = torch.randn((T * K, d), generator=gen).to(ydt)
+    ys = torch.randn((T, d), generator=gen).to(ydt)
     gate = torch.rand((T, K), generator=gen)
     ref = om.combine(as_f64(u), as_f64(y), as_f64(ys), inv, as_f64(gate))
     cfg = get_config("tiny").with_(T=T, n_routed=N, top_k=K, d=d, n_shared=S,

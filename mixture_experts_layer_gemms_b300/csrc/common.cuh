@@ -297,6 +297,19 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst,
       "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(x), "r"(y)
       : "memory");
 }
+// 3-D variant (box {64, rows, atoms}: `atoms` 128-byte K-atoms of `rows`
+// rows, stacked atom-major in shared memory).
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst,
+                                                 const CUtensorMap* m, int row,
+                                                 int katom, uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::"
+      "complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(0), "r"(row),
+      "r"(katom)
+      : "memory");
+}
+
 // TMEM allocation shared by a CTA pair: one warp of each CTA executes it.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem,
                                                 uint32_t ncols) {

@@ -33,12 +33,16 @@ namespace moe {
 
 constexpr int kPairBM = 256;       // weight rows per item (128 per CTA)
 constexpr int kPairBN = 256;       // max tokens per item (128 per CTA)
-constexpr int kPairStages = 6;
+// K per pipeline stage: two 64-wide swizzle atoms per operand, loaded by one
+// 3-D TMA box each, one MMA commit per stage.
+constexpr int kPairBK = 128;
+constexpr int kPairAtoms = kPairBK / 64;
+constexpr int kPairStages = 3;
 constexpr int kPairHalfRows = kPairBN / 2;
 
 struct PairSmem {
-  static constexpr int a_bytes = 128 * kGemmBK * 2;            // 16 KB
-  static constexpr int b_bytes = kPairHalfRows * kGemmBK * 2;  // 16 KB
+  static constexpr int a_bytes = 128 * kPairBK * 2;            // 32 KB
+  static constexpr int b_bytes = kPairHalfRows * kPairBK * 2;  // 32 KB
   static constexpr int a_off = 0;
   static constexpr int b_off = a_off + kPairStages * a_bytes;
   static constexpr int stg_off = b_off + kPairStages * b_bytes;
@@ -266,8 +270,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA_r,
                                    : (t.shared ? &tmB_s128 : &tmB_r128));
         const int a_row = t.a_row + static_cast<int>(rank) * 128;
         const int b_row = t.b_row + static_cast<int>(rank) * half;
-        const uint32_t pair_bytes = 2u * (L::a_bytes + box * kGemmBK * 2);
-        const int nk = t.k / kGemmBK;
+        const uint32_t pair_bytes = 2u * (L::a_bytes + box * kPairBK * 2);
+        const int nk = t.k / kPairBK;
         bool ok = true;
         for (int i = 0; i < nk; ++i) {
           if (!mbar_wait_cl(bar_empty + 8 * stage, phase ^ 1, abort_flag,
@@ -277,11 +281,11 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA_r,
           }
           if (leader) mbar_arrive_expect_tx(bar_full + 8 * stage, pair_bytes);
           const uint32_t fb = full_L + 8 * stage;
-          const int kx = i * kGemmBK;
-          tma_load_2d_pair(sbase + L::a_off + stage * L::a_bytes, mA, kx, a_row,
+          const int ka = i * kPairAtoms;
+          tma_load_3d_pair(sbase + L::a_off + stage * L::a_bytes, mA, a_row, ka,
                            fb);
-          tma_load_2d_pair(sbase + L::b_off + stage * L::b_bytes, mB, kx,
-                           b_row, fb);
+          tma_load_3d_pair(sbase + L::b_off + stage * L::b_bytes, mB, b_row, ka,
+                           fb);
           ++issued;
           if (++stage == ST) {
             stage = 0;
@@ -331,7 +335,11 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA_r,
         tc_fence_after();
         const uint32_t d_tmem = tmem + acc * kPairBN;
         const uint32_t idesc = idesc_bf16_f32(kPairBM, t.n_mma);
-        const int nk = t.k / kGemmBK;
+        const int nk = t.k / kPairBK;
+        // token box rows of this item (the K-atom stride of its B stage)
+        const int half = t.n_mma >> 1;
+        const uint32_t b_atom =
+            (half <= 32 ? 32u : (half <= 64 ? 64u : 128u)) * 128u;
         bool ok = true;
         for (int i = 0; i < nk; ++i) {
           if (!mbar_wait_cl(bar_full + 8 * stage, phase, abort_flag, KID_GEMM,
@@ -343,9 +351,12 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA_r,
           const uint32_t a0 = sbase + L::a_off + stage * L::a_bytes;
           const uint32_t b0 = sbase + L::b_off + stage * L::b_bytes;
 #pragma unroll
-          for (int kk = 0; kk < kGemmBK / 16; ++kk)
-            mma_bf16_pair(d_tmem, sdesc_k128(a0 + kk * 32),
-                          sdesc_k128(b0 + kk * 32), idesc, (i | kk) != 0);
+          for (int kk = 0; kk < kPairBK / 16; ++kk) {
+            const uint32_t at = kk >> 2, w = (kk & 3) * 32;
+            mma_bf16_pair(d_tmem, sdesc_k128(a0 + at * (128u * 128u) + w),
+                          sdesc_k128(b0 + at * b_atom + w), idesc,
+                          (i | kk) != 0);
+          }
           mma_commit_pair_mc(bar_empty + 8 * stage, 0x3);
           if (++stage == ST) {
             stage = 0;

@@ -146,6 +146,32 @@ moe_status make_map(CUtensorMap* m, const void* ptr, long long rows,
   return MOE_OK;
 }
 
+// 3-D view of a K-major bf16 operand [rows, cols] as {64, rows, cols/64}
+// with a box of {64, box_rows, atoms}: `atoms` consecutive 64-wide K-atoms
+// of box_rows rows in one TMA load, stacked atom-major in shared memory,
+// 128-byte swizzle.
+moe_status make_map3(CUtensorMap* m, const void* ptr, long long rows,
+                     long long cols, int box_rows, int atoms) {
+  moe_status st = get_encoder();
+  if (st != MOE_OK) return st;
+  cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows > 0 ? rows : 1),
+                        static_cast<cuuint64_t>(cols / 64)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 2, 128};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows),
+                       static_cast<cuuint32_t>(atoms)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                        const_cast<void*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled (3-D) failed (%d) "
+                "rows=%lld cols=%lld box_rows=%d", static_cast<int>(r), rows,
+                cols, box_rows);
+  return MOE_OK;
+}
+
 size_t elem_size(moe_dtype dt) { return dt == MOE_BF16 ? 2 : 4; }
 
 bool aligned16(const void* p) {
@@ -264,11 +290,46 @@ moe_status launch_gemm(const CUtensorMap& a_r, const CUtensorMap& b_r,
   return MOE_OK;
 }
 
-moe_status launch_gemm_pair(const CUtensorMap& a_r, const CUtensorMap& b_r,
-                            const CUtensorMap& a_s, const CUtensorMap& b_s,
-                            const CUtensorMap& b_r64, const CUtensorMap& b_s64,
-                            const CUtensorMap& b_r128,
-                            const CUtensorMap& b_s128, const GemmParams& p,
+// Tensor maps of the CTA-pair GEMM: 3-D views (two K-atoms per box) of the
+// weights (128-row boxes) and tokens (32/64/128-row boxes), routed/shared.
+struct PairMaps {
+  CUtensorMap a_r, a_s, b_r32, b_s32, b_r64, b_s64, b_r128, b_s128;
+};
+
+// k_r / k_s: reduction length (row length) of the routed / shared operands.
+moe_status pair_maps(const void* w_r, long long w_r_rows, const void* x_r,
+                     long long x_r_rows, long long k_r, const void* w_s,
+                     long long w_s_rows, const void* x_s, long long x_s_rows,
+                     long long k_s, PairMaps& m) {
+  moe_status st;
+  const int at = kPairAtoms;
+  if ((st = make_map3(&m.a_r, w_r, w_r_rows, k_r, 128, at)) != MOE_OK)
+    return st;
+  if ((st = make_map3(&m.b_r32, x_r, x_r_rows, k_r, 32, at)) != MOE_OK)
+    return st;
+  if ((st = make_map3(&m.b_r64, x_r, x_r_rows, k_r, 64, at)) != MOE_OK)
+    return st;
+  if ((st = make_map3(&m.b_r128, x_r, x_r_rows, k_r, 128, at)) != MOE_OK)
+    return st;
+  if (w_s != nullptr) {
+    if ((st = make_map3(&m.a_s, w_s, w_s_rows, k_s, 128, at)) != MOE_OK)
+      return st;
+    if ((st = make_map3(&m.b_s32, x_s, x_s_rows, k_s, 32, at)) != MOE_OK)
+      return st;
+    if ((st = make_map3(&m.b_s64, x_s, x_s_rows, k_s, 64, at)) != MOE_OK)
+      return st;
+    if ((st = make_map3(&m.b_s128, x_s, x_s_rows, k_s, 128, at)) != MOE_OK)
+      return st;
+  } else {
+    m.a_s = m.a_r;
+    m.b_s32 = m.b_r32;
+    m.b_s64 = m.b_r64;
+    m.b_s128 = m.b_r128;
+  }
+  return MOE_OK;
+}
+
+moe_status launch_gemm_pair(const PairMaps& m, const GemmParams& p,
                             cudaStream_t cs) {
   long long items = 0;
   if (p.shared_rows > 0)
@@ -282,8 +343,8 @@ moe_status launch_gemm_pair(const CUtensorMap& a_r, const CUtensorMap& b_r,
     return fail(MOE_ERR_CUDA, "CTA-pair GEMM cannot be resident on this GPU");
   const long long n = items < clusters ? items : clusters;
   grouped_gemm_pair_kernel<<<static_cast<int>(2 * n), 192, PairSmem::alloc,
-                             cs>>>(a_r, b_r, a_s, b_s, b_r64, b_s64, b_r128,
-                                   b_s128, p);
+                             cs>>>(m.a_r, m.b_r32, m.a_s, m.b_s32, m.b_r64,
+                                   m.b_s64, m.b_r128, m.b_s128, p);
   MOE_CHECK_LAUNCH();
   return MOE_OK;
 }
@@ -513,23 +574,15 @@ moe_status moe_expert_ffn(const moe_shape* s, const void* x_perm,
   // pass 1: gate/up + SwiGLU -> H
   if ((st = make_map(&a_r, w_gu_packed, 2LL * N * I, d, kGemmBM)) != MOE_OK)
     return st;
-  // token maps with 32-, 64- and 128-row boxes (the CTA-pair kernel loads a
-  // token half-tile with the smallest box that covers it)
-  CUtensorMap b_r64, b_s64, b_r128, b_s128;
+  PairMaps pm;
   if ((st = make_map(&b_r, x_perm, A, d, box)) != MOE_OK) return st;
-  if ((st = make_map(&b_r64, x_perm, A, d, 64)) != MOE_OK) return st;
-  if ((st = make_map(&b_r128, x_perm, A, d, 128)) != MOE_OK) return st;
   if (has_shared) {
     if ((st = make_map(&a_s, ws_gu_packed, 2LL * SI, d, kGemmBM)) != MOE_OK)
       return st;
     if ((st = make_map(&b_s, u, s->T, d, box)) != MOE_OK) return st;
-    if ((st = make_map(&b_s64, u, s->T, d, 64)) != MOE_OK) return st;
-    if ((st = make_map(&b_s128, u, s->T, d, 128)) != MOE_OK) return st;
   } else {
     a_s = a_r;
     b_s = b_r;
-    b_s64 = b_r64;
-    b_s128 = b_r128;
   }
   p.offsets = offsets;
   p.n_groups = N;
@@ -545,29 +598,29 @@ moe_status moe_expert_ffn(const moe_shape* s, const void* x_perm,
   p.ld_shared = SI;
   p.swiglu = 1;
   p.item_counter = ctr;
-  st = pair ? launch_gemm_pair(a_r, b_r, a_s, b_s, b_r64, b_s64, b_r128,
-                               b_s128, p, cs)
-       : small ? launch_gemm<32, 10>(a_r, b_r, a_s, b_s, p, sms, cs)
+  if (pair) {
+    if ((st = pair_maps(w_gu_packed, 2LL * N * I, x_perm, A, d,
+                        has_shared ? ws_gu_packed : nullptr, 2LL * SI,
+                        u, s->T, d, pm)) != MOE_OK)
+      return st;
+    st = launch_gemm_pair(pm, p, cs);
+  } else {
+    st = small ? launch_gemm<32, 10>(a_r, b_r, a_s, b_s, p, sms, cs)
                : launch_gemm<256, 4>(a_r, b_r, a_s, b_s, p, sms, cs);
+  }
   if (st != MOE_OK) return st;
   // pass 2: down -> y
   if ((st = make_map(&a_r, w_down, static_cast<long long>(N) * d, I,
                      kGemmBM)) != MOE_OK)
     return st;
   if ((st = make_map(&b_r, h_r, A, I, box)) != MOE_OK) return st;
-  if ((st = make_map(&b_r64, h_r, A, I, 64)) != MOE_OK) return st;
-  if ((st = make_map(&b_r128, h_r, A, I, 128)) != MOE_OK) return st;
   if (has_shared) {
     if ((st = make_map(&a_s, ws_down_packed, d, SI, kGemmBM)) != MOE_OK)
       return st;
     if ((st = make_map(&b_s, h_s, s->T, SI, box)) != MOE_OK) return st;
-    if ((st = make_map(&b_s64, h_s, s->T, SI, 64)) != MOE_OK) return st;
-    if ((st = make_map(&b_s128, h_s, s->T, SI, 128)) != MOE_OK) return st;
   } else {
     a_s = a_r;
     b_s = b_r;
-    b_s64 = b_r64;
-    b_s128 = b_r128;
   }
   p.w_rows_routed = d;
   p.k_routed = I;
@@ -580,11 +633,15 @@ moe_status moe_expert_ffn(const moe_shape* s, const void* x_perm,
   p.swiglu = 0;
   p.y_fp16 = 1;
   p.item_counter = ctr + 1;
-  st = pair ? launch_gemm_pair(a_r, b_r, a_s, b_s, b_r64, b_s64, b_r128,
-                               b_s128, p, cs)
-       : small ? launch_gemm<32, 10>(a_r, b_r, a_s, b_s, p, sms, cs)
+  if (pair) {
+    if ((st = pair_maps(w_down, static_cast<long long>(N) * d, h_r, A, I,
+                        has_shared ? ws_down_packed : nullptr, d, h_s, s->T,
+                        SI, pm)) != MOE_OK)
+      return st;
+    return launch_gemm_pair(pm, p, cs);
+  }
+  return small ? launch_gemm<32, 10>(a_r, b_r, a_s, b_s, p, sms, cs)
                : launch_gemm<256, 4>(a_r, b_r, a_s, b_s, p, sms, cs);
-  return st;
 }
 
 moe_status moe_combine(const moe_shape* s, const void* u, const void* y_perm,

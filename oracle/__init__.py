@@ -12,5 +12,5 @@ See ``oracle/moe.py`` for the definitions and their sources, and
 from .moe import (  # noqa: F401
     sigmoid, silu, affinity, biased_topk, route, swiglu_ffn, permute,
     expert_ffn, combine, layer_forward, update_bias, relative_load,
-    topk_near_tie_ok,
+    topk_near_tie_ok, group_limited_topk, group_topk_near_tie_ok,
 )

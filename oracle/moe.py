@@ -105,14 +105,89 @@ def biased_topk(s, b, K: int):
     return idx.astype(np.int64), margin
 
 
-def route(u, E, b, K: int):
+def group_limited_topk(s, b, K: int, G: int, M: int):
+    """Top-K_r experts restricted to the M best of G expert groups.
+
+    [report-commentary], training-framework paragraph: each token is sent to
+    at most 4 nodes; [lineage], V3 part: node-limited routing.  The pages
+    give no group-score rule; the reading taken here: experts form G
+    contiguous groups of N/G; a group's score is the largest biased score
+    s + b among its experts; the M groups with the highest score are kept
+    (lower group index first on ties); the top-K of s + b is then taken
+    among the experts of the kept groups only (lower index first on ties).
+
+    Returns (idx [T, K] sorted by (s+b desc, index asc), margin [T]) with
+    margin the smaller of the gap between the K-th and (K+1)-th eligible
+    biased scores and the gap between the M-th and (M+1)-th group scores
+    (either gap being tiny makes the selection fragile under rounding).
+    """
+    s = _f64(s)
+    beta = s + _f64(b)[None, :]
+    T, N = beta.shape
+    if G < 1 or N % G != 0 or not 1 <= M <= G:
+        raise ValueError("need N % G == 0 and 1 <= M <= G")
+    per = N // G
+    if K > M * per:
+        raise ValueError("K larger than the experts of the kept groups")
+    gscore = beta.reshape(T, G, per).max(axis=2)
+    gorder = np.argsort(-gscore, axis=1, kind="stable")[:, :M]
+    eligible = np.zeros((T, G), dtype=bool)
+    np.put_along_axis(eligible, gorder, True, axis=1)
+    masked = np.where(np.repeat(eligible, per, axis=1), beta, -np.inf)
+    order = np.argsort(-masked, axis=1, kind="stable")
+    idx = order[:, :K]
+    rows = np.arange(T)
+    if K < M * per:
+        margin = masked[rows, order[:, K - 1]] - masked[rows, order[:, K]]
+    else:
+        margin = np.full(T, np.inf)
+    if M < G:
+        gs = -np.sort(-gscore, axis=1)
+        margin = np.minimum(margin, gs[:, M - 1] - gs[:, M])
+    return idx.astype(np.int64), margin
+
+
+def group_topk_near_tie_ok(s, b, idx_sel, K: int, G: int, M: int,
+                           tol: float = 1e-5) -> bool:
+    """True when ``idx_sel`` is a valid group-limited top-K of s+b up to
+    ``tol``: distinct experts from at most M groups, each of those groups
+    scoring within tol of the M-th best group score, and the selection a
+    valid top-K (within tol) among the experts of the groups it uses plus
+    every group that scores above the M-th best by more than tol."""
+    beta = _f64(s) + _f64(b)
+    sel = np.asarray(idx_sel)
+    N = beta.size
+    per = N // G
+    if len(set(sel.tolist())) != K:
+        return False
+    gscore = beta.reshape(G, per).max(axis=1)
+    gth = np.sort(gscore)[::-1][M - 1]
+    used = set((sel // per).tolist())
+    if len(used) > M or any(gscore[g] < gth - tol for g in used):
+        return False
+    sure = {g for g in range(G) if gscore[g] > gth + tol}
+    if not sure <= used and len(sure | used) > M:
+        return False
+    pool = sorted(used | sure)
+    elig = np.concatenate([np.arange(g * per, (g + 1) * per) for g in pool])
+    sub = beta[elig]
+    pos = {int(e): i for i, e in enumerate(elig)}
+    return topk_near_tie_ok(sub, np.zeros_like(sub),
+                            [pos[int(e)] for e in sel], K, tol)
+
+
+def route(u, E, b, K: int, groups=None):
     """Routing of [V3-paper-notes] 2.2: affinity, biased top-K, gate, load.
 
     Returns dict with s [T,N], idx [T,K], gate [T,K] (= s at idx, never s+b),
     counts [N] (tokens per expert over the whole batch) and margin [T].
+    ``groups=(G, M)`` selects the group-limited variant.
     """
     s = affinity(u, E)
-    idx, margin = biased_topk(s, b, K)
+    if groups is None:
+        idx, margin = biased_topk(s, b, K)
+    else:
+        idx, margin = group_limited_topk(s, b, K, *groups)
     gate = np.take_along_axis(s, idx, axis=1)
     counts = np.bincount(idx.ravel(), minlength=s.shape[1]).astype(np.int64)
     return {"s": s, "idx": idx, "gate": gate, "counts": counts,

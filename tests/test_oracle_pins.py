@@ -213,6 +213,53 @@ def check_bias_sign_dynamics():
     return ok, "" if ok else f"max load {first:.2f} -> {last:.2f}"
 
 
+def check_golden_group_routing():
+    g = _load("group_routing_worked_example.json")
+    beta = np.array(g["beta"])[None, :]
+    s = beta.copy()
+    b = np.zeros(beta.shape[1])
+    for c in g["cases"]:
+        idx, _ = om.group_limited_topk(s, b, c["K"], g["G"], g["M"])
+        if idx[0].tolist() != c["idx"]:
+            return False, f"K={c['K']}: {idx[0].tolist()}"
+        if "ungrouped" in c:
+            u_idx, _ = om.biased_topk(s, b, c["K"])
+            if u_idx[0].tolist() != c["ungrouped"]:
+                return False, "ungrouped"
+    t = g["ties"]
+    idx, _ = om.group_limited_topk(np.full_like(s, 0.5), b, t["K"], g["G"],
+                                   g["M"])
+    if idx[0].tolist() != t["idx"]:
+        return False, f"ties: {idx[0].tolist()}"
+    return True, ""
+
+
+def check_group_bruteforce(T=40, N=12, G=4, M=2, K=3, seed=11):
+    """Enumerate every choice of M groups: the kept groups are the unique set
+    whose weakest group score beats every group left out, and the experts
+    are the unique top-K of the pool of kept groups (continuous scores, no
+    ties)."""
+    rng = np.random.default_rng(seed)
+    s = scipy.special.expit(rng.standard_normal((T, N)))
+    b = rng.uniform(-0.05, 0.05, N)
+    idx, _ = om.group_limited_topk(s, b, K, G, M)
+    beta = s + b
+    per = N // G
+    for t in range(T):
+        gsc = beta[t].reshape(G, per).max(axis=1)
+        kept = [S for S in itertools.combinations(range(G), M)
+                if min(gsc[list(S)]) > max(np.delete(gsc, list(S)))]
+        if len(kept) != 1:
+            return False, f"token {t}: {len(kept)} group sets"
+        pool = [e for g_ in kept[0] for e in range(g_ * per, (g_ + 1) * per)]
+        best = [S for S in itertools.combinations(pool, K)
+                if min(beta[t, list(S)]) >
+                max(beta[t, [e for e in pool if e not in S]])]
+        if len(best) != 1 or set(best[0]) != set(idx[t].tolist()):
+            return False, f"token {t}: {idx[t]} vs {best}"
+    return True, ""
+
+
 # --- the pins as tests ----------------------------------------------------
 
 def test_golden_routing():
@@ -518,3 +565,55 @@ def test_mutant_is_caught(name, monkeypatch):
         except Exception:          # a crash also counts as caught
             ok = False
         assert not ok, f"pin {chk.__name__} missed mutant {name}"
+
+
+def test_golden_group_routing():
+    ok, msg = check_golden_group_routing()
+    assert ok, msg
+
+
+def test_group_routing_bruteforce():
+    ok, msg = check_group_bruteforce()
+    assert ok, msg
+
+
+def test_group_routing_reduces_to_plain():
+    """M = G keeps every group: plain routing.  G = N and M = K: each expert
+    is its own group, so the kept groups are the plain top-K experts."""
+    rng = np.random.default_rng(4)
+    s = scipy.special.expit(rng.standard_normal((50, 16)))
+    b = rng.uniform(-0.02, 0.02, 16)
+    plain, _ = om.biased_topk(s, b, 4)
+    a, _ = om.group_limited_topk(s, b, 4, 4, 4)
+    c, _ = om.group_limited_topk(s, b, 4, 16, 4)
+    assert np.array_equal(a, plain) and np.array_equal(c, plain)
+
+
+def test_group_near_tie_check():
+    beta = np.array([0.70, 0.69, 0.20, 0.95, 0.90, 0.85, 0.10, 0.60])
+    z = np.zeros(8)
+    assert om.group_topk_near_tie_ok(beta, z, [3, 4], 2, 4, 2)
+    assert not om.group_topk_near_tie_ok(beta, z, [3, 0], 2, 4, 2)
+    tied = beta.copy()
+    tied[0] = 0.90 - 2e-6          # group 0 now ties group 2 within 1e-5
+    assert om.group_topk_near_tie_ok(tied, z, [3, 0], 2, 4, 2)
+
+
+def _mut_group_score_sum(monkeypatch):
+    def glt(s, b, K, G, M):
+        beta = np.asarray(s, float) + np.asarray(b, float)[None, :]
+        T, N = beta.shape
+        per = N // G
+        gscore = beta.reshape(T, G, per).sum(axis=2)      # wrong rule
+        gorder = np.argsort(-gscore, axis=1, kind="stable")[:, :M]
+        el = np.zeros((T, G), bool)
+        np.put_along_axis(el, gorder, True, axis=1)
+        masked = np.where(np.repeat(el, per, axis=1), beta, -np.inf)
+        return np.argsort(-masked, axis=1, kind="stable")[:, :K], None
+    monkeypatch.setattr(om, "group_limited_topk", glt)
+
+
+def test_mutant_group_score_caught(monkeypatch):
+    _mut_group_score_sum(monkeypatch)
+    ok, _ = check_golden_group_routing()
+    assert not ok

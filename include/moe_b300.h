@@ -108,6 +108,28 @@ MOE_API moe_status moe_route(const moe_shape* shape, const void* u,
                      int32_t* topk_idx, float* topk_gate, int32_t* counts,
                      void* workspace, size_t workspace_bytes, void* stream);
 
+/* Group-limited routing.  The pages name node-limited routing (a token's
+ * experts drawn from at most a few nodes: "解码DeepSeek创新之道：三代模型
+ * 演进路线图", V3 part; at most 4 nodes, the cooktownmusic.com report
+ * commentary, training-framework part) but give no rule for choosing the
+ * nodes.  The rule implemented: the n_routed experts form n_groups groups of
+ * n_routed/n_groups consecutive indices; a group's score is the largest
+ * s+b among its experts; each token keeps the topk_groups best groups (lower
+ * group index first on ties) and takes its top_k experts, by s+b, among the
+ * experts of the kept groups only.  Gates are s, as in moe_route.
+ *  1 <= topk_groups <= n_groups <= 64, n_routed % n_groups == 0,
+ *  topk_groups <= 8 unless topk_groups == n_groups,
+ *  top_k <= topk_groups * n_routed / n_groups; else MOE_ERR_INVALID_ARG or
+ *  MOE_ERR_UNSUPPORTED and nothing is launched.
+ * topk_groups == n_groups (e.g. 1, 1) is exactly moe_route.  Other
+ * arguments, outputs and workspace as moe_route.                          */
+MOE_API moe_status moe_route_grouped(const moe_shape* shape, int n_groups,
+                                     int topk_groups, const void* u,
+                                     const void* centroids, const float* bias,
+                                     int32_t* topk_idx, float* topk_gate,
+                                     int32_t* counts, void* workspace,
+                                     size_t workspace_bytes, void* stream);
+
 /* Dispatch: expert-contiguous copy of the token rows.
  *  offsets [n_routed+1]: exclusive prefix sum of counts (offsets[N] = T*K);
  *  perm [T*K]: token filling each slot; slots of expert e are

@@ -2,8 +2,8 @@
 
 Calls (same names as the C ABI without the ``moe_`` prefix): ``route``,
 ``permute``, ``expert_ffn``, ``combine``, ``update_bias``, plus
-``pack_weights``, ``workspace_size``, ``get_device_error`` and
-``route_noalloc``.  ``MoELayer`` chains them for one forward.
+``pack_weights``, ``workspace_size``, ``get_device_error``,
+``route_grouped`` and ``route_noalloc``.  ``MoELayer`` chains them for one forward.
 
 The shared library is loaded on first use of any of these names; if
 ``libmoe_b300.so`` has not been built
@@ -15,7 +15,8 @@ from importlib import import_module
 _FROM_LIB = ("EXPORTED", "LIB", "LIB_PATH", "MOE_BF16", "MOE_F32", "MoEError",
              "MoeShape", "combine", "expert_ffn", "get_device_error",
              "last_launch_count", "make_shape", "pack_weights", "permute",
-             "route", "route_noalloc", "selftest_wait_timeout", "update_bias",
+             "route", "route_grouped", "route_noalloc",
+             "selftest_wait_timeout", "update_bias",
              "workspace_size")
 _FROM_LAYER = ("Buffers", "MoELayer")
 

@@ -26,7 +26,8 @@ EXPORTED = ("moe_workspace_size", "moe_pack_weights", "moe_route",
             "moe_permute", "moe_expert_ffn", "moe_combine", "moe_update_bias",
             "moe_get_device_error", "moe_status_string",
             "moe_last_error_detail", "moe_last_launch_count",
-            "moe_route_noalloc", "moe_selftest_wait_timeout")
+            "moe_route_noalloc", "moe_selftest_wait_timeout",
+            "moe_route_grouped")
 
 
 class MoEError(RuntimeError):
@@ -64,6 +65,7 @@ def _load() -> ctypes.CDLL:
         "moe_last_launch_count": [],
         "moe_route_noalloc": [SP, P, P, P, P, P, P, V],
         "moe_selftest_wait_timeout": [ctypes.c_uint, V],
+        "moe_route_grouped": [SP, I, I, P, P, P, P, P, P, P, Z, V],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -136,6 +138,17 @@ def route(shape, u, centroids, bias, topk_idx, topk_gate, counts, workspace,
                          _ptr(counts), _ptr(workspace),
                          workspace.numel() * workspace.element_size(),
                          _stream(stream)), "moe_route")
+
+
+def route_grouped(shape, n_groups, topk_groups, u, centroids, bias, topk_idx,
+                  topk_gate, counts, workspace, stream=None) -> None:
+    """moe_route restricted to each token's topk_groups best expert groups."""
+    _check(LIB.moe_route_grouped(ctypes.byref(shape), int(n_groups),
+                                 int(topk_groups), _ptr(u), _ptr(centroids),
+                                 _ptr(bias), _ptr(topk_idx), _ptr(topk_gate),
+                                 _ptr(counts), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(),
+                                 _stream(stream)), "moe_route_grouped")
 
 
 def route_noalloc(shape, u, centroids, bias, topk_idx, topk_gate, counts,

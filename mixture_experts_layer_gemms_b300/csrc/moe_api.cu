@@ -349,6 +349,70 @@ moe_status launch_gemm_pair(const PairMaps& m, const GemmParams& p,
   return MOE_OK;
 }
 
+// Shape, pointer and group checks shared by the routing entry points.
+moe_status check_route_args(const moe_shape* s, int G, int M, const void* u,
+                            const void* centroids, const float* bias,
+                            const int32_t* topk_idx, const float* topk_gate,
+                            const int32_t* counts) {
+  moe_status st = check_shape(s);
+  if (st != MOE_OK) return st;
+  if (s->T > 0) {
+    NEED_PTR(u);
+    NEED_PTR(topk_idx);
+    NEED_PTR(topk_gate);
+  }
+  NEED_PTR(centroids);
+  NEED_PTR(bias);
+  NEED_PTR(counts);
+  if (G < 1 || G > kMaxExpertGroups || s->n_routed % G != 0 || M < 1 || M > G)
+    return fail(MOE_ERR_INVALID_ARG,
+                "n_groups=%d topk_groups=%d: need 1 <= topk_groups <= "
+                "n_groups <= %d and n_routed %% n_groups == 0",
+                G, M, kMaxExpertGroups);
+  if (M < G && M > kMaxTopGroups)
+    return fail(MOE_ERR_UNSUPPORTED, "topk_groups=%d (max %d)", M,
+                kMaxTopGroups);
+  if (static_cast<long long>(M) * (s->n_routed / G) < s->top_k)
+    return fail(MOE_ERR_INVALID_ARG,
+                "top_k=%d exceeds the %d experts of %d kept groups",
+                s->top_k, M * (s->n_routed / G), M);
+  return MOE_OK;
+}
+
+// Router launches; `hist` holds ceil(T/128) * n_routed int32.
+moe_status launch_route(const moe_shape* s, int G, int M, const void* u,
+                        const void* centroids, const float* bias,
+                        int32_t* topk_idx, float* topk_gate, int32_t* counts,
+                        int* hist, cudaStream_t cs) {
+  int sms = 0;
+  moe_status st = device_setup(&sms);
+  if (st != MOE_OK) return st;
+  const int nblk = static_cast<int>(cdiv(s->T, kRouteTile));
+  if (nblk > 0) {
+    if (s->dtype == MOE_BF16) {
+      CUtensorMap tm_u, tm_e;
+      st = make_map(&tm_u, u, s->T, s->d, kRouteTile);
+      if (st != MOE_OK) return st;
+      st = make_map(&tm_e, centroids, s->n_routed, s->d, s->n_routed);
+      if (st != MOE_OK) return st;
+      route_tc_kernel<<<nblk, 128, RouteTcSmemLayout::alloc, cs>>>(
+          tm_u, tm_e, bias, s->T, s->d, s->n_routed, s->top_k, G, M, topk_idx,
+          topk_gate, hist);
+      MOE_CHECK_LAUNCH();
+    } else {
+      route_f32_kernel<<<nblk, 128, 4 * s->n_routed * sizeof(float), cs>>>(
+          static_cast<const float*>(u), static_cast<const float*>(centroids),
+          bias, s->T, s->d, s->n_routed, s->top_k, G, M, topk_idx, topk_gate,
+          hist);
+      MOE_CHECK_LAUNCH();
+    }
+  }
+  route_hist_reduce_kernel<<<static_cast<int>(cdiv(s->n_routed, 256)), 256, 0,
+                             cs>>>(hist, nblk, s->n_routed, counts);
+  MOE_CHECK_LAUNCH();
+  return MOE_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -405,51 +469,31 @@ moe_status moe_pack_weights(const moe_shape* s, const void* w_gate,
   return MOE_OK;
 }
 
+moe_status moe_route_grouped(const moe_shape* s, int n_groups,
+                             int topk_groups, const void* u,
+                             const void* centroids, const float* bias,
+                             int32_t* topk_idx, float* topk_gate,
+                             int32_t* counts, void* ws, size_t ws_bytes,
+                             void* stream) {
+  g_launches = 0;
+  moe_status st = check_route_args(s, n_groups, topk_groups, u, centroids,
+                                   bias, topk_idx, topk_gate, counts);
+  if (st != MOE_OK) return st;
+  st = check_ws(s, ws, ws_bytes);
+  if (st != MOE_OK) return st;
+  const WsLayout w = ws_layout(s);
+  return launch_route(s, n_groups, topk_groups, u, centroids, bias, topk_idx,
+                      topk_gate, counts,
+                      reinterpret_cast<int*>(static_cast<char*>(ws) +
+                                             w.route_hist),
+                      as_stream(stream));
+}
+
 moe_status moe_route(const moe_shape* s, const void* u, const void* centroids,
                      const float* bias, int32_t* topk_idx, float* topk_gate,
                      int32_t* counts, void* ws, size_t ws_bytes, void* stream) {
-  g_launches = 0;
-  moe_status st = check_shape(s);
-  if (st != MOE_OK) return st;
-  if (s->T > 0) {
-    NEED_PTR(u);
-    NEED_PTR(topk_idx);
-    NEED_PTR(topk_gate);
-  }
-  NEED_PTR(centroids);
-  NEED_PTR(bias);
-  NEED_PTR(counts);
-  st = check_ws(s, ws, ws_bytes);
-  if (st != MOE_OK) return st;
-  int sms = 0;
-  st = device_setup(&sms);
-  if (st != MOE_OK) return st;
-  const WsLayout w = ws_layout(s);
-  int* hist = reinterpret_cast<int*>(static_cast<char*>(ws) + w.route_hist);
-  const int nblk = static_cast<int>(cdiv(s->T, kRouteTile));
-  cudaStream_t cs = as_stream(stream);
-  if (nblk > 0) {
-    if (s->dtype == MOE_BF16) {
-      CUtensorMap tm_u, tm_e;
-      st = make_map(&tm_u, u, s->T, s->d, kRouteTile);
-      if (st != MOE_OK) return st;
-      st = make_map(&tm_e, centroids, s->n_routed, s->d, s->n_routed);
-      if (st != MOE_OK) return st;
-      route_tc_kernel<<<nblk, 128, RouteTcSmemLayout::alloc, cs>>>(
-          tm_u, tm_e, bias, s->T, s->d, s->n_routed, s->top_k, topk_idx,
-          topk_gate, hist);
-      MOE_CHECK_LAUNCH();
-    } else {
-      route_f32_kernel<<<nblk, 128, 4 * s->n_routed * sizeof(float), cs>>>(
-          static_cast<const float*>(u), static_cast<const float*>(centroids),
-          bias, s->T, s->d, s->n_routed, s->top_k, topk_idx, topk_gate, hist);
-      MOE_CHECK_LAUNCH();
-    }
-  }
-  route_hist_reduce_kernel<<<static_cast<int>(cdiv(s->n_routed, 256)), 256, 0,
-                             cs>>>(hist, nblk, s->n_routed, counts);
-  MOE_CHECK_LAUNCH();
-  return MOE_OK;
+  return moe_route_grouped(s, 1, 1, u, centroids, bias, topk_idx, topk_gate,
+                           counts, ws, ws_bytes, stream);
 }
 
 moe_status moe_permute(const moe_shape* s, const void* u,
@@ -796,16 +840,9 @@ moe_status moe_route_noalloc(const moe_shape* s, const void* u,
                              int32_t* topk_idx, float* topk_gate,
                              int32_t* counts, void* stream) {
   g_launches = 0;
-  moe_status st = check_shape(s);
+  moe_status st = check_route_args(s, 1, 1, u, centroids, bias, topk_idx,
+                                   topk_gate, counts);
   if (st != MOE_OK) return st;
-  if (s->T > 0) {
-    NEED_PTR(u);
-    NEED_PTR(topk_idx);
-    NEED_PTR(topk_gate);
-  }
-  NEED_PTR(centroids);
-  NEED_PTR(bias);
-  NEED_PTR(counts);
   const long long nblk = cdiv(s->T, kRouteTile);
   const long long need = nblk * s->n_routed;
   if (need > MOE_ROUTE_NOALLOC_MAX_ENTRIES)
@@ -820,31 +857,8 @@ moe_status moe_route_noalloc(const moe_shape* s, const void* u,
   int* hist = nullptr;
   st = noalloc_scratch(&hist);
   if (st != MOE_OK) return st;
-  cudaStream_t cs = as_stream(stream);
-  if (nblk > 0) {
-    if (s->dtype == MOE_BF16) {
-      CUtensorMap tm_u, tm_e;
-      st = make_map(&tm_u, u, s->T, s->d, kRouteTile);
-      if (st != MOE_OK) return st;
-      st = make_map(&tm_e, centroids, s->n_routed, s->d, s->n_routed);
-      if (st != MOE_OK) return st;
-      route_tc_kernel<<<static_cast<int>(nblk), 128, RouteTcSmemLayout::alloc,
-                        cs>>>(tm_u, tm_e, bias, s->T, s->d, s->n_routed,
-                              s->top_k, topk_idx, topk_gate, hist);
-      MOE_CHECK_LAUNCH();
-    } else {
-      route_f32_kernel<<<static_cast<int>(nblk), 128,
-                         4 * s->n_routed * sizeof(float), cs>>>(
-          static_cast<const float*>(u), static_cast<const float*>(centroids),
-          bias, s->T, s->d, s->n_routed, s->top_k, topk_idx, topk_gate, hist);
-      MOE_CHECK_LAUNCH();
-    }
-  }
-  route_hist_reduce_kernel<<<static_cast<int>(cdiv(s->n_routed, 256)), 256, 0,
-                             cs>>>(hist, static_cast<int>(nblk), s->n_routed,
-                                   counts);
-  MOE_CHECK_LAUNCH();
-  return MOE_OK;
+  return launch_route(s, 1, 1, u, centroids, bias, topk_idx, topk_gate,
+                      counts, hist, as_stream(stream));
 }
 
 }  // extern "C"

@@ -87,10 +87,66 @@ __device__ __forceinline__ void select_token(const float* s, int stride,
   top.store(t, K, N, topk_idx, topk_gate, hist);
 }
 
+constexpr int kMaxExpertGroups = 64;  // group mask is one 64-bit word
+constexpr int kMaxTopGroups = 8;
+
+// Group-limited variant.  The pages name node-limited routing
+// ("解码DeepSeek创新之道：三代模型演进路线图", V3 part) and a limit of 4
+// nodes per token (the cooktownmusic.com report commentary, training
+// framework part) without a group-score rule; the reading taken here: the
+// N experts form G groups of N/G consecutive indices; a group scores the
+// largest beta among its experts; the token keeps its M best groups (lower
+// group index first on ties) and takes its top-K experts among them only.
+// Kept groups are visited in ascending order, so candidates still arrive in
+// ascending expert order and TopK's tie rule holds.
+template <int KT>
+__device__ __forceinline__ void select_token_grouped(
+    const float* s, int stride, const float* bias, int N, int K, int G, int M,
+    int t, int* topk_idx, float* topk_gate, int* hist) {
+  const int per = N / G;
+  TopK<kMaxTopGroups> gtop;
+  gtop.reset();
+  for (int g = 0; g < G; ++g) {
+    float gm = -INFINITY;
+    for (int e = g * per; e < (g + 1) * per; ++e)
+      gm = fmaxf(gm, __fadd_rn(s[e * stride], bias[e]));
+    gtop.push(gm, 0.f, g);
+  }
+  unsigned long long keep = 0;
+#pragma unroll
+  for (int j = 0; j < kMaxTopGroups; ++j)
+    if (j < M && gtop.i[j] < G) keep |= 1ull << gtop.i[j];
+  TopK<KT> top;
+  top.reset();
+  while (keep) {
+    const int g = __ffsll(static_cast<long long>(keep)) - 1;
+    keep &= keep - 1;
+    for (int e = g * per; e < (g + 1) * per; ++e) {
+      const float sv = s[e * stride];
+      top.push(__fadd_rn(sv, bias[e]), sv, e);
+    }
+  }
+  top.store(t, K, N, topk_idx, topk_gate, hist);
+}
+
+// G == M keeps every group: plain selection.
 __device__ __forceinline__ void select_token_any(const float* s, int stride,
                                                  const float* bias, int N,
-                                                 int K, int t, int* topk_idx,
+                                                 int K, int G, int M, int t,
+                                                 int* topk_idx,
                                                  float* topk_gate, int* hist) {
+  if (M < G) {
+    if (K <= 4)
+      select_token_grouped<4>(s, stride, bias, N, K, G, M, t, topk_idx,
+                              topk_gate, hist);
+    else if (K <= 8)
+      select_token_grouped<8>(s, stride, bias, N, K, G, M, t, topk_idx,
+                              topk_gate, hist);
+    else
+      select_token_grouped<16>(s, stride, bias, N, K, G, M, t, topk_idx,
+                               topk_gate, hist);
+    return;
+  }
   if (K <= 4)
     select_token<4>(s, stride, bias, N, K, t, topk_idx, topk_gate, hist);
   else if (K <= 8)
@@ -125,7 +181,8 @@ __global__ void __launch_bounds__(128, 1)
 route_tc_kernel(const __grid_constant__ CUtensorMap tm_u,
                 const __grid_constant__ CUtensorMap tm_e,
                 const float* __restrict__ bias, int T, int d, int N, int K,
-                int* __restrict__ topk_idx, float* __restrict__ topk_gate,
+                int G, int M, int* __restrict__ topk_idx,
+                float* __restrict__ topk_gate,
                 int* __restrict__ hist_partial) {
   using L = RouteTcSmemLayout;
   extern __shared__ uint8_t smem_raw[];
@@ -253,7 +310,8 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tm_u,
         if (c0 + j < N) srow[c0 + j] = sigmoid_f32(z[j]);
     }
     if (t < T)
-      select_token_any(srow, 1, bias_s, N, K, t, topk_idx, topk_gate, hist);
+      select_token_any(srow, 1, bias_s, N, K, G, M, t, topk_idx, topk_gate,
+                       hist);
   }
   tc_fence_before();
   __syncthreads();
@@ -271,7 +329,8 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tm_u,
 __global__ void __launch_bounds__(128)
 route_f32_kernel(const float* __restrict__ u, const float* __restrict__ E,
                  const float* __restrict__ bias, int T, int d, int N, int K,
-                 int* __restrict__ topk_idx, float* __restrict__ topk_gate,
+                 int G, int M, int* __restrict__ topk_idx,
+                 float* __restrict__ topk_gate,
                  int* __restrict__ hist_partial) {
   extern __shared__ float zbuf[];        // [4 warps][N]
   __shared__ int hist[1024];
@@ -295,7 +354,7 @@ route_f32_kernel(const float* __restrict__ u, const float* __restrict__ E,
     for (int e = lane; e < N; e += 32) z[e] = sigmoid_f32(z[e]);
     __syncwarp();
     if (lane == 0)
-      select_token_any(z, 1, bias, N, K, t, topk_idx, topk_gate, hist);
+      select_token_any(z, 1, bias, N, K, G, M, t, topk_idx, topk_gate, hist);
     __syncwarp();
   }
   __syncthreads();

@@ -41,7 +41,8 @@ class MoELayer:
                  ws_gate: Optional[torch.Tensor] = None,
                  ws_up: Optional[torch.Tensor] = None,
                  ws_down: Optional[torch.Tensor] = None, top_k: int = 8,
-                 h_dtype: torch.dtype = torch.float32, stream=None):
+                 h_dtype: torch.dtype = torch.float32, stream=None,
+                 n_groups: int = 1, topk_groups: int = 1):
         if not E.is_cuda:
             raise ValueError("MoELayer needs CUDA tensors")
         self.dtype = E.dtype
@@ -49,6 +50,8 @@ class MoELayer:
         self.I = w_gate.shape[1]
         self.S = 0 if ws_gate is None else ws_gate.shape[0]
         self.K = int(top_k)
+        # group-limited routing when topk_groups < n_groups
+        self.n_groups, self.topk_groups = int(n_groups), int(topk_groups)
         self.h_dtype = h_dtype
         # expert outputs: fp16 for bf16 layers, fp32 for fp32 layers
         self.y_dtype = torch.float16 if E.dtype == torch.bfloat16 \
@@ -106,8 +109,9 @@ class MoELayer:
         T = u.shape[0]
         b = self.buffers(T)
         sh = self.shape(T)
-        _lib.route(sh, u, self.E, self.bias, b.topk_idx, b.topk_gate, b.counts,
-                   b.workspace, stream)
+        _lib.route_grouped(sh, self.n_groups, self.topk_groups, u, self.E,
+                           self.bias, b.topk_idx, b.topk_gate, b.counts,
+                           b.workspace, stream)
         _lib.permute(sh, u, b.topk_idx, b.counts, b.offsets, b.perm, b.inv,
                      b.x_perm, b.workspace, stream)
         _lib.expert_ffn(sh, b.x_perm, b.offsets, self.w_gu, self.w_down, u,

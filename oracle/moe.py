@@ -297,7 +297,7 @@ def combine(u, y_perm, y_shared, inv, gate) -> np.ndarray:
 def layer_forward(u, E, b, K: int, routed: Callable[[int], Weights],
                   shared: Sequence[Weights] = (),
                   idx_override: Optional[np.ndarray] = None,
-                  tokens: Optional[np.ndarray] = None):
+                  tokens: Optional[np.ndarray] = None, groups=None):
     """h = u + sum_s FFN^(s)(u) + sum_i g_i FFN^(r)_i(u), by the definition.
 
     No permutation buffer: for each expert, the tokens that selected it are
@@ -306,12 +306,13 @@ def layer_forward(u, E, b, K: int, routed: Callable[[int], Weights],
     near-tied token); the gate is then s at those experts.  ``tokens``
     restricts the output to a subset of rows (sampled checks at full size):
     routing is still computed for those rows only, since it is per token.
+    ``groups=(G, M)`` routes by the group-limited rule.
     Returns (h, routing dict).
     """
     u = _f64(u)
     if tokens is not None:
         u = u[np.asarray(tokens)]
-    r = route(u, E, b, K)
+    r = route(u, E, b, K, groups)
     idx = r["idx"] if idx_override is None else np.asarray(idx_override)
     gate = np.take_along_axis(r["s"], idx, axis=1)
     h = u.copy()

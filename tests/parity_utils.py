@@ -58,8 +58,10 @@ def oracle_weights(t: dict):
     return routed, shared
 
 
-def check_routing(r, b64, idx_gpu, counts_gpu, K, rows=None):
-    """Returns the number of near-tied tokens; asserts the rules above."""
+def check_routing(r, b64, idx_gpu, counts_gpu, K, rows=None, groups=None):
+    """Returns the number of near-tied tokens; asserts the rules above.
+    ``groups=(G, M)``: ``r`` comes from group-limited routing, and a
+    near-tied token is checked against the group-limited rule."""
     idx_gpu = np.asarray(idx_gpu)
     s = r["s"]
     near = r["margin"] < NEAR_TIE
@@ -75,7 +77,11 @@ def check_routing(r, b64, idx_gpu, counts_gpu, K, rows=None):
     ordered = ok & (gaps.min(axis=1, initial=np.inf) >= NEAR_TIE)
     np.testing.assert_array_equal(idx_gpu[ordered], r["idx"][ordered])
     for t in np.nonzero(near)[0]:
-        assert om.topk_near_tie_ok(s[t], b64, idx_gpu[t], K, NEAR_TIE), t
+        if groups is None:
+            assert om.topk_near_tie_ok(s[t], b64, idx_gpu[t], K, NEAR_TIE), t
+        else:
+            assert om.group_topk_near_tie_ok(s[t], b64, idx_gpu[t], K,
+                                             *groups, NEAR_TIE), t
     # counts: consistent with the GPU's own selection, and with the oracle's
     # on every token that is not near-tied
     N = s.shape[1]

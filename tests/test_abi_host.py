@@ -129,3 +129,22 @@ def test_combine_bad_dtype(moe):
 def test_status_strings(moe):
     for code in range(7):
         assert moe.LIB.moe_status_string(code)
+
+
+@pytest.mark.parametrize("G,M,K,code", [
+    (0, 1, 4, 1),       # no groups
+    (3, 1, 4, 1),       # 16 experts do not split into 3 groups
+    (4, 0, 4, 1),       # keep no group
+    (4, 5, 4, 1),       # keep more groups than exist
+    (128, 1, 1, 1),     # more groups than experts / the 64-group limit
+    (16, 9, 4, 2),      # more than 8 kept groups
+    (4, 1, 5, 1),       # top_k above the 4 experts of one kept group
+])
+def test_route_grouped_validation(moe, G, M, K, code):
+    sh = _shape(moe, top_k=K)
+    _, n = _ws(moe, sh)
+    P = ctypes.c_void_p
+    st = moe.LIB.moe_route_grouped(ctypes.byref(sh), G, M, P(256), P(512),
+                                   P(768), P(1024), P(1280), P(1536), P(4096),
+                                   n, None)
+    assert st == code, moe.LIB.moe_last_error_detail()

@@ -28,13 +28,17 @@ def _ws(moe, sh):
                        device="cuda")
 
 
-def _route_gpu(moe, cfg, u, E, b):
+def _route_gpu(moe, cfg, u, E, b, groups=None):
     T, K, N = u.shape[0], cfg.top_k, cfg.n_routed
     sh = _shape(moe, cfg, T)
     idx = torch.full((T, K), -7, dtype=torch.int32, device="cuda")
     gate = torch.empty((T, K), dtype=torch.float32, device="cuda")
     counts = torch.full((N,), -7, dtype=torch.int32, device="cuda")
-    moe.route(sh, u, E, b, idx, gate, counts, _ws(moe, sh))
+    if groups is None:
+        moe.route(sh, u, E, b, idx, gate, counts, _ws(moe, sh))
+    else:
+        moe.route_grouped(sh, groups[0], groups[1], u, E, b, idx, gate,
+                          counts, _ws(moe, sh))
     moe.get_device_error()
     return idx.cpu().numpy(), gate.cpu().numpy(), counts.cpu().numpy()
 
@@ -113,6 +117,96 @@ def test_route_empty_batch(moe, dtype):
     moe.route(sh, None, E, b, None, None, counts, _ws(moe, sh))
     moe.get_device_error()
     assert counts.cpu().tolist() == [0] * cfg.n_routed
+
+
+# -------------------------------------------------------- grouped route --
+GROUP_CASES = {
+    "tiny_f32_G4_M2": ("tiny", {}, (4, 2)),
+    "mid_bf16_G8_M4": ("mid", {}, (8, 4)),
+    "mid_bf16_G32_M1": ("mid", {"top_k": 1}, (32, 1)),
+    "v3_T300_G8_M4": ("v3_prefill", {"T": 300}, (8, 4)),
+    "v3_T300_G64_M8": ("v3_prefill", {"T": 300}, (64, 8)),
+    "skew_T1024_G8_M3": ("skew", {"T": 1024}, (8, 3)),
+}
+
+
+@pytest.mark.parametrize("case", sorted(GROUP_CASES))
+def test_route_grouped_parity(moe, case):
+    name, over, groups = GROUP_CASES[case]
+    cfg = get_config(name).with_(**over)
+    t = generate(cfg, "cpu", experts=False)
+    u, E, b = (t[k].cuda() for k in ("u", "E", "b"))
+    idx, gate, counts = _route_gpu(moe, cfg, u, E, b, groups)
+    b64 = as_f64(t["b"])
+    r = om.route(as_f64(t["u"]), as_f64(t["E"]), b64, cfg.top_k, groups)
+    near = check_routing(r, b64, idx, counts, cfg.top_k, groups=groups)
+    s_at = np.take_along_axis(r["s"], idx.astype(np.int64), axis=1)
+    np.testing.assert_allclose(gate, s_at, rtol=0, atol=GATE_ATOL)
+    # every token's experts come from at most M groups
+    per = cfg.n_routed // groups[0]
+    used = [len(set((row // per).tolist())) for row in idx]
+    assert max(used) <= groups[1]
+    assert near <= max(2, cfg.T // 50) or cfg.zipf is not None, near
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_route_grouped_all_groups_is_plain(moe, dtype):
+    """Keeping every group (M = G) is plain routing, bit for bit."""
+    cfg = get_config("mid").with_(dtype=dtype, T=500)
+    t = generate(cfg, "cpu", experts=False)
+    u, E, b = (t[k].cuda() for k in ("u", "E", "b"))
+    plain = _route_gpu(moe, cfg, u, E, b)
+    for groups in ((1, 1), (8, 8)):
+        got = _route_gpu(moe, cfg, u, E, b, groups)
+        for x, y in zip(plain, got):
+            assert x.tobytes() == y.tobytes(), groups
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_route_grouped_ties(moe, dtype):
+    """E = 0 makes every affinity 1/2, so the bias alone decides.  32
+    experts in 4 groups of 8; biases put groups 1 and 3 level on top."""
+    cfg = get_config("tiny").with_(T=130, dtype=dtype, n_routed=32, top_k=4)
+    dt = torch.float32 if dtype == "f32" else torch.bfloat16
+    u = torch.randn((cfg.T, cfg.d), generator=torch.Generator().manual_seed(1)
+                    ).to(dt).cuda()
+    E = torch.zeros((cfg.n_routed, cfg.d), dtype=dt, device="cuda")
+    bias = np.zeros(32, np.float32)
+    bias[[12, 30, 20]] = [0.25, 0.25, 0.125]
+    bd = torch.from_numpy(bias).cuda()
+    want = {(4, 2): [12, 30, 8, 9],       # groups 1, 3 kept
+            (4, 1): [12, 8, 9, 10],       # tie 1 vs 3 -> group 1
+            (4, 4): [12, 30, 20, 0]}      # plain routing
+    for groups, exp in want.items():
+        idx, gate, counts = _route_gpu(moe, cfg, u, E, bd, groups)
+        assert (idx == np.array(exp)[None, :]).all(), (groups, idx[0])
+        assert (gate == 0.5).all()
+        assert counts[exp].tolist() == [cfg.T] * 4
+        r = om.route(np.zeros((1, cfg.d)), np.zeros((32, cfg.d)),
+                     bias.astype(np.float64), 4, groups)
+        assert r["idx"][0].tolist() == exp
+
+
+def test_route_grouped_full_v3_prefill(moe):
+    """8192 tokens, 256 experts in 8 groups, 4 kept, top-8."""
+    cfg = get_config("v3_prefill")
+    t = generate(cfg, "cuda", experts=False)
+    idx, gate, counts = _route_gpu(moe, cfg, t["u"], t["E"], t["b"], (8, 4))
+    b64 = as_f64(t["b"])
+    r = om.route(as_f64(t["u"]), as_f64(t["E"]), b64, cfg.top_k, (8, 4))
+    check_routing(r, b64, idx, counts, cfg.top_k, groups=(8, 4))
+    assert counts.sum() == cfg.T * cfg.top_k
+
+
+@pytest.mark.parametrize("name,over,groups", [
+    ("mid", {}, (8, 2)),
+    ("v3_prefill", {"T": 200, "n_routed": 64}, (8, 4)),
+])
+def test_layer_grouped_parity(moe, name, over, groups):
+    cfg = get_config(name).with_(**over)
+    t, g = _layer_inputs(cfg)
+    e, near, _ = _layer_check(moe, cfg, t, g, groups=groups)
+    print(name, groups, e, "near-ties", near)
 
 
 # ----------------------------------------------------------- update_bias --
@@ -267,13 +361,16 @@ def test_combine_parity(moe, dtype, hdt):
 
 
 # ------------------------------------------------------- the whole layer --
-def _layer_check(moe, cfg, t, g, tokens=None, h_dtype=torch.float32):
+def _layer_check(moe, cfg, t, g, tokens=None, h_dtype=torch.float32,
+                 groups=None):
+    G, M = (1, 1) if groups is None else groups
     layer = moe.MoELayer(g["E"], g["b"].clone(), g["w_gate"], g["w_up"],
                          g["w_down"],
                          g["ws_gate"] if cfg.n_shared else None,
                          g["ws_up"] if cfg.n_shared else None,
                          g["ws_down"] if cfg.n_shared else None,
-                         top_k=cfg.top_k, h_dtype=h_dtype)
+                         top_k=cfg.top_k, h_dtype=h_dtype, n_groups=G,
+                         topk_groups=M)
     h = layer(g["u"])
     torch.cuda.synchronize()
     moe.get_device_error()
@@ -284,8 +381,8 @@ def _layer_check(moe, cfg, t, g, tokens=None, h_dtype=torch.float32):
     b64 = as_f64(t["b"])
     sel = np.arange(cfg.T) if tokens is None else np.asarray(tokens)
     u64 = as_f64(t["u"][torch.from_numpy(sel).to(t["u"].device)])
-    r = om.route(u64, as_f64(t["E"]), b64, cfg.top_k)
-    near = check_routing(r, b64, idx[sel], None, cfg.top_k)
+    r = om.route(u64, as_f64(t["E"]), b64, cfg.top_k, groups)
+    near = check_routing(r, b64, idx[sel], None, cfg.top_k, groups=groups)
     assert counts.sum() == cfg.T * cfg.top_k
     np.testing.assert_array_equal(
         counts, np.bincount(idx.ravel(), minlength=cfg.n_routed))

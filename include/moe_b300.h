@@ -118,9 +118,8 @@ MOE_API moe_status moe_route(const moe_shape* shape, const void* u,
  * group index first on ties) and takes its top_k experts, by s+b, among the
  * experts of the kept groups only.  Gates are s, as in moe_route.
  *  1 <= topk_groups <= n_groups <= 64, n_routed % n_groups == 0,
- *  topk_groups <= 8 unless topk_groups == n_groups,
- *  top_k <= topk_groups * n_routed / n_groups; else MOE_ERR_INVALID_ARG or
- *  MOE_ERR_UNSUPPORTED and nothing is launched.
+ *  top_k <= topk_groups * n_routed / n_groups; else MOE_ERR_INVALID_ARG and
+ *  nothing is launched.
  * topk_groups == n_groups (e.g. 1, 1) is exactly moe_route.  Other
  * arguments, outputs and workspace as moe_route.                          */
 MOE_API moe_status moe_route_grouped(const moe_shape* shape, int n_groups,
@@ -210,9 +209,11 @@ MOE_API int moe_last_launch_count(void);
  * Arguments and results are those of moe_route (same kernels).  The router's
  * per-block histograms go to a library-owned array in device memory of
  * MOE_ROUTE_NOALLOC_MAX_ENTRIES int32 (1 MiB), which every GPU that loads
- * the library holds until the process exits.  A call needs
- * ceil(T/128) * n_routed entries (for example T up to 131072 tokens with 256
- * experts); larger shapes return MOE_ERR_UNSUPPORTED and launch nothing.
+ * the library holds until the process exits.  A call needs n_routed
+ * entries per router CTA: ceil(T/128) CTAs, or up to 8 per 128-token tile
+ * while the grid stays within one wave of the GPU's SMs (for example T up to
+ * 131072 tokens with 256 experts); larger shapes return MOE_ERR_UNSUPPORTED
+ * and launch nothing.
  * The call allocates nothing (no cudaMalloc, no cudaFree).  Its first call
  * on a device looks up that array's device address (cudaGetSymbolAddress)
  * with the device current; make that first call before any stream capture.

@@ -248,6 +248,12 @@ __device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr,
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v)
                : "memory");
 }
+__device__ __forceinline__ float ld_cluster_f32(uint32_t cluster_addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr)
+               : "memory");
+  return v;
+}
 // try_wait with cluster-scope acquire: for barriers that the peer CTA (or
 // its tensor core) arrives on.
 __device__ __forceinline__ bool mbar_try_wait_cl(uint32_t bar, uint32_t parity) {

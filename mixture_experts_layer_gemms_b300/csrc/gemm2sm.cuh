@@ -274,8 +274,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA_r,
         const int nk = t.k / kPairBK;
         bool ok = true;
         for (int i = 0; i < nk; ++i) {
-          if (!mbar_wait_cl(bar_empty + 8 * stage, phase ^ 1, abort_flag,
-                            KID_GEMM, 103)) {
+          if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag,
+                         KID_GEMM, 103)) {
             ok = false;
             break;
           }
@@ -342,8 +342,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA_r,
             (half <= 32 ? 32u : (half <= 64 ? 64u : 128u)) * 128u;
         bool ok = true;
         for (int i = 0; i < nk; ++i) {
-          if (!mbar_wait_cl(bar_full + 8 * stage, phase, abort_flag, KID_GEMM,
-                            106)) {
+          if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag, KID_GEMM,
+                         106)) {
             ok = false;
             break;
           }
@@ -393,8 +393,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA_r,
       }
       bool ok = got;
       if (got && item < n_items)
-        ok = mbar_wait_cl(bar_tfull + 8 * acc, acc_phase, abort_flag,
-                          KID_GEMM, 108);
+        ok = mbar_wait(bar_tfull + 8 * acc, acc_phase, abort_flag, KID_GEMM,
+                       108);
       const bool wok = __all_sync(0xffffffffu, ok);
       if (lane == 0) ep_ok[ep] = wok ? 1 : 0;
       named_bar_sync(1, 128);

@@ -228,8 +228,9 @@ WsLayout ws_layout(const moe_shape* s) {
   size_t off = 0;
   w.sched = off;                      // item counters of the GEMM passes
   off = round256(off + 2 * sizeof(int));
-  w.route_hist = off;
-  off = round256(off + static_cast<size_t>(nblk) * s->n_routed * 4);
+  w.route_hist = off;   // one histogram per router CTA (<= 8 per tile)
+  off = round256(off + static_cast<size_t>(nblk) * kRtMaxSplit *
+                           s->n_routed * 4);
   w.perm_hist = off;
   off = round256(off + static_cast<size_t>(cdiv(s->T, kPermChunk)) *
                            s->n_routed * 4);
@@ -369,9 +370,6 @@ moe_status check_route_args(const moe_shape* s, int G, int M, const void* u,
                 "n_groups=%d topk_groups=%d: need 1 <= topk_groups <= "
                 "n_groups <= %d and n_routed %% n_groups == 0",
                 G, M, kMaxExpertGroups);
-  if (M < G && M > kMaxTopGroups)
-    return fail(MOE_ERR_UNSUPPORTED, "topk_groups=%d (max %d)", M,
-                kMaxTopGroups);
   if (static_cast<long long>(M) * (s->n_routed / G) < s->top_k)
     return fail(MOE_ERR_INVALID_ARG,
                 "top_k=%d exceeds the %d experts of %d kept groups",
@@ -379,7 +377,14 @@ moe_status check_route_args(const moe_shape* s, int G, int M, const void* u,
   return MOE_OK;
 }
 
-// Router launches; `hist` holds ceil(T/128) * n_routed int32.
+// Router CTAs per 128-token tile on this device (bf16: split of d across a
+// cluster; fp32: 1).
+int route_ctas_per_tile(const moe_shape* s, int sms) {
+  return s->dtype == MOE_BF16 ? route_split(s->T, s->d, sms) : 1;
+}
+
+// Router launches; `hist` holds ceil(T/128) * route_ctas_per_tile int32
+// histograms of n_routed entries.
 moe_status launch_route(const moe_shape* s, int G, int M, const void* u,
                         const void* centroids, const float* bias,
                         int32_t* topk_idx, float* topk_gate, int32_t* counts,
@@ -388,6 +393,7 @@ moe_status launch_route(const moe_shape* s, int G, int M, const void* u,
   moe_status st = device_setup(&sms);
   if (st != MOE_OK) return st;
   const int nblk = static_cast<int>(cdiv(s->T, kRouteTile));
+  const int S = route_ctas_per_tile(s, sms);
   if (nblk > 0) {
     if (s->dtype == MOE_BF16) {
       CUtensorMap tm_u, tm_e;
@@ -395,9 +401,28 @@ moe_status launch_route(const moe_shape* s, int G, int M, const void* u,
       if (st != MOE_OK) return st;
       st = make_map(&tm_e, centroids, s->n_routed, s->d, s->n_routed);
       if (st != MOE_OK) return st;
-      route_tc_kernel<<<nblk, 128, RouteTcSmemLayout::alloc, cs>>>(
-          tm_u, tm_e, bias, s->T, s->d, s->n_routed, s->top_k, G, M, topk_idx,
-          topk_gate, hist);
+      if (S == 1) {
+        route_tc_kernel<<<nblk, kRouteThreads, RouteTcSmemLayout::alloc,
+                          cs>>>(
+            tm_u, tm_e, bias, s->T, s->d, s->n_routed, s->top_k, G, M, 1,
+            topk_idx, topk_gate, hist);
+      } else {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(nblk * S));
+        cfg.blockDim = dim3(kRouteThreads);
+        cfg.dynamicSmemBytes = RouteTcSmemLayout::alloc;
+        cfg.stream = cs;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(S);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        MOE_CHECK_CUDA(cudaLaunchKernelEx(
+            &cfg, route_tc_kernel, tm_u, tm_e, bias, s->T, s->d, s->n_routed,
+            s->top_k, G, M, S, topk_idx, topk_gate, hist));
+      }
       MOE_CHECK_LAUNCH();
     } else {
       route_f32_kernel<<<nblk, 128, 4 * s->n_routed * sizeof(float), cs>>>(
@@ -408,7 +433,7 @@ moe_status launch_route(const moe_shape* s, int G, int M, const void* u,
     }
   }
   route_hist_reduce_kernel<<<static_cast<int>(cdiv(s->n_routed, 256)), 256, 0,
-                             cs>>>(hist, nblk, s->n_routed, counts);
+                             cs>>>(hist, nblk * S, s->n_routed, counts);
   MOE_CHECK_LAUNCH();
   return MOE_OK;
 }
@@ -843,17 +868,18 @@ moe_status moe_route_noalloc(const moe_shape* s, const void* u,
   moe_status st = check_route_args(s, 1, 1, u, centroids, bias, topk_idx,
                                    topk_gate, counts);
   if (st != MOE_OK) return st;
-  const long long nblk = cdiv(s->T, kRouteTile);
-  const long long need = nblk * s->n_routed;
-  if (need > MOE_ROUTE_NOALLOC_MAX_ENTRIES)
-    return fail(MOE_ERR_UNSUPPORTED,
-                "moe_route_noalloc: ceil(T/128)*n_routed = %lld histogram "
-                "entries exceeds the static scratch of %d; use moe_route "
-                "with a workspace",
-                need, MOE_ROUTE_NOALLOC_MAX_ENTRIES);
   int sms = 0;
   st = device_setup(&sms);
   if (st != MOE_OK) return st;
+  const long long nblk = cdiv(s->T, kRouteTile);
+  const long long need = nblk * route_ctas_per_tile(s, sms) * s->n_routed;
+  if (need > MOE_ROUTE_NOALLOC_MAX_ENTRIES)
+    return fail(MOE_ERR_UNSUPPORTED,
+                "moe_route_noalloc: %lld router CTAs x n_routed = %lld "
+                "histogram entries exceeds the static scratch of %d; use "
+                "moe_route with a workspace",
+                nblk * route_ctas_per_tile(s, sms), need,
+                MOE_ROUTE_NOALLOC_MAX_ENTRIES);
   int* hist = nullptr;
   st = noalloc_scratch(&hist);
   if (st != MOE_OK) return st;

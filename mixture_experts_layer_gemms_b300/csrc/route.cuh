@@ -10,166 +10,158 @@ namespace moe {
 constexpr int kRouteTile = 128;   // tokens per CTA (both router variants)
 constexpr int kTopKMax = 16;
 
-// Running top-KT of (beta, index) pairs, best first, in registers (KT is a
-// compile-time size >= K; the first K entries are the top-K).  A pair ranks
-// above another when its beta is larger, or equal with a lower index -- so
-// the lowest index wins a tie, whatever order candidates arrive in.
-template <int KT>
-struct TopK {
-  float b[KT];
-  float s[KT];
-  int i[KT];
+constexpr int kMaxExpertGroups = 64;  // group mask is one 64-bit word
 
-  __device__ __forceinline__ void reset() {
-#pragma unroll
-    for (int j = 0; j < KT; ++j) {
-      b[j] = -INFINITY;
-      s[j] = 0.f;
-      i[j] = 0x7fffffff;
-    }
-  }
-  // Candidates arrive in ascending index order, so a candidate whose beta
-  // only equals the current last entry never enters (the earlier index
-  // keeps its place).
-  __device__ __forceinline__ void push(float beta, float sv, int idx) {
-    if (!(beta > b[KT - 1])) return;
-    float cb = beta, cs = sv;
-    int ci = idx;
-#pragma unroll
-    for (int j = 0; j < KT; ++j) {
-      const bool better = (cb > b[j]) || (cb == b[j] && ci < i[j]);
-      const float tb = b[j], ts = s[j];
-      const int ti = i[j];
-      b[j] = better ? cb : tb;
-      s[j] = better ? cs : ts;
-      i[j] = better ? ci : ti;
-      cb = better ? tb : cb;
-      cs = better ? ts : cs;
-      ci = better ? ti : ci;
-    }
-  }
-  // Writes token t's first K entries and counts them in the CTA histogram.
-  // A slot left empty (only possible with non-finite affinities) is written
-  // as -1 and reported; it is never used as an index.
-  __device__ __forceinline__ void store(int t, int K, int N, int* topk_idx,
-                                        float* topk_gate, int* hist) const {
-#pragma unroll
-    for (int j = 0; j < KT; ++j) {
-      if (j < K) {
-        int e = i[j];
-        if (e < 0 || e >= N) {
-          report_error(ERR_CHECK, KID_ROUTE_TC, static_cast<unsigned>(t));
-          e = -1;
-        } else {
-          atomicAdd(&hist[e], 1);
-        }
-        topk_idx[static_cast<size_t>(t) * K + j] = e;
-        topk_gate[static_cast<size_t>(t) * K + j] = s[j];
-      }
-    }
-  }
-};
-
-// Biased top-K of one token from its affinities s[e * stride] (e < N), fp32:
-// beta = s + b, candidates in ascending expert order.
-template <int KT>
-__device__ __forceinline__ void select_token(const float* s, int stride,
-                                             const float* bias, int N, int K,
-                                             int t, int* topk_idx,
-                                             float* topk_gate, int* hist) {
-  TopK<KT> top;
-  top.reset();
-#pragma unroll 4
-  for (int e = 0; e < N; ++e) {
-    const float sv = s[e * stride];
-    top.push(__fadd_rn(sv, bias[e]), sv, e);
-  }
-  top.store(t, K, N, topk_idx, topk_gate, hist);
+// (beta, e) ranks above (ob, oe): larger beta, or equal beta and lower index.
+__device__ __forceinline__ bool ranks_above(float b, int e, float ob, int oe) {
+  return b > ob || (b == ob && e < oe);
 }
 
-constexpr int kMaxExpertGroups = 64;  // group mask is one 64-bit word
-constexpr int kMaxTopGroups = 8;
-
+// Mask of the M best of G contiguous expert groups for one token, computed
+// by one warp (every lane gets the mask).  A group scores the largest beta
+// among its N/G experts; ties go to the lower group index.
+//
 // Group-limited variant.  The pages name node-limited routing
 // ("解码DeepSeek创新之道：三代模型演进路线图", V3 part) and a limit of 4
 // nodes per token (the cooktownmusic.com report commentary, training
 // framework part) without a group-score rule; the reading taken here: the
 // N experts form G groups of N/G consecutive indices; a group scores the
-// largest beta among its experts; the token keeps its M best groups (lower
-// group index first on ties) and takes its top-K experts among them only.
-// Kept groups are visited in ascending order, so candidates still arrive in
-// ascending expert order and TopK's tie rule holds.
-template <int KT>
-__device__ __forceinline__ void select_token_grouped(
-    const float* s, int stride, const float* bias, int N, int K, int G, int M,
-    int t, int* topk_idx, float* topk_gate, int* hist) {
+// largest beta among its experts; the token keeps its M best groups and
+// takes its top-K experts among them only.
+__device__ __forceinline__ unsigned long long warp_group_mask(
+    const float* s, const float* bias, int N, int G, int M, int lane) {
   const int per = N / G;
-  TopK<kMaxTopGroups> gtop;
-  gtop.reset();
-  for (int g = 0; g < G; ++g) {
-    float gm = -INFINITY;
-    for (int e = g * per; e < (g + 1) * per; ++e)
-      gm = fmaxf(gm, __fadd_rn(s[e * stride], bias[e]));
-    gtop.push(gm, 0.f, g);
+  float g0 = -INFINITY, g1 = -INFINITY;   // groups lane and lane + 32
+  if (lane < G)
+    for (int e = lane * per; e < (lane + 1) * per; ++e)
+      g0 = fmaxf(g0, __fadd_rn(s[e], bias[e]));
+  if (lane + 32 < G)
+    for (int e = (lane + 32) * per; e < (lane + 33) * per; ++e)
+      g1 = fmaxf(g1, __fadd_rn(s[e], bias[e]));
+  int r0 = 0, r1 = 0;                     // groups ranked above each
+  for (int h = 0; h < G; ++h) {
+    const float a = __shfl_sync(0xffffffffu, g0, h & 31);
+    const float c = __shfl_sync(0xffffffffu, g1, h & 31);
+    const float gh = h < 32 ? a : c;
+    r0 += ranks_above(gh, h, g0, lane) ? 1 : 0;
+    r1 += ranks_above(gh, h, g1, lane + 32) ? 1 : 0;
   }
-  unsigned long long keep = 0;
-#pragma unroll
-  for (int j = 0; j < kMaxTopGroups; ++j)
-    if (j < M && gtop.i[j] < G) keep |= 1ull << gtop.i[j];
-  TopK<KT> top;
-  top.reset();
-  while (keep) {
-    const int g = __ffsll(static_cast<long long>(keep)) - 1;
-    keep &= keep - 1;
-    for (int e = g * per; e < (g + 1) * per; ++e) {
-      const float sv = s[e * stride];
-      top.push(__fadd_rn(sv, bias[e]), sv, e);
-    }
-  }
-  top.store(t, K, N, topk_idx, topk_gate, hist);
+  const unsigned lo = __ballot_sync(0xffffffffu, lane < G && r0 < M);
+  const unsigned hi = __ballot_sync(0xffffffffu, lane + 32 < G && r1 < M);
+  return (static_cast<unsigned long long>(hi) << 32) | lo;
 }
 
-// G == M keeps every group: plain selection.
-__device__ __forceinline__ void select_token_any(const float* s, int stride,
-                                                 const float* bias, int N,
-                                                 int K, int G, int M, int t,
-                                                 int* topk_idx,
-                                                 float* topk_gate, int* hist) {
-  if (M < G) {
-    if (K <= 4)
-      select_token_grouped<4>(s, stride, bias, N, K, G, M, t, topk_idx,
-                              topk_gate, hist);
-    else if (K <= 8)
-      select_token_grouped<8>(s, stride, bias, N, K, G, M, t, topk_idx,
-                              topk_gate, hist);
-    else
-      select_token_grouped<16>(s, stride, bias, N, K, G, M, t, topk_idx,
-                               topk_gate, hist);
-    return;
+// Biased top-K of one token by one warp ("【推理llm論文精讀】DeepSeek V3
+// 技術論文", section 2.2: selection over s + b, gate = s).  s[e] (e < N <=
+// 32 PER) are the token's affinities in shared memory; lane j holds experts
+// j, j + 32, ... (conflict-free reads).  K rounds: every lane offers its best
+// remaining candidate, a butterfly max in the order (beta desc, index asc)
+// gives every lane the winner, and its owner retires it -- so the result is
+// sorted and the lowest index wins ties.  With M < G only experts of the
+// token's M best groups compete.  Lanes 0..K-1 write the winners of rounds
+// 0..K-1 and count them in the CTA histogram.  A round without a finite
+// candidate (only with non-finite inputs) writes expert -1 and reports it.
+template <int PER>
+__device__ __forceinline__ void warp_select(const float* s, const float* bias,
+                                            int N, int K, int G, int M, int t,
+                                            int lane, int* topk_idx,
+                                            float* topk_gate, int* hist) {
+  float beta[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int e = lane + 32 * i;
+    beta[i] = e < N ? __fadd_rn(s[e], bias[e]) : -INFINITY;
   }
-  if (K <= 4)
-    select_token<4>(s, stride, bias, N, K, t, topk_idx, topk_gate, hist);
-  else if (K <= 8)
-    select_token<8>(s, stride, bias, N, K, t, topk_idx, topk_gate, hist);
-  else
-    select_token<16>(s, stride, bias, N, K, t, topk_idx, topk_gate, hist);
+  if (M < G) {
+    const unsigned long long keep = warp_group_mask(s, bias, N, G, M, lane);
+    const int per = N / G;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int e = lane + 32 * i;
+      if (e < N && !((keep >> (e / per)) & 1ull)) beta[i] = -INFINITY;
+    }
+  }
+  int mine = -1;
+  for (int k = 0; k < K; ++k) {
+    float bb = -INFINITY;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < PER; ++i)       // ascending index: '>' keeps the lowest
+      if (beta[i] > bb) {
+        bb = beta[i];
+        bi = lane + 32 * i;
+      }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ob = __shfl_xor_sync(0xffffffffu, bb, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ranks_above(ob, oi, bb, bi)) {
+        bb = ob;
+        bi = oi;
+      }
+    }
+    if (lane == k) mine = bi;
+#pragma unroll
+    for (int i = 0; i < PER; ++i)
+      if (lane + 32 * i == bi) beta[i] = -INFINITY;
+  }
+  if (lane < K) {
+    int e = mine;
+    float g = 0.f;
+    if (e < 0 || e >= N) {
+      report_error(ERR_CHECK, KID_ROUTE_TC, static_cast<unsigned>(t));
+      e = -1;
+    } else {
+      g = s[e];
+      atomicAdd(&hist[e], 1);
+    }
+    topk_idx[static_cast<size_t>(t) * K + lane] = e;
+    topk_gate[static_cast<size_t>(t) * K + lane] = g;
+  }
 }
 
 // ------------------------------------------------------------------------
-// bf16 router on the tensor cores.  One CTA = 128 tokens x all N experts:
-// D[token lane, expert column] = u_tile . E^T accumulated in fp32 in TMEM,
-// K-loop over d in 64-wide TMA stages.  Warp 0 lane 0 issues TMA, warp 1
-// lane 0 issues tcgen05.mma; then all 4 warps read their 32 TMEM lanes (one
-// token per thread) and run the sigmoid + biased top-K in fp32.
+// bf16 router on the tensor cores.  A 128-token tile x all N experts is
+// computed by a cluster of S CTAs (S = 1, 2, 4 or 8) that split d:
+// D[token lane, expert column] = u_tile . E^T over the CTA's share of d,
+// accumulated in fp32 in TMEM, K-loop in 64-wide TMA stages.  Warp 0 lane 0
+// issues TMA, warp 1 lane 0 issues tcgen05.mma.  With S = 1 all 4 warps then
+// read their 32 TMEM lanes (one token per thread) and run the sigmoid +
+// biased top-K in fp32.  With S > 1 every CTA dumps its partial z to its own
+// shared memory; CTA r then sums the S partials (in rank order, through
+// distributed shared memory) for tokens r*128/S .. (r+1)*128/S - 1 and
+// selects for those tokens.  Splitting d keeps one wave of CTAs busy when
+// there are fewer tiles than SMs.
 constexpr int kRtStages = 4;
 constexpr int kRtBK = 64;
+constexpr int kRouteThreads = 512;   // 16 warps: 2 pipeline roles, all epilogue
+constexpr int kRtMaxSplit = 8;
+
+// CTAs per token tile: the largest of 1, 2, 4, 8 that keeps the grid within
+// one wave of `sms` CTAs and gives each CTA at least 8 of the 64-wide
+// K-blocks.
+inline int route_split(long long T, int d, int sms) {
+  const long long nblk = (T + kRouteTile - 1) / kRouteTile;
+  int S = 1;
+  while (S < kRtMaxSplit && nblk * S * 2 <= sms && d / kRtBK >= S * 2 * 8)
+    S *= 2;
+  return S;
+}
 
 struct RouteTcSmemLayout {
   static constexpr int a_bytes = kRouteTile * kRtBK * 2;   // 16 KB / stage
   static constexpr int b_bytes_max = 256 * kRtBK * 2;      // 32 KB / stage
   static constexpr int a_off = 0;
   static constexpr int b_off = a_off + kRtStages * a_bytes;
-  static constexpr int bar_off = b_off + kRtStages * b_bytes_max;
+  static constexpr int ring_end = b_off + kRtStages * b_bytes_max;
+  // split epilogue, over the freed ring: partial z [128][N+1] fp32, then
+  // the affinities of this CTA's token slice [128/S][N+1] (S >= 2)
+  static constexpr int zpart_off = 0;
+  static constexpr int zpart_bytes = kRouteTile * 257 * 4;
+  static constexpr int slice_off = zpart_off + zpart_bytes;
+  static constexpr int slice_end = slice_off + (kRouteTile / 2) * 257 * 4;
+  static constexpr int bar_off =
+      ((ring_end > slice_end ? ring_end : slice_end) + 15) & ~15;
   static constexpr int misc_off = bar_off + (2 * kRtStages + 1) * 8;
   static constexpr int hist_off = misc_off + 16;
   static constexpr int bias_off = hist_off + 256 * 4;
@@ -177,11 +169,11 @@ struct RouteTcSmemLayout {
   static constexpr int alloc = total + 1024;   // base re-aligned to 1024
 };
 
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(kRouteThreads, 1)
 route_tc_kernel(const __grid_constant__ CUtensorMap tm_u,
                 const __grid_constant__ CUtensorMap tm_e,
                 const float* __restrict__ bias, int T, int d, int N, int K,
-                int G, int M, int* __restrict__ topk_idx,
+                int G, int M, int split, int* __restrict__ topk_idx,
                 float* __restrict__ topk_gate,
                 int* __restrict__ hist_partial) {
   using L = RouteTcSmemLayout;
@@ -199,8 +191,12 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tm_u,
   float* bias_s = reinterpret_cast<float*>(smem + L::bias_off);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tile = blockIdx.x;
-  const int nk = d / kRtBK;
+  const int S = split;
+  const int rank = S > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int tile = blockIdx.x / S;
+  const int nk_all = d / kRtBK;
+  const int kb_lo = rank * nk_all / S;
+  const int nk = (rank + 1) * nk_all / S - kb_lo;   // this CTA's K-blocks
   const uint32_t b_bytes = static_cast<uint32_t>(N) * kRtBK * 2;
   // The K loop round-robins over n_acc TMEM accumulators (summed in fp32 in
   // the epilogue): each accumulator then sees 1/n_acc of the d/16 MMA
@@ -244,7 +240,7 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tm_u,
     for (int i = 0; i < nk; ++i) {
       const int s = i % kRtStages;
       const uint32_t ph = (i / kRtStages) & 1;
-      const int kb = (kb0 + i) % nk;
+      const int kb = kb_lo + (kb0 + i) % nk;
       if (!mbar_wait(bar_empty + 8 * s, ph ^ 1, abort_flag, KID_ROUTE_TC, 1))
         break;
       ++issued;
@@ -279,39 +275,85 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tm_u,
   }
   __syncwarp();
 
-  // Epilogue: every thread owns one token (TMEM lane).  Its affinities go
-  // to shared memory (the pipeline buffers are free by now), row-major with
-  // a padded stride so a warp's accesses hit distinct banks, then a plain
-  // loop selects the top-K.
+  // Epilogue.  Warp w reads TMEM lane quarter w % 4 (32 token rows, one per
+  // lane) and every fourth 32-column chunk from chunk w / 4, and stores z
+  // summed over the accumulators to shared memory (the pipeline buffers are
+  // free by now), row-major with a padded stride so a warp's stores hit
+  // distinct banks: as affinities s = sigmoid(z) when S = 1, as the raw
+  // partial when S > 1.  Then one warp per token selects (warp_select).
   const bool done_ok = mbar_wait(bar_done, 0, abort_flag, KID_ROUTE_TC, 3);
   tc_fence_after();
   const bool go = __all_sync(0xffffffffu, done_ok && !*abort_flag);
-  const int row = warp * 32 + lane;
-  const int t = tile * kRouteTile + row;
-  float* srow = reinterpret_cast<float*>(smem) + row * (N + 1);
-  if (go) {
-    const int used = min(n_acc, nk);
-    for (int c0 = 0; c0 < N; c0 += 32) {
-      float z[32];
-      uint32_t r[32];
-      const uint32_t ta = tmem + (static_cast<uint32_t>(warp * 32) << 16) + c0;
-      tmem_ld32(ta, r);
-      tmem_ld_wait();
-#pragma unroll
-      for (int j = 0; j < 32; ++j) z[j] = __uint_as_float(r[j]);
-      for (int a = 1; a < used; ++a) {
-        tmem_ld32(ta + a * acc_cols, r);
+  constexpr int kWarps = kRouteThreads / 32;
+  {
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    float* srow = reinterpret_cast<float*>(smem) + row * (N + 1);
+    if (go) {
+      const int used = min(n_acc, nk);
+      for (int c0 = (warp >> 2) * 32; c0 < N; c0 += 32 * (kWarps / 4)) {
+        float z[32];
+        uint32_t r[32];
+        const uint32_t ta = tmem + (static_cast<uint32_t>(q * 32) << 16) + c0;
+        tmem_ld32(ta, r);
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) z[j] += __uint_as_float(r[j]);
-      }
+        for (int j = 0; j < 32; ++j) z[j] = __uint_as_float(r[j]);
+        for (int a = 1; a < used; ++a) {
+          tmem_ld32(ta + a * acc_cols, r);
+          tmem_ld_wait();
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (c0 + j < N) srow[c0 + j] = sigmoid_f32(z[j]);
+          for (int j = 0; j < 32; ++j) z[j] += __uint_as_float(r[j]);
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (c0 + j < N) srow[c0 + j] = S == 1 ? sigmoid_f32(z[j]) : z[j];
+      }
     }
-    if (t < T)
-      select_token_any(srow, 1, bias_s, N, K, G, M, t, topk_idx, topk_gate,
-                       hist);
+  }
+  __syncthreads();
+  if (S == 1) {
+    const float* sfull = reinterpret_cast<const float*>(smem);
+    for (int r = warp; r < kRouteTile; r += kWarps) {
+      const int t = tile * kRouteTile + r;
+      if (go && t < T)
+        warp_select<8>(sfull + r * (N + 1), bias_s, N, K, G, M, t, lane,
+                       topk_idx, topk_gate, hist);
+    }
+  } else {
+    // Every CTA of the cluster passes both cluster barriers, whatever its
+    // own state (a CTA that skipped one would leave the others waiting).
+    cluster_sync();                     // all partials are in place
+    const int R = kRouteTile / S;       // tokens selected by this CTA
+    const int r0 = rank * R;
+    float* slice = reinterpret_cast<float*>(smem + L::slice_off);
+    if (go) {
+      // z = the S partials summed in rank order; the loads of one element
+      // are all issued before they are added
+      const uint32_t zbase = sbase + L::zpart_off;
+      for (int i = threadIdx.x; i < R * N; i += blockDim.x) {
+        const int rl = i / N, c = i - rl * N;
+        const uint32_t off =
+            static_cast<uint32_t>(((r0 + rl) * (N + 1) + c) * 4);
+        float v[kRtMaxSplit];
+#pragma unroll
+        for (int q = 0; q < kRtMaxSplit; ++q)
+          if (q < S) v[q] = ld_cluster_f32(mapa_shared(zbase + off, q));
+        float z = v[0];
+#pragma unroll
+        for (int q = 1; q < kRtMaxSplit; ++q)
+          if (q < S) z += v[q];
+        slice[rl * (N + 1) + c] = sigmoid_f32(z);
+      }
+    }
+    __syncthreads();
+    for (int r = warp; r < R; r += kWarps) {
+      const int t = tile * kRouteTile + r0 + r;
+      if (go && t < T)
+        warp_select<8>(slice + r * (N + 1), bias_s, N, K, G, M, t, lane,
+                       topk_idx, topk_gate, hist);
+    }
+    cluster_sync();                     // no CTA leaves while read remotely
   }
   tc_fence_before();
   __syncthreads();
@@ -353,8 +395,11 @@ route_f32_kernel(const float* __restrict__ u, const float* __restrict__ E,
     __syncwarp();
     for (int e = lane; e < N; e += 32) z[e] = sigmoid_f32(z[e]);
     __syncwarp();
-    if (lane == 0)
-      select_token_any(z, 1, bias, N, K, G, M, t, topk_idx, topk_gate, hist);
+    if (N <= 256)
+      warp_select<8>(z, bias, N, K, G, M, t, lane, topk_idx, topk_gate, hist);
+    else
+      warp_select<32>(z, bias, N, K, G, M, t, lane, topk_idx, topk_gate,
+                      hist);
     __syncwarp();
   }
   __syncthreads();

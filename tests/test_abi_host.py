@@ -137,7 +137,6 @@ def test_status_strings(moe):
     (4, 0, 4, 1),       # keep no group
     (4, 5, 4, 1),       # keep more groups than exist
     (128, 1, 1, 1),     # more groups than experts / the 64-group limit
-    (16, 9, 4, 2),      # more than 8 kept groups
     (4, 1, 5, 1),       # top_k above the 4 experts of one kept group
 ])
 def test_route_grouped_validation(moe, G, M, K, code):

@@ -152,12 +152,22 @@ permute_gather_kernel(const uint4* __restrict__ u, const int* __restrict__ inv,
       }
     }
     const uint4* src = u + static_cast<size_t>(t) * nvec;
-    for (int v = lane; v < nvec; v += 32) {
-      const uint4 val = __ldg(src + v);
+    // four 16-byte loads in flight per lane before the stores
+    for (int v0 = lane; v0 < nvec; v0 += 128) {
+      uint4 val[4];
 #pragma unroll
-      for (int k = 0; k < 16; ++k)
-        if (k < K && slot[k] >= 0)
-          x_perm[static_cast<size_t>(slot[k]) * nvec + v] = val;
+      for (int j = 0; j < 4; ++j)
+        if (v0 + 32 * j < nvec) val[j] = __ldg(src + v0 + 32 * j);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int v = v0 + 32 * j;
+        if (v < nvec) {
+#pragma unroll
+          for (int k = 0; k < 16; ++k)
+            if (k < K && slot[k] >= 0)
+              x_perm[static_cast<size_t>(slot[k]) * nvec + v] = val[j];
+        }
+      }
     }
   }
 }

@@ -6,7 +6,8 @@ never does, and this package never imports the CUDA path: the two share no
 code.  The one common dependency is ``moe_inputs`` (seeded random inputs,
 no layer arithmetic).
 
-See ``oracle/moe.py`` for the definitions and their sources, and
+See ``oracle/moe.py`` for the definitions and their sources,
+``oracle/fp8.py`` for the e4m3 block-scaled expert FFN, and
 ``oracle/micro.py`` for the pure-Python scalar cross-check.
 """
 from .moe import (  # noqa: F401

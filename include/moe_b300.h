@@ -33,6 +33,10 @@
  *  - Element type of u, E, weights and x_perm: shape->dtype.  y_perm and
  *    y_shared are fp16 when dtype is bf16 and fp32 when dtype is fp32.
  *    bias and topk_gate are fp32; indices and counts int32.
+ *  - MOE_FP8: activations (u, h) and the router stay bf16; the expert GEMMs
+ *    run on e4m3 codes with power-of-two block scales (see
+ *    moe_pack_weights_fp8); x_perm is an e4m3 buffer (moe_x_perm_bytes);
+ *    y_perm and y_shared are fp16.  d_ff must be a multiple of 128.
  *  - The library never aborts the process.
  */
 #ifndef MOE_B300_H
@@ -61,7 +65,7 @@ typedef enum {
   MOE_ERR_DEVICE_CHECK = 6   /* a device-side bounds check failed           */
 } moe_status;
 
-typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_FP8 = 2 } moe_dtype;
 
 typedef struct {
   int T;          /* tokens in the batch                                    */
@@ -94,6 +98,41 @@ MOE_API moe_status moe_pack_weights(const moe_shape* shape,
                             const void* ws_down,
                             void* w_gu_packed, void* ws_gu_packed,
                             void* ws_down_packed, void* stream);
+
+/* FP8 expert weights (MOE_FP8).  The pages run most GEMMs on FP8 inputs
+ * with activations and weights grouped into blocks that are scaled on their
+ * own, and promote the tensor cores' partial sums to FP32 every 128
+ * elements of the reduction (DeepSeek-V3 report commentary,
+ * cooktownmusic.com, FP8 training-framework part, Fig. 7a/7b).  The
+ * library's reading of the unstated details:
+ *   element e4m3 (largest finite 448), round to nearest even, saturating;
+ *   weight blocks 128 x 128, activation blocks 1 x 128 along the reduction;
+ *   scale 2^e with e the smallest integer such that the block's largest
+ *   magnitude is <= 448 * 2^e (0 for an all-zero block), stored as fp32;
+ *   codes = e4m3(x * 2^-e).  H = SiLU(G) * U is requantized the same way
+ *   (1 x 128 along d_ff) before the down projection.
+ * moe_fp8_weight_bytes gives the size of each packed buffer (which: 0
+ * routed gate/up, 1 routed down, 2 shared gate/up, 3 shared down); each
+ * holds the codes followed, at the next 256-byte boundary, by the fp32
+ * scales.  moe_pack_weights_fp8 quantizes the bf16 weights (layouts as in
+ * moe_pack_weights, plus w_down [n_routed, d, d_ff]) into them; the shared
+ * arguments may be NULL when n_shared == 0.  Layouts inside the packed
+ * buffers are private to the library.                                    */
+MOE_API moe_status moe_fp8_weight_bytes(const moe_shape* shape, int which,
+                                        size_t* bytes);
+MOE_API moe_status moe_pack_weights_fp8(const moe_shape* shape,
+                                        const void* w_gate, const void* w_up,
+                                        const void* w_down,
+                                        const void* ws_gate, const void* ws_up,
+                                        const void* ws_down, void* w_gu8,
+                                        void* w_down8, void* ws_gu8,
+                                        void* ws_down8, void* stream);
+
+/* Bytes of the x_perm buffer of moe_permute / moe_expert_ffn: T*top_k*d
+ * elements of shape->dtype, or for MOE_FP8 the e4m3 codes [T*top_k, d]
+ * followed, at the next 256-byte boundary, by fp32 scales
+ * [d/128][T*top_k].                                                       */
+MOE_API moe_status moe_x_perm_bytes(const moe_shape* shape, size_t* bytes);
 
 /* Routing (affinity equation, biased selection, routing-weight equation).
  *  u [T, d], centroids E [n_routed, d] (row i = e_i), bias b [n_routed] fp32
@@ -134,7 +173,8 @@ MOE_API moe_status moe_route_grouped(const moe_shape* shape, int n_groups,
  *  perm [T*K]: token filling each slot; slots of expert e are
  *     [offsets[e], offsets[e+1]) in ascending token order (deterministic);
  *  inv [T, top_k]: slot of assignment (t, k);
- *  x_perm [T*K, d]: x_perm[slot] = u[perm[slot]].                         */
+ *  x_perm [T*K, d]: x_perm[slot] = u[perm[slot]] (MOE_FP8: its e4m3 codes
+ *     and 1 x 128 block scales, layout of moe_x_perm_bytes).              */
 MOE_API moe_status moe_permute(const moe_shape* shape, const void* u,
                        const int32_t* topk_idx, const int32_t* counts,
                        int32_t* offsets, int32_t* perm, int32_t* inv,
@@ -150,7 +190,12 @@ MOE_API moe_status moe_permute(const moe_shape* shape, const void* u,
  * operand), y rounded once to fp16 (11 significant bits); an output
  * outside the fp16 range is reported as MOE_ERR_DEVICE_CHECK by
  * moe_get_device_error, never stored silently as inf.  fp32: fp32 FMA and
- * fp32 y.                                                                 */
+ * fp32 y.  MOE_FP8: x_perm from moe_permute, w_gu_packed / w_down /
+ * ws_gu_packed / ws_down_packed are the four moe_pack_weights_fp8 buffers,
+ * u (bf16) is quantized in the workspace for the shared experts; e4m3
+ * tensor-core GEMMs with the block scales applied to the partial sum of
+ * every 128-wide block of the reduction in fp32; H requantized to e4m3 in
+ * the workspace; y fp16 as for bf16.                                      */
 MOE_API moe_status moe_expert_ffn(const moe_shape* shape, const void* x_perm,
                           const int32_t* offsets, const void* w_gu_packed,
                           const void* w_down, const void* u,

@@ -17,7 +17,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoe_b300.so")
 
-MOE_F32, MOE_BF16 = 0, 1
+MOE_F32, MOE_BF16, MOE_FP8 = 0, 1, 2
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
           3: "MOE_ERR_WORKSPACE", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT",
           6: "MOE_ERR_DEVICE_CHECK"}
@@ -27,7 +27,8 @@ EXPORTED = ("moe_workspace_size", "moe_pack_weights", "moe_route",
             "moe_get_device_error", "moe_status_string",
             "moe_last_error_detail", "moe_last_launch_count",
             "moe_route_noalloc", "moe_selftest_wait_timeout",
-            "moe_route_grouped")
+            "moe_route_grouped", "moe_fp8_weight_bytes",
+            "moe_pack_weights_fp8", "moe_x_perm_bytes")
 
 
 class MoEError(RuntimeError):
@@ -66,6 +67,9 @@ def _load() -> ctypes.CDLL:
         "moe_route_noalloc": [SP, P, P, P, P, P, P, V],
         "moe_selftest_wait_timeout": [ctypes.c_uint, V],
         "moe_route_grouped": [SP, I, I, P, P, P, P, P, P, P, Z, V],
+        "moe_fp8_weight_bytes": [SP, I, ctypes.POINTER(ctypes.c_size_t)],
+        "moe_pack_weights_fp8": [SP, P, P, P, P, P, P, P, P, P, P, V],
+        "moe_x_perm_bytes": [SP, ctypes.POINTER(ctypes.c_size_t)],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -94,7 +98,8 @@ def make_shape(T, d, n_routed, top_k, n_shared, d_ff, dtype) -> MoeShape:
     if isinstance(dtype, torch.dtype):
         dt = {torch.float32: MOE_F32, torch.bfloat16: MOE_BF16}[dtype]
     else:
-        dt = {"f32": MOE_F32, "bf16": MOE_BF16}.get(dtype, dtype)
+        dt = {"f32": MOE_F32, "bf16": MOE_BF16, "fp8": MOE_FP8}.get(dtype,
+                                                                 dtype)
     return MoeShape(int(T), int(d), int(n_routed), int(top_k), int(n_shared),
                     int(d_ff), int(dt))
 
@@ -129,6 +134,30 @@ def pack_weights(shape, w_gate, w_up, ws_gate, ws_up, ws_down, w_gu_packed,
                                 _ptr(w_gu_packed), _ptr(ws_gu_packed),
                                 _ptr(ws_down_packed), _stream(stream)),
            "moe_pack_weights")
+
+
+def fp8_weight_bytes(shape, which: int) -> int:
+    """Bytes of a packed e4m3 weight buffer (0 routed gate/up, 1 routed
+    down, 2 shared gate/up, 3 shared down)."""
+    n = ctypes.c_size_t(0)
+    _check(LIB.moe_fp8_weight_bytes(ctypes.byref(shape), int(which),
+                                    ctypes.byref(n)), "moe_fp8_weight_bytes")
+    return int(n.value)
+
+
+def x_perm_bytes(shape) -> int:
+    n = ctypes.c_size_t(0)
+    _check(LIB.moe_x_perm_bytes(ctypes.byref(shape), ctypes.byref(n)),
+           "moe_x_perm_bytes")
+    return int(n.value)
+
+
+def pack_weights_fp8(shape, w_gate, w_up, w_down, ws_gate, ws_up, ws_down,
+                     w_gu8, w_down8, ws_gu8, ws_down8, stream=None) -> None:
+    _check(LIB.moe_pack_weights_fp8(
+        ctypes.byref(shape), _ptr(w_gate), _ptr(w_up), _ptr(w_down),
+        _ptr(ws_gate), _ptr(ws_up), _ptr(ws_down), _ptr(w_gu8), _ptr(w_down8),
+        _ptr(ws_gu8), _ptr(ws_down8), _stream(stream)), "moe_pack_weights_fp8")
 
 
 def route(shape, u, centroids, bias, topk_idx, topk_gate, counts, workspace,

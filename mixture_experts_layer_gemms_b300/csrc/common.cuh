@@ -210,6 +210,26 @@ __device__ __forceinline__ uint64_t sdesc_k128(uint32_t saddr) {
   return d;
 }
 
+// e4m3 x e4m3 -> fp32 (tcgen05.mma kind::f8f6f4): K = 32 per instruction,
+// the same 32-byte step along a 128-byte swizzled row as bf16's K = 16.
+__device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t a_desc,
+                                         uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Instruction descriptor: D fp32, A and B e4m3 (format code 0), K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+  return (1u << 4)                                   // D format f32
+         | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+
 // Instruction descriptor, kind::f16: bf16 A and B (both K-major), fp32 D.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4)                                   // D format f32
@@ -394,6 +414,8 @@ __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) {
 enum KernelId : unsigned {
   KID_ROUTE_TC = 1,
   KID_GEMM = 2,
+  KID_GEMM_FP8 = 3,
+  KID_QUANT = 4,
   KID_SELFTEST = 99,
 };
 

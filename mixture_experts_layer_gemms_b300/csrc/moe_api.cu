@@ -15,6 +15,7 @@
 #include "gemm2sm.cuh"
 #include "permute.cuh"
 #include "route.cuh"
+#include "gemm_fp8.cuh"
 #include "moe_b300.h"
 
 using namespace moe;
@@ -88,6 +89,14 @@ moe_status device_setup(int* sm_count) {
     MOE_CHECK_CUDA(allow_smem(grouped_gemm_kernel<32, 10>,
                               GemmSmem<32, 10>::alloc));
     MOE_CHECK_CUDA(allow_smem(grouped_gemm_pair_kernel, PairSmem::alloc));
+    MOE_CHECK_CUDA(allow_smem(grouped_gemm_fp8_kernel<32, 1, true, 5>,
+                              Fp8Smem<32, 1, true, 5>::alloc));
+    MOE_CHECK_CUDA(allow_smem(grouped_gemm_fp8_kernel<32, 1, false, 10>,
+                              Fp8Smem<32, 1, false, 10>::alloc));
+    MOE_CHECK_CUDA(allow_smem(grouped_gemm_fp8_kernel<128, 2, true, 4>,
+                              Fp8Smem<128, 2, true, 4>::alloc));
+    MOE_CHECK_CUDA(allow_smem(grouped_gemm_fp8_kernel<128, 2, false, 6>,
+                              Fp8Smem<128, 2, false, 6>::alloc));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (di.sm_count / 2));
     cfg.blockDim = dim3(192);
@@ -172,7 +181,31 @@ moe_status make_map3(CUtensorMap* m, const void* ptr, long long rows,
   return MOE_OK;
 }
 
-size_t elem_size(moe_dtype dt) { return dt == MOE_BF16 ? 2 : 4; }
+// element size of activations (and of weights, except for MOE_FP8)
+// e4m3 codes [rows, cols] (one byte each), box {128 bytes, box_rows},
+// 128-byte swizzle.
+moe_status make_map_u8(CUtensorMap* m, const void* ptr, long long rows,
+                       long long cols, int box_rows) {
+  moe_status st = get_encoder();
+  if (st != MOE_OK) return st;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols),
+                        static_cast<cuuint64_t>(rows > 0 ? rows : 1)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols)};
+  cuuint32_t box[2] = {128, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                        const_cast<void*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled (u8) failed (%d) "
+                "rows=%lld cols=%lld box_rows=%d", static_cast<int>(r), rows,
+                cols, box_rows);
+  return MOE_OK;
+}
+
+size_t elem_size(moe_dtype dt) { return dt == MOE_F32 ? 4 : 2; }
 
 bool aligned16(const void* p) {
   return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
@@ -183,7 +216,7 @@ inline size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
 moe_status check_shape(const moe_shape* s) {
   if (s == nullptr) return fail(MOE_ERR_INVALID_ARG, "shape is NULL");
-  if (s->dtype != MOE_F32 && s->dtype != MOE_BF16)
+  if (s->dtype != MOE_F32 && s->dtype != MOE_BF16 && s->dtype != MOE_FP8)
     return fail(MOE_ERR_INVALID_ARG, "dtype %d", static_cast<int>(s->dtype));
   if (s->T < 0 || s->d <= 0 || s->n_routed <= 0 || s->top_k <= 0 ||
       s->n_shared < 0 || s->d_ff <= 0)
@@ -198,11 +231,14 @@ moe_status check_shape(const moe_shape* s) {
                 s->top_k, kTopKMax);
   if (s->n_shared > 8)
     return fail(MOE_ERR_UNSUPPORTED, "n_shared=%d (max 8)", s->n_shared);
-  if (s->dtype == MOE_BF16) {
+  if (s->dtype != MOE_F32) {
     if (s->n_routed > 256 || s->n_routed % 16 != 0)
       return fail(MOE_ERR_UNSUPPORTED,
                   "bf16 n_routed=%d must be a multiple of 16, <= 256",
                   s->n_routed);
+    if (s->dtype == MOE_FP8 && s->d_ff % 128 != 0)
+      return fail(MOE_ERR_UNSUPPORTED,
+                  "fp8: d_ff=%d must be a multiple of 128", s->d_ff);
   } else {
     if (s->n_routed > 1024)
       return fail(MOE_ERR_UNSUPPORTED, "fp32 n_routed=%d (max 1024)",
@@ -217,7 +253,7 @@ moe_status check_shape(const moe_shape* s) {
 }
 
 struct WsLayout {
-  size_t sched, route_hist, perm_hist, h_routed, h_shared, total;
+  size_t sched, route_hist, perm_hist, h_routed, h_shared, u_q, total;
 };
 
 WsLayout ws_layout(const moe_shape* s) {
@@ -238,6 +274,10 @@ WsLayout ws_layout(const moe_shape* s) {
   off = round256(off + static_cast<size_t>(A) * s->d_ff * es);
   w.h_shared = off;
   off = round256(off + static_cast<size_t>(s->T) * s->n_shared * s->d_ff * es);
+  w.u_q = off;          // MOE_FP8: e4m3 codes of u and their block scales
+  if (s->dtype == MOE_FP8 && s->n_shared > 0)
+    off = round256(round256(off + static_cast<size_t>(s->T) * s->d) +
+                   static_cast<size_t>(s->d / 128) * s->T * 4);
   w.total = off;
   return w;
 }
@@ -330,6 +370,31 @@ moe_status pair_maps(const void* w_r, long long w_r_rows, const void* x_r,
   return MOE_OK;
 }
 
+// Packed e4m3 operand: codes [rows, cols] then, at the next 256-byte
+// boundary, fp32 scales.
+inline size_t fp8_codes_bytes(long long rows, long long cols) {
+  return round256(static_cast<size_t>(rows) * cols);
+}
+
+template <int BN, int CW, bool DUAL, int STAGES>
+moe_status launch_gemm_fp8(const CUtensorMap& a_r, const CUtensorMap& b_r,
+                           const CUtensorMap& a_s, const CUtensorMap& b_s,
+                           const Fp8Params& p, int sms, cudaStream_t cs) {
+  using L = Fp8Smem<BN, CW, DUAL, STAGES>;
+  long long items = 0;
+  if (p.shared_rows > 0)
+    items += cdiv(p.shared_rows, BN) * (p.w_rows_shared / L::TR);
+  if (p.n_groups > 0)
+    items += (cdiv(p.max_routed_rows, BN) + p.n_groups) *
+             (p.w_rows_routed / L::TR);
+  if (items == 0) return MOE_OK;
+  const int grid = static_cast<int>(items < sms ? items : sms);
+  grouped_gemm_fp8_kernel<BN, CW, DUAL, STAGES>
+      <<<grid, L::threads, L::alloc, cs>>>(a_r, b_r, a_s, b_s, p);
+  MOE_CHECK_LAUNCH();
+  return MOE_OK;
+}
+
 moe_status launch_gemm_pair(const PairMaps& m, const GemmParams& p,
                             cudaStream_t cs) {
   long long items = 0;
@@ -348,6 +413,113 @@ moe_status launch_gemm_pair(const PairMaps& m, const GemmParams& p,
                                    m.b_s64, m.b_r128, m.b_s128, p);
   MOE_CHECK_LAUNCH();
   return MOE_OK;
+}
+
+// MOE_FP8 expert FFNs: quantize u for the shared experts, gate/up (+ SwiGLU
+// + requantization of H), down.  Small average group size -> 32-token
+// chunks (weight streaming); else 128-token chunks.
+moe_status expert_ffn_fp8(const moe_shape* s, const void* x_perm,
+                          const int32_t* offsets, const void* w_gu8,
+                          const void* w_down8, const void* u,
+                          const void* ws_gu8, const void* ws_down8,
+                          void* y_perm, void* y_shared, void* ws,
+                          bool has_shared, int sms, cudaStream_t cs) {
+  const WsLayout w = ws_layout(s);
+  const long long A = static_cast<long long>(s->T) * s->top_k;
+  const int N = s->n_routed, d = s->d, I = s->d_ff, SI = s->n_shared * s->d_ff;
+  const long long T = s->T;
+  char* wsb = static_cast<char*>(ws);
+  // operands: codes, then scales at the next 256-byte boundary
+  auto scales = [](const void* base, long long rows, long long cols) {
+    return reinterpret_cast<float*>(static_cast<char*>(const_cast<void*>(base)) +
+                                    fp8_codes_bytes(rows, cols));
+  };
+  uint8_t* h8 = reinterpret_cast<uint8_t*>(wsb + w.h_routed);
+  uint8_t* h8s = reinterpret_cast<uint8_t*>(wsb + w.h_shared);
+  uint8_t* u8 = reinterpret_cast<uint8_t*>(wsb + w.u_q);
+  moe_status st;
+  if (has_shared) {
+    const long long warps = T * (d / kQBlock);
+    quantize_rows_kernel<<<static_cast<unsigned>(cdiv(warps, 8)), 256, 0, cs>>>(
+        static_cast<const __nv_bfloat16*>(u), s->T, d, u8, scales(u8, T, d), T);
+    MOE_CHECK_LAUNCH();
+  }
+  int* ctr = reinterpret_cast<int*>(wsb + w.sched);
+  zero_i32_kernel<<<1, 32, 0, cs>>>(ctr, 2);
+  MOE_CHECK_LAUNCH();
+  const bool small = A <= 48LL * N;
+  const int bn = small ? 32 : 128;
+  CUtensorMap a_r, b_r, a_s, b_s;
+  Fp8Params p{};
+  // pass 1: gate/up
+  if ((st = make_map_u8(&a_r, w_gu8, 2LL * N * I, d, 256)) != MOE_OK) return st;
+  if ((st = make_map_u8(&b_r, x_perm, A, d, bn)) != MOE_OK) return st;
+  if (has_shared) {
+    if ((st = make_map_u8(&a_s, ws_gu8, 2LL * SI, d, 256)) != MOE_OK) return st;
+    if ((st = make_map_u8(&b_s, u8, T, d, bn)) != MOE_OK) return st;
+  } else {
+    a_s = a_r;
+    b_s = b_r;
+  }
+  p.offsets = offsets;
+  p.n_groups = N;
+  p.max_routed_rows = A;
+  p.shared_rows = has_shared ? s->T : 0;
+  p.w_rows_routed = 2 * I;
+  p.w_rows_shared = 2 * SI;
+  p.k_routed = d;
+  p.k_shared = d;
+  p.sw_routed = scales(w_gu8, 2LL * N * I, d);
+  p.sw_shared = has_shared ? scales(ws_gu8, 2LL * SI, d) : nullptr;
+  p.sx_routed = scales(x_perm, A, d);
+  p.ldsx_routed = A;
+  p.sx_shared = has_shared ? scales(u8, T, d) : nullptr;
+  p.ldsx_shared = T;
+  p.out_routed = h8;
+  p.ld_routed = I;
+  p.sh_routed = scales(h8, A, I);
+  p.ldsh_routed = A;
+  p.out_shared = h8s;
+  p.ld_shared = SI;
+  p.sh_shared = has_shared ? scales(h8s, T, SI) : nullptr;
+  p.ldsh_shared = T;
+  p.item_counter = ctr;
+  st = small ? launch_gemm_fp8<32, 1, true, 5>(a_r, b_r, a_s, b_s, p, sms, cs)
+             : launch_gemm_fp8<128, 2, true, 4>(a_r, b_r, a_s, b_s, p, sms, cs);
+  if (st != MOE_OK) return st;
+  // pass 2: down
+  if ((st = make_map_u8(&a_r, w_down8, static_cast<long long>(N) * d, I, 128)) !=
+      MOE_OK)
+    return st;
+  if ((st = make_map_u8(&b_r, h8, A, I, bn)) != MOE_OK) return st;
+  if (has_shared) {
+    if ((st = make_map_u8(&a_s, ws_down8, d, SI, 128)) != MOE_OK) return st;
+    if ((st = make_map_u8(&b_s, h8s, T, SI, bn)) != MOE_OK) return st;
+  } else {
+    a_s = a_r;
+    b_s = b_r;
+  }
+  p.w_rows_routed = d;
+  p.w_rows_shared = d;
+  p.k_routed = I;
+  p.k_shared = SI;
+  p.sw_routed = scales(w_down8, static_cast<long long>(N) * d, I);
+  p.sw_shared = has_shared ? scales(ws_down8, d, SI) : nullptr;
+  p.sx_routed = scales(h8, A, I);
+  p.ldsx_routed = A;
+  p.sx_shared = has_shared ? scales(h8s, T, SI) : nullptr;
+  p.ldsx_shared = T;
+  p.out_routed = y_perm;
+  p.ld_routed = d;
+  p.sh_routed = nullptr;
+  p.out_shared = y_shared;
+  p.ld_shared = d;
+  p.sh_shared = nullptr;
+  p.item_counter = ctr + 1;
+  return small
+             ? launch_gemm_fp8<32, 1, false, 10>(a_r, b_r, a_s, b_s, p, sms, cs)
+             : launch_gemm_fp8<128, 2, false, 6>(a_r, b_r, a_s, b_s, p, sms,
+                                                 cs);
 }
 
 // Shape, pointer and group checks shared by the routing entry points.
@@ -380,7 +552,7 @@ moe_status check_route_args(const moe_shape* s, int G, int M, const void* u,
 // Router CTAs per 128-token tile on this device (bf16: split of d across a
 // cluster; fp32: 1).
 int route_ctas_per_tile(const moe_shape* s, int sms) {
-  return s->dtype == MOE_BF16 ? route_split(s->T, s->d, sms) : 1;
+  return s->dtype != MOE_F32 ? route_split(s->T, s->d, sms) : 1;
 }
 
 // Router launches; `hist` holds ceil(T/128) * route_ctas_per_tile int32
@@ -395,7 +567,7 @@ moe_status launch_route(const moe_shape* s, int G, int M, const void* u,
   const int nblk = static_cast<int>(cdiv(s->T, kRouteTile));
   const int S = route_ctas_per_tile(s, sms);
   if (nblk > 0) {
-    if (s->dtype == MOE_BF16) {
+    if (s->dtype != MOE_F32) {     // bf16 router (also for MOE_FP8 layers)
       CUtensorMap tm_u, tm_e;
       st = make_map(&tm_u, u, s->T, s->d, kRouteTile);
       if (st != MOE_OK) return st;
@@ -450,6 +622,93 @@ moe_status moe_workspace_size(const moe_shape* shape, size_t* bytes) {
   return MOE_OK;
 }
 
+moe_status moe_fp8_weight_bytes(const moe_shape* s, int which,
+                                size_t* bytes) {
+  moe_status st = check_shape(s);
+  if (st != MOE_OK) return st;
+  if (bytes == nullptr) return fail(MOE_ERR_INVALID_ARG, "bytes is NULL");
+  if (s->dtype != MOE_FP8)
+    return fail(MOE_ERR_INVALID_ARG, "moe_fp8_weight_bytes needs MOE_FP8");
+  const long long N = s->n_routed, d = s->d, I = s->d_ff,
+                  SI = static_cast<long long>(s->n_shared) * s->d_ff;
+  long long rows, cols;
+  switch (which) {
+    case 0: rows = 2 * N * I; cols = d; break;     // routed gate/up
+    case 1: rows = N * d; cols = I; break;         // routed down
+    case 2: rows = 2 * SI; cols = d; break;        // shared gate/up
+    case 3: rows = d; cols = SI; break;            // shared down
+    default:
+      return fail(MOE_ERR_INVALID_ARG, "which=%d (0..3)", which);
+  }
+  *bytes = fp8_codes_bytes(rows, cols) +
+           round256(static_cast<size_t>(rows / 128) * (cols / 128) * 4);
+  return MOE_OK;
+}
+
+moe_status moe_x_perm_bytes(const moe_shape* s, size_t* bytes) {
+  moe_status st = check_shape(s);
+  if (st != MOE_OK) return st;
+  if (bytes == nullptr) return fail(MOE_ERR_INVALID_ARG, "bytes is NULL");
+  const long long A = static_cast<long long>(s->T) * s->top_k;
+  if (s->dtype == MOE_FP8)
+    *bytes = fp8_codes_bytes(A, s->d) +
+             round256(static_cast<size_t>(s->d / 128) * A * 4);
+  else
+    *bytes = static_cast<size_t>(A) * s->d * elem_size(s->dtype);
+  return MOE_OK;
+}
+
+moe_status moe_pack_weights_fp8(const moe_shape* s, const void* w_gate,
+                                const void* w_up, const void* w_down,
+                                const void* ws_gate, const void* ws_up,
+                                const void* ws_down, void* w_gu8,
+                                void* w_down8, void* ws_gu8, void* ws_down8,
+                                void* stream) {
+  g_launches = 0;
+  moe_status st = check_shape(s);
+  if (st != MOE_OK) return st;
+  if (s->dtype != MOE_FP8)
+    return fail(MOE_ERR_INVALID_ARG, "moe_pack_weights_fp8 needs MOE_FP8");
+  NEED_PTR(w_gate);
+  NEED_PTR(w_up);
+  NEED_PTR(w_down);
+  NEED_PTR(w_gu8);
+  NEED_PTR(w_down8);
+  if (s->n_shared > 0) {
+    NEED_PTR(ws_gate);
+    NEED_PTR(ws_up);
+    NEED_PTR(ws_down);
+    NEED_PTR(ws_gu8);
+    NEED_PTR(ws_down8);
+  }
+  cudaStream_t cs = as_stream(stream);
+  const int N = s->n_routed, d = s->d, I = s->d_ff, SI = s->n_shared * s->d_ff;
+  auto launch = [&](const void* a, const void* b, int mode, long long rows,
+                    int K, void* dst) -> moe_status {
+    uint8_t* q = static_cast<uint8_t*>(dst);
+    float* sc = reinterpret_cast<float*>(q + fp8_codes_bytes(rows, K));
+    const dim3 grid(static_cast<unsigned>(K / kQBlock),
+                    static_cast<unsigned>(rows / kQBlock));
+    quantize_weight_blocks_kernel<<<grid, 256, 0, cs>>>(
+        static_cast<const __nv_bfloat16*>(a),
+        static_cast<const __nv_bfloat16*>(b), mode, K, I, d, q, sc);
+    MOE_CHECK_LAUNCH();
+    return MOE_OK;
+  };
+  if ((st = launch(w_gate, w_up, 1, 2LL * N * I, d, w_gu8)) != MOE_OK)
+    return st;
+  if ((st = launch(w_down, nullptr, 0, static_cast<long long>(N) * d, I,
+                   w_down8)) != MOE_OK)
+    return st;
+  if (s->n_shared > 0) {
+    if ((st = launch(ws_gate, ws_up, 1, 2LL * SI, d, ws_gu8)) != MOE_OK)
+      return st;
+    if ((st = launch(ws_down, nullptr, 2, d, SI, ws_down8)) != MOE_OK)
+      return st;
+  }
+  return MOE_OK;
+}
+
 moe_status moe_pack_weights(const moe_shape* s, const void* w_gate,
                             const void* w_up, const void* ws_gate,
                             const void* ws_up, const void* ws_down,
@@ -458,6 +717,8 @@ moe_status moe_pack_weights(const moe_shape* s, const void* w_gate,
   g_launches = 0;
   moe_status st = check_shape(s);
   if (st != MOE_OK) return st;
+  if (s->dtype == MOE_FP8)
+    return fail(MOE_ERR_INVALID_ARG, "MOE_FP8 weights: moe_pack_weights_fp8");
   NEED_PTR(w_gate);
   NEED_PTR(w_up);
   NEED_PTR(w_gu_packed);
@@ -558,6 +819,15 @@ moe_status moe_permute(const moe_shape* s, const void* u,
     if (st != MOE_OK) return st;
     const long long want = cdiv(s->T, 8);
     const int grid = static_cast<int>(want < sms * 8LL ? want : sms * 8LL);
+    if (s->dtype == MOE_FP8) {
+      const long long A = static_cast<long long>(s->T) * s->top_k;
+      uint8_t* x8 = static_cast<uint8_t*>(x_perm);
+      permute_gather_fp8_kernel<<<grid, 256, 0, cs>>>(
+          static_cast<const __nv_bfloat16*>(u), inv, s->T, s->top_k, s->d, A,
+          x8, reinterpret_cast<float*>(x8 + fp8_codes_bytes(A, s->d)));
+      MOE_CHECK_LAUNCH();
+      return MOE_OK;
+    }
     permute_gather_kernel<<<grid, 256, 0, cs>>>(
         static_cast<const uint4*>(u), inv, s->T, s->top_k, nvec,
         static_cast<long long>(s->T) * s->top_k, static_cast<uint4*>(x_perm));
@@ -627,6 +897,11 @@ moe_status moe_expert_ffn(const moe_shape* s, const void* x_perm,
     }
     return MOE_OK;
   }
+
+  if (s->dtype == MOE_FP8)
+    return expert_ffn_fp8(s, x_perm, offsets, w_gu_packed, w_down, u,
+                          ws_gu_packed, ws_down_packed, y_perm, y_shared, ws,
+                          has_shared, sms, cs);
 
   // bf16: tcgen05 grouped GEMMs.  Small average group size -> 32-token
   // chunks and a deeper ring (weight streaming); else 256-token chunks.
@@ -732,8 +1007,8 @@ moe_status moe_combine(const moe_shape* s, const void* u, const void* y_perm,
   const void* ys = s->n_shared > 0 ? y_shared : nullptr;
   const long long A = static_cast<long long>(s->T) * s->top_k;
   cudaStream_t cs = as_stream(stream);
-  if (s->dtype == MOE_BF16) {
-    // bf16 layers keep the expert outputs in fp16
+  if (s->dtype != MOE_F32) {
+    // bf16 and fp8 layers keep the expert outputs in fp16
     const __nv_bfloat16* a = static_cast<const __nv_bfloat16*>(u);
     const __half* y = static_cast<const __half*>(y_perm);
     const __half* z = static_cast<const __half*>(ys);

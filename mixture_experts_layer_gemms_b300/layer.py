@@ -42,10 +42,19 @@ class MoELayer:
                  ws_up: Optional[torch.Tensor] = None,
                  ws_down: Optional[torch.Tensor] = None, top_k: int = 8,
                  h_dtype: torch.dtype = torch.float32, stream=None,
-                 n_groups: int = 1, topk_groups: int = 1):
+                 n_groups: int = 1, topk_groups: int = 1,
+                 quant: Optional[str] = None):
+        """quant="fp8": bf16 weights are quantized to e4m3 with block scales
+        and the expert GEMMs run in e4m3 (activations and router stay
+        bf16)."""
         if not E.is_cuda:
             raise ValueError("MoELayer needs CUDA tensors")
+        if quant not in (None, "fp8"):
+            raise ValueError(f"quant={quant!r}")
+        if quant == "fp8" and E.dtype != torch.bfloat16:
+            raise ValueError("fp8 layers take bf16 weights and activations")
         self.dtype = E.dtype
+        self.code = "fp8" if quant == "fp8" else E.dtype
         self.N, self.d = E.shape
         self.I = w_gate.shape[1]
         self.S = 0 if ws_gate is None else ws_gate.shape[0]
@@ -53,27 +62,42 @@ class MoELayer:
         # group-limited routing when topk_groups < n_groups
         self.n_groups, self.topk_groups = int(n_groups), int(topk_groups)
         self.h_dtype = h_dtype
-        # expert outputs: fp16 for bf16 layers, fp32 for fp32 layers
+        # expert outputs: fp16 for bf16 and fp8 layers, fp32 for fp32 layers
         self.y_dtype = torch.float16 if E.dtype == torch.bfloat16 \
             else torch.float32
-        self.E, self.bias, self.w_down = E, bias, w_down
+        self.E, self.bias = E, bias
         dev, dt = E.device, E.dtype
-        self.w_gu = torch.empty((self.N, 2 * self.I, self.d), dtype=dt,
-                                device=dev)
-        if self.S:
-            self.ws_gu = torch.empty((2 * self.S * self.I, self.d), dtype=dt,
-                                     device=dev)
-            self.ws_down = torch.empty((self.d, self.S * self.I), dtype=dt,
-                                       device=dev)
+        if quant == "fp8":
+            sh = self.shape(1)
+
+            def buf(which):
+                return torch.empty((_lib.fp8_weight_bytes(sh, which),),
+                                   dtype=torch.uint8, device=dev)
+            self.w_gu, self.w_down = buf(0), buf(1)
+            self.ws_gu, self.ws_down = (buf(2), buf(3)) if self.S \
+                else (None, None)
+            _lib.pack_weights_fp8(sh, w_gate, w_up, w_down, ws_gate, ws_up,
+                                  ws_down, self.w_gu, self.w_down, self.ws_gu,
+                                  self.ws_down, stream)
         else:
-            self.ws_gu = self.ws_down = None
-        _lib.pack_weights(self.shape(1), w_gate, w_up, ws_gate, ws_up, ws_down,
-                          self.w_gu, self.ws_gu, self.ws_down, stream)
+            self.w_down = w_down
+            self.w_gu = torch.empty((self.N, 2 * self.I, self.d), dtype=dt,
+                                    device=dev)
+            if self.S:
+                self.ws_gu = torch.empty((2 * self.S * self.I, self.d),
+                                         dtype=dt, device=dev)
+                self.ws_down = torch.empty((self.d, self.S * self.I),
+                                           dtype=dt, device=dev)
+            else:
+                self.ws_gu = self.ws_down = None
+            _lib.pack_weights(self.shape(1), w_gate, w_up, ws_gate, ws_up,
+                              ws_down, self.w_gu, self.ws_gu, self.ws_down,
+                              stream)
         self._bufs: Dict[int, Buffers] = {}
 
     def shape(self, T: int) -> _lib.MoeShape:
         return _lib.make_shape(T, self.d, self.N, self.K, self.S, self.I,
-                               self.dtype)
+                               self.code)
 
     def buffers(self, T: int) -> Buffers:
         b = self._bufs.get(T)
@@ -91,7 +115,11 @@ class MoELayer:
             offsets=torch.empty((self.N + 1,), **i32),
             perm=torch.empty((max(A, 1),), **i32),
             inv=torch.empty((T, K), **i32),
-            x_perm=torch.empty((max(A, 1), self.d), dtype=dt, device=dev),
+            x_perm=(torch.empty((max(_lib.x_perm_bytes(self.shape(T)), 256),),
+                                dtype=torch.uint8, device=dev)
+                    if self.code == "fp8"
+                    else torch.empty((max(A, 1), self.d), dtype=dt,
+                                     device=dev)),
             y_perm=torch.empty((max(A, 1), self.d), dtype=self.y_dtype,
                                device=dev),
             y_shared=(torch.empty((T, self.d), dtype=self.y_dtype,

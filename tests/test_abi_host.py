@@ -147,3 +147,27 @@ def test_route_grouped_validation(moe, G, M, K, code):
                                    P(768), P(1024), P(1280), P(1536), P(4096),
                                    n, None)
     assert st == code, moe.LIB.moe_last_error_detail()
+
+
+def test_fp8_sizes_and_checks(moe):
+    sh = _shape(moe, dtype=moe.MOE_FP8, d_ff=256)
+    n = ctypes.c_size_t()
+    # routed gate/up: 2*N*I x d codes + (2NI/128)*(d/128) fp32 scales
+    assert moe.LIB.moe_fp8_weight_bytes(ctypes.byref(sh), 0,
+                                        ctypes.byref(n)) == 0
+    assert n.value == 2 * 16 * 256 * 256 + 512     # 64 x 2 scales
+    assert moe.LIB.moe_fp8_weight_bytes(ctypes.byref(sh), 3,
+                                        ctypes.byref(n)) == 0
+    assert n.value == 256 * 256 + 256
+    assert moe.LIB.moe_fp8_weight_bytes(ctypes.byref(sh), 4,
+                                        ctypes.byref(n)) == 1
+    assert moe.LIB.moe_x_perm_bytes(ctypes.byref(sh), ctypes.byref(n)) == 0
+    A = 64 * 4
+    assert n.value == A * 256 + ((2 * A * 4 + 255) // 256) * 256
+    bad = _shape(moe, dtype=moe.MOE_FP8, d_ff=192)     # d_ff % 128
+    assert _ws(moe, bad)[0] == 2
+    P = ctypes.c_void_p
+    st = moe.LIB.moe_pack_weights(ctypes.byref(sh), P(256), P(512), P(768),
+                                  P(1024), P(1280), P(1536), P(1792),
+                                  P(2048), None)
+    assert st == 1 and b"moe_pack_weights_fp8" in moe.LIB.moe_last_error_detail()

@@ -66,13 +66,18 @@ def ffn_flops(cfg) -> float:
 def ffn_bytes(cfg, counts) -> float:
     """Algorithmic bytes of the expert-FFN call: weights of the experts that
     received tokens plus the shared experts (read once), the routed and
-    shared input rows, and the fp32 outputs."""
+    shared input rows, and the outputs (fp16 for bf16 and e4m3 layers, fp32
+    for fp32).  e4m3: one byte per weight plus one fp32 scale per 128 x 128
+    block, one byte per input element plus one fp32 scale per 128."""
+    fp8 = cfg.quant == "fp8"
     es = 2 if cfg.dtype == "bf16" else 4
-    ys = 2 if cfg.dtype == "bf16" else 4      # expert outputs fp16 / fp32
+    ws = 1.0 + 4.0 / (128 * 128) if fp8 else es
+    xs = 1.0 + 4.0 / 128 if fp8 else es
+    ys = 2 if cfg.dtype == "bf16" else 4
     touched = int((np.asarray(counts) > 0).sum())
-    w = 3.0 * cfg.d * cfg.d_ff * es * (touched + cfg.n_shared)
+    w = 3.0 * cfg.d * cfg.d_ff * ws * (touched + cfg.n_shared)
     A = cfg.T * cfg.top_k
-    act = A * cfg.d * es + cfg.T * cfg.d * es + (A + cfg.T) * cfg.d * ys
+    act = (A + cfg.T) * cfg.d * xs + (A + cfg.T) * cfg.d * ys
     return w + act
 
 
@@ -135,6 +140,8 @@ def cpu_baseline(cfg, t, budget_s: float = 15.0, max_tokens: int = 64):
     the whole routing of sampled tokens plus their routed and shared FFNs.
     Returns tokens/s and what the sample was."""
     import oracle.moe as om
+    import oracle.fp8 as of
+    fp8 = cfg.quant == "fp8"
     try:
         from threadpoolctl import threadpool_info
         blas = max((i.get("num_threads", 1) for i in threadpool_info()),
@@ -146,11 +153,12 @@ def cpu_baseline(cfg, t, budget_s: float = 15.0, max_tokens: int = 64):
     E64, b64 = as_f64(t["E"]), as_f64(t["b"])
     shared = [tuple(as_f64(t[k][s]) for k in ("ws_gate", "ws_up", "ws_down"))
               for s in range(cfg.n_shared)]
+    if fp8:       # weights are quantized once, outside the timed region
+        shared = [of.quantize_expert(*w) for w in shared]
     host = {}
 
     def routed(e):
-        return tuple(host[e][k].to(torch.float64).numpy()
-                     for k in range(3))
+        return host[e]
     done, spent = 0, 0.0
     for tok in order[:max_tokens]:
         u64 = as_f64(t["u"][int(tok):int(tok) + 1])
@@ -159,10 +167,15 @@ def cpu_baseline(cfg, t, budget_s: float = 15.0, max_tokens: int = 64):
         spent += time.perf_counter() - t0
         for e in r["idx"][0].tolist():      # stage weights on the host (untimed)
             if e not in host:
-                host[e] = tuple(t[k][e].cpu() for k in
-                                ("w_gate", "w_up", "w_down"))
+                w = tuple(t[k][e].cpu().to(torch.float64).numpy() for k in
+                          ("w_gate", "w_up", "w_down"))
+                host[e] = of.quantize_expert(*w) if fp8 else w
         t0 = time.perf_counter()
-        om.layer_forward(u64, E64, b64, cfg.top_k, routed, shared)
+        if fp8:
+            r = om.route(u64, E64, b64, cfg.top_k)
+            of.fp8_layer_forward(u64, r["idx"], r["gate"], routed, shared)
+        else:
+            om.layer_forward(u64, E64, b64, cfg.top_k, routed, shared)
         spent += time.perf_counter() - t0
         done += 1
         if spent >= budget_s:
@@ -170,7 +183,8 @@ def cpu_baseline(cfg, t, budget_s: float = 15.0, max_tokens: int = 64):
     return {"value": done / spent, "unit": "tokens/s", "cores": int(blas),
             "kind": "oracle",
             "sample": f"{done} of {cfg.T} tokens of {cfg.name} (routing + "
-                      f"routed and shared FFNs, fp64), {spent:.1f} s"}
+                      f"routed and shared FFNs, fp64"
+                      f"{', e4m3 operands' if fp8 else ''}), {spent:.1f} s"}
 
 
 def run_reference(args, cfg):
@@ -278,7 +292,8 @@ def run_ours(args, cfg):
     t = generate(cfg, dev)
     layer = moe.MoELayer(t["E"], t["b"].clone(), t["w_gate"], t["w_up"],
                          t["w_down"], t["ws_gate"], t["ws_up"], t["ws_down"],
-                         top_k=cfg.top_k, h_dtype=torch.float32)
+                         top_k=cfg.top_k, h_dtype=torch.float32,
+                         quant=cfg.quant)
     u = t["u"]
     bufs = layer.buffers(cfg.T)
     sh = layer.shape(cfg.T)
@@ -373,6 +388,12 @@ def run_ours(args, cfg):
     moe.get_device_error()
 
     peaks = _peaks()
+    fp8 = cfg.quant == "fp8"
+    # e4m3 contractions: the measured bf16 peak times the nominal dense
+    # e4m3 : bf16 ratio (4.5 : 2.25 PFLOP/s)
+    tc_peak = peaks["bf16_tflops"] * (2.0 if fp8 else 1.0)
+    tc_src = (f"{peaks['source']} bf16_tflops (burst) x 2 (nominal e4m3:bf16)"
+              if fp8 else f"{peaks['source']} bf16_tflops (burst)")
     ms_step = ms / args.steps
     value = ws * cfg.T * args.steps / (ms / 1e3)
     decode = cfg.T * cfg.top_k <= 48 * cfg.n_routed
@@ -381,34 +402,37 @@ def run_ours(args, cfg):
         roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": ach / peaks["hbm_gbs"],
                 "traffic": None,
-                "kernel": "grouped_gemm_kernel<32,10> (gate/up + down launches "
-                          "of one expert-FFN call)",
+                "kernel": ("grouped_gemm_fp8_kernel<32,1,*>" if fp8 else
+                           "grouped_gemm_kernel<32,10>") +
+                          " (gate/up + down launches of one expert-FFN call)",
                 "peak_source": f"{peaks['source']} hbm_gbs"}
     else:
         ach = ffn_flops(cfg) / (ffn_ms / 1e3) / 1e12
+        sus = peaks["bf16_tflops_sustained"]
         roof = {"bound": "tensor", "achieved": ach,
-                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": ach / peaks["bf16_tflops"],
+                "peak": tc_peak, "unit": "TFLOP/s",
+                "frac": ach / tc_peak,
                 "traffic": MEASURED_TRAFFIC.get(cfg.name),
-                "kernel": "grouped_gemm_pair_kernel (gate/up + down launches "
-                          "of one expert-FFN call)",
-                "peak_source": f"{peaks['source']} bf16_tflops (burst)",
-                "frac_of_sustained": (ach / peaks["bf16_tflops_sustained"]
-                                      if peaks["bf16_tflops_sustained"]
-                                      else None)}
+                "kernel": ("grouped_gemm_fp8_kernel<128,2,*>" if fp8 else
+                           "grouped_gemm_pair_kernel") +
+                          " (gate/up + down launches of one expert-FFN call)",
+                "peak_source": tc_src,
+                "frac_of_sustained": (ach / (sus * (2.0 if fp8 else 1.0))
+                                      if sus else None)}
     roof["ms_per_launch_pair"] = ffn_ms
     line = {"metric": METRIC, "value": value, "unit": "tokens/s",
             "n_gpus": ws, "steps": args.steps, "warmup": max(3, args.warmup),
             "ms_per_step": ms_step, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3" if fp8 else "bf16",
             "data": "synthetic",
             "config": {"workload": cfg.name, "T": cfg.T, "d": cfg.d,
                        "n_routed": cfg.n_routed, "top_k": cfg.top_k,
                        "n_shared": cfg.n_shared, "d_ff": cfg.d_ff,
                        "parallelism": f"replicas x{ws}", "l2": L2_NOTE},
             "layer_tflops": layer_flops(cfg) / (ms_step / 1e3) / 1e12,
-            "layer_frac_of_bf16_peak": layer_flops(cfg) / (ms_step / 1e3) /
-            1e12 / peaks["bf16_tflops"],
+            ("layer_frac_of_e4m3_peak" if fp8 else "layer_frac_of_bf16_peak"):
+            layer_flops(cfg) / (ms_step / 1e3) / 1e12 / tc_peak,
             "roofline": roof,
             "clocks": clk,
             "gpu_launches": launches * ws,

@@ -18,15 +18,17 @@
 //     scales (weight block x token block, both powers of two), into fp32
 //     registers -- the promotion of the pages' Fig. 7b, done by the warps
 //     that also finish the item, while the tensor cores run the next block;
-//   * gate/up (DUAL): a weight tile is 128 gate rows followed by the 128 up
+//   * an item covers two 128-row weight tiles (TWO) -- two M = 128 MMAs per
+//     K-step on the same token operand -- or one;
+//   * gate/up (SWIGLU, TWO): a weight tile is 128 gate rows followed by the 128 up
 //     rows of the same intermediate indices, two M = 128 MMAs per K-step on
 //     the same token operand, so a thread holds gate and up of one
 //     intermediate index: H = SiLU(g) * u needs no exchange.  H is then
 //     quantized in 1 x 128 blocks along the intermediate index (one block =
 //     the tile's 128 rows, reduced over the four lane-quarter warps) and
 //     stored as codes plus scales [I/128][rows] for the down pass;
-//   * down (!DUAL): 128 output channels of Y, stored as fp16 (a value beyond
-//     the fp16 range is reported, never written as inf).
+//   * down (!SWIGLU): 128 or 256 output channels of Y, stored as fp16 (a
+//     value beyond the fp16 range is reported, never written as inf).
 //
 // Warp roles (64 + 128 CW threads, one CTA per SM, persistent):
 //   warp 0 lane 0: scheduler + TMA producer;  warp 1 lane 0: MMA issuer and
@@ -53,9 +55,9 @@ struct Fp8Params {
   long long ldsx_routed;
   const float* sx_shared;
   long long ldsx_shared;
-  void* out_routed;            // DUAL: H codes [rows][ld]; else Y fp16
+  void* out_routed;            // SwiGLU pass: H codes [rows][ld]; else Y fp16
   long long ld_routed;
-  float* sh_routed;            // DUAL: H scales [I/128][ld]
+  float* sh_routed;            // SwiGLU pass: H scales [I/128][ld]
   long long ldsh_routed;
   void* out_shared;
   long long ld_shared;
@@ -64,16 +66,16 @@ struct Fp8Params {
   int* item_counter;
 };
 
-template <int BN, int CW, bool DUAL, int STAGES>
+template <int BN, int CW, bool TWO, int STAGES>
 struct Fp8Smem {
-  static constexpr int TR = DUAL ? 256 : 128;           // weight rows / item
+  static constexpr int TR = TWO ? 256 : 128;            // weight rows / item
   static constexpr int a_bytes = TR * kQBlock;
   static constexpr int b_bytes = BN * kQBlock;
   static constexpr int a_off = 0;
   static constexpr int b_off = a_off + STAGES * a_bytes;
   static constexpr int amax_off = b_off + STAGES * b_bytes;   // [CW][4][BN/CW]
-  static constexpr int PC = (DUAL ? 2 : 1) * BN;         // TMEM cols / partial
-  static constexpr int NBUF = (512 / PC) < 4 ? (512 / PC) : 4;
+  static constexpr int PC = (TWO ? 2 : 1) * BN;          // TMEM cols / partial
+  static constexpr int NBUF = (512 / PC) < 8 ? (512 / PC) : 8;
   static constexpr int bar_off = amax_off + 4 * BN * 4;
   static constexpr int n_bars = 2 * STAGES + 2 * NBUF + 1 + 2 * kSchedDepth;
   static constexpr int misc_off = bar_off + n_bars * 8;
@@ -130,14 +132,16 @@ __device__ __forceinline__ Tile decode_item8(int item, const Fp8Params& p,
   return t;
 }
 
-template <int BN, int CW, bool DUAL, int STAGES>
+template <int BN, int CW, bool TWO, bool SWIGLU, int STAGES>
 __global__ void __launch_bounds__(64 + 128 * CW, 1)
 grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA_r,
                         const __grid_constant__ CUtensorMap tmB_r,
                         const __grid_constant__ CUtensorMap tmA_s,
                         const __grid_constant__ CUtensorMap tmB_s,
                         const Fp8Params p) {
-  using L = Fp8Smem<BN, CW, DUAL, STAGES>;
+  using L = Fp8Smem<BN, CW, TWO, STAGES>;
+  static_assert(TWO || !SWIGLU, "SwiGLU needs gate and up tiles");
+  constexpr bool DUAL = TWO;          // two 128-row tiles per item
   constexpr int TR = L::TR;
   constexpr int PC = L::PC;
   constexpr int NBUF = L::NBUF;
@@ -422,22 +426,39 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA_r,
             uint32_t r[32];
             const uint32_t ta = tmem + (static_cast<uint32_t>(q * 32) << 16) +
                                 buf * PC + cbase;
-            tmem_ld32(ta, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float sj = __shfl_sync(0xffffffffu, sxl, j);
-              acc_g[c * 32 + j] =
-                  fmaf(__uint_as_float(r[j]), swg * sj, acc_g[c * 32 + j]);
-            }
-            if constexpr (DUAL) {
-              tmem_ld32(ta + BN, r);
+            if constexpr (DUAL && NC == 32) {
+              // one 32-column slice per thread: both partials in flight
+              // before the wait (registers allow it at this width)
+              uint32_t r2[32];
+              tmem_ld32(ta, r);
+              tmem_ld32(ta + BN, r2);
               tmem_ld_wait();
 #pragma unroll
               for (int j = 0; j < 32; ++j) {
                 const float sj = __shfl_sync(0xffffffffu, sxl, j);
+                acc_g[c * 32 + j] =
+                    fmaf(__uint_as_float(r[j]), swg * sj, acc_g[c * 32 + j]);
                 acc_u[c * 32 + j] =
-                    fmaf(__uint_as_float(r[j]), swu * sj, acc_u[c * 32 + j]);
+                    fmaf(__uint_as_float(r2[j]), swu * sj, acc_u[c * 32 + j]);
+              }
+            } else {
+              tmem_ld32(ta, r);
+              tmem_ld_wait();
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const float sj = __shfl_sync(0xffffffffu, sxl, j);
+                acc_g[c * 32 + j] =
+                    fmaf(__uint_as_float(r[j]), swg * sj, acc_g[c * 32 + j]);
+              }
+              if constexpr (DUAL) {
+                tmem_ld32(ta + BN, r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                  const float sj = __shfl_sync(0xffffffffu, sxl, j);
+                  acc_u[c * 32 + j] =
+                      fmaf(__uint_as_float(r[j]), swu * sj, acc_u[c * 32 + j]);
+                }
               }
             }
           }
@@ -451,7 +472,7 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA_r,
         }
       }
       const int row = q * 32 + lane;   // row of the 128-row output block
-      if constexpr (DUAL) {
+      if constexpr (SWIGLU) {
         // H = SiLU(g) * u for intermediate index wt*128 + row, then the
         // 1 x 128 block of each token: max over the four lane quarters
         float* am = amax_s + cg * 4 * NC;
@@ -490,14 +511,18 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA_r,
         __half* Y = static_cast<__half*>(t.shared ? p.out_shared
                                                   : p.out_routed);
         const long long ldy = t.shared ? p.ld_shared : p.ld_routed;
-        const int ycol = t.wt * 128 + row;
+        const int ycol = t.wt * TR + row;     // second tile: + 128
 #pragma unroll
         for (int j = 0; j < NC; ++j) {
           const int col = col0 + j;
           if (col < t.n_valid) {
+            __half* yr = Y + static_cast<size_t>(t.b_row + col) * ldy + ycol;
             overflow |= !(fabsf(acc_g[j]) <= 65504.f);
-            Y[static_cast<size_t>(t.b_row + col) * ldy + ycol] =
-                __float2half_rn(acc_g[j]);
+            yr[0] = __float2half_rn(acc_g[j]);
+            if constexpr (DUAL) {
+              overflow |= !(fabsf(acc_u[j]) <= 65504.f);
+              yr[128] = __float2half_rn(acc_u[j]);
+            }
           }
         }
       }

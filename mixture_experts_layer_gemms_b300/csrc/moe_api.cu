@@ -89,14 +89,16 @@ moe_status device_setup(int* sm_count) {
     MOE_CHECK_CUDA(allow_smem(grouped_gemm_kernel<32, 10>,
                               GemmSmem<32, 10>::alloc));
     MOE_CHECK_CUDA(allow_smem(grouped_gemm_pair_kernel, PairSmem::alloc));
-    MOE_CHECK_CUDA(allow_smem(grouped_gemm_fp8_kernel<32, 1, true, 5>,
-                              Fp8Smem<32, 1, true, 5>::alloc));
-    MOE_CHECK_CUDA(allow_smem(grouped_gemm_fp8_kernel<32, 1, false, 10>,
-                              Fp8Smem<32, 1, false, 10>::alloc));
-    MOE_CHECK_CUDA(allow_smem(grouped_gemm_fp8_kernel<128, 2, true, 4>,
-                              Fp8Smem<128, 2, true, 4>::alloc));
-    MOE_CHECK_CUDA(allow_smem(grouped_gemm_fp8_kernel<128, 2, false, 6>,
-                              Fp8Smem<128, 2, false, 6>::alloc));
+#define MOE_FP8_SMEM(BN, CW, TWO, SW, ST)                                  \
+  MOE_CHECK_CUDA(allow_smem(grouped_gemm_fp8_kernel<BN, CW, TWO, SW, ST>, \
+                            Fp8Smem<BN, CW, TWO, ST>::alloc))
+    MOE_FP8_SMEM(32, 1, true, true, 6);
+    MOE_FP8_SMEM(32, 1, true, false, 6);
+    MOE_FP8_SMEM(32, 1, false, false, 10);
+    MOE_FP8_SMEM(128, 2, true, true, 4);
+    MOE_FP8_SMEM(128, 2, true, false, 4);
+    MOE_FP8_SMEM(128, 2, false, false, 6);
+#undef MOE_FP8_SMEM
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (di.sm_count / 2));
     cfg.blockDim = dim3(192);
@@ -376,11 +378,11 @@ inline size_t fp8_codes_bytes(long long rows, long long cols) {
   return round256(static_cast<size_t>(rows) * cols);
 }
 
-template <int BN, int CW, bool DUAL, int STAGES>
+template <int BN, int CW, bool TWO, bool SWIGLU, int STAGES>
 moe_status launch_gemm_fp8(const CUtensorMap& a_r, const CUtensorMap& b_r,
                            const CUtensorMap& a_s, const CUtensorMap& b_s,
                            const Fp8Params& p, int sms, cudaStream_t cs) {
-  using L = Fp8Smem<BN, CW, DUAL, STAGES>;
+  using L = Fp8Smem<BN, CW, TWO, STAGES>;
   long long items = 0;
   if (p.shared_rows > 0)
     items += cdiv(p.shared_rows, BN) * (p.w_rows_shared / L::TR);
@@ -389,7 +391,7 @@ moe_status launch_gemm_fp8(const CUtensorMap& a_r, const CUtensorMap& b_r,
              (p.w_rows_routed / L::TR);
   if (items == 0) return MOE_OK;
   const int grid = static_cast<int>(items < sms ? items : sms);
-  grouped_gemm_fp8_kernel<BN, CW, DUAL, STAGES>
+  grouped_gemm_fp8_kernel<BN, CW, TWO, SWIGLU, STAGES>
       <<<grid, L::threads, L::alloc, cs>>>(a_r, b_r, a_s, b_s, p);
   MOE_CHECK_LAUNCH();
   return MOE_OK;
@@ -484,16 +486,20 @@ moe_status expert_ffn_fp8(const moe_shape* s, const void* x_perm,
   p.sh_shared = has_shared ? scales(h8s, T, SI) : nullptr;
   p.ldsh_shared = T;
   p.item_counter = ctr;
-  st = small ? launch_gemm_fp8<32, 1, true, 5>(a_r, b_r, a_s, b_s, p, sms, cs)
-             : launch_gemm_fp8<128, 2, true, 4>(a_r, b_r, a_s, b_s, p, sms, cs);
+  st = small
+           ? launch_gemm_fp8<32, 1, true, true, 6>(a_r, b_r, a_s, b_s, p, sms, cs)
+           : launch_gemm_fp8<128, 2, true, true, 4>(a_r, b_r, a_s, b_s, p, sms,
+                                                    cs);
   if (st != MOE_OK) return st;
-  // pass 2: down
-  if ((st = make_map_u8(&a_r, w_down8, static_cast<long long>(N) * d, I, 128)) !=
+  // pass 2: down, two 128-row tiles of W_down per item when d allows
+  const bool two = d % 256 == 0;
+  const int tr = two ? 256 : 128;
+  if ((st = make_map_u8(&a_r, w_down8, static_cast<long long>(N) * d, I, tr)) !=
       MOE_OK)
     return st;
   if ((st = make_map_u8(&b_r, h8, A, I, bn)) != MOE_OK) return st;
   if (has_shared) {
-    if ((st = make_map_u8(&a_s, ws_down8, d, SI, 128)) != MOE_OK) return st;
+    if ((st = make_map_u8(&a_s, ws_down8, d, SI, tr)) != MOE_OK) return st;
     if ((st = make_map_u8(&b_s, h8s, T, SI, bn)) != MOE_OK) return st;
   } else {
     a_s = a_r;
@@ -516,10 +522,15 @@ moe_status expert_ffn_fp8(const moe_shape* s, const void* x_perm,
   p.ld_shared = d;
   p.sh_shared = nullptr;
   p.item_counter = ctr + 1;
-  return small
-             ? launch_gemm_fp8<32, 1, false, 10>(a_r, b_r, a_s, b_s, p, sms, cs)
-             : launch_gemm_fp8<128, 2, false, 6>(a_r, b_r, a_s, b_s, p, sms,
-                                                 cs);
+  if (small)
+    return two ? launch_gemm_fp8<32, 1, true, false, 6>(a_r, b_r, a_s, b_s, p,
+                                                        sms, cs)
+               : launch_gemm_fp8<32, 1, false, false, 10>(a_r, b_r, a_s, b_s,
+                                                          p, sms, cs);
+  return two ? launch_gemm_fp8<128, 2, true, false, 4>(a_r, b_r, a_s, b_s, p,
+                                                       sms, cs)
+             : launch_gemm_fp8<128, 2, false, false, 6>(a_r, b_r, a_s, b_s, p,
+                                                        sms, cs);
 }
 
 // Shape, pointer and group checks shared by the routing entry points.

@@ -18,6 +18,9 @@ v3_decode  bf16    128     7168   256   8   1   2048   3      0
 skew  bf16         16384   7168   256   8   1   2048   4      0 (+50 steps)
 ====  ===========  ======  =====  ====  ==  ==  =====  =====  ===========
 
+v3_prefill_fp8 and v3_decode_fp8 are v3_prefill and v3_decode (same seeds,
+same tensors) run with e4m3 expert GEMMs.
+
 Distributions: u ~ N(0,1); centroids e_i ~ N(0, 1/d); gate/up weights
 ~ N(0, 1/d); down weights ~ N(0, 1/I).  The skew workload scales centroid i
 by (i+1)^-1.1 (largest at i = 0) so that routing starts imbalanced, and
@@ -59,6 +62,7 @@ class MoEConfig:
     zipf: Optional[float] = None   # centroid i scaled by (i+1)**-zipf
     steps: int = 1
     gamma: float = 1e-3
+    quant: Optional[str] = None   # "fp8": e4m3 expert GEMMs (inputs unchanged)
 
     @property
     def assignments(self) -> int:
@@ -82,6 +86,10 @@ CONFIGS: Dict[str, MoEConfig] = {
                       n_shared=1, d_ff=2048, dtype="bf16", seed=4,
                       zipf=1.1, steps=50, gamma=1e-3),
 }
+# The two V3 workloads with e4m3 expert GEMMs: same inputs (same seeds),
+# bf16 weights quantized by the library.
+for _n in ("v3_prefill", "v3_decode"):
+    CONFIGS[_n + "_fp8"] = CONFIGS[_n].with_(name=_n + "_fp8", quant="fp8")
 
 
 def get_config(name: str) -> MoEConfig:

@@ -406,23 +406,37 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA_r,
         if constexpr (DUAL) acc_u[j] = 0.f;
       }
       bool ok = true;
+      // Block scales of chunk i: weight (gate, up) and this lane's token
+      // column in each 32-column slice.  They are loaded one chunk ahead so
+      // that their latency hides behind the wait for the partial sums.
+      auto load_scales = [&](int i, float& g, float& u, float* x) {
+        g = __ldg(sw + static_cast<size_t>(rb) * nk + i);
+        u = DUAL ? __ldg(sw + static_cast<size_t>(rb + 1) * nk + i) : 0.f;
+#pragma unroll
+        for (int c = 0; c < NC / 32; ++c) {
+          const int col = col0 + c * 32 + lane;
+          x[c] = col < t.n_valid
+                     ? __ldg(sx + static_cast<size_t>(i) * ldsx + t.b_row + col)
+                     : 0.f;
+        }
+      };
+      float nswg, nswu, nsx[NC / 32];
+      load_scales(0, nswg, nswu, nsx);
       for (int i = 0; i < nk; ++i) {
+        const float swg = nswg, swu = nswu;
+        float sxc[NC / 32];
+#pragma unroll
+        for (int c = 0; c < NC / 32; ++c) sxc[c] = nsx[c];
+        if (i + 1 < nk) load_scales(i + 1, nswg, nswu, nsx);
         ok = mbar_wait(bar_pfull + 8 * buf, bph, abort_flag, KID_GEMM_FP8, 7) &&
              ok;
         tc_fence_after();
-        const float swg = __ldg(sw + static_cast<size_t>(rb) * nk + i);
-        const float swu =
-            DUAL ? __ldg(sw + static_cast<size_t>(rb + 1) * nk + i) : 0.f;
 #pragma unroll
         for (int c = 0; c < NC / 32; ++c) {
           const int cbase = col0 + c * 32;
           if (cbase < t.n_mma) {
             // token scale of column cbase + lane, broadcast by shuffles
-            const float sxl =
-                (cbase + lane < t.n_valid)
-                    ? __ldg(sx + static_cast<size_t>(i) * ldsx + t.b_row +
-                            cbase + lane)
-                    : 0.f;
+            const float sxl = sxc[c];
             uint32_t r[32];
             const uint32_t ta = tmem + (static_cast<uint32_t>(q * 32) << 16) +
                                 buf * PC + cbase;

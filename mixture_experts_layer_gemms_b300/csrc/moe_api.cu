@@ -833,7 +833,9 @@ moe_status moe_permute(const moe_shape* s, const void* u,
     if (s->dtype == MOE_FP8) {
       const long long A = static_cast<long long>(s->T) * s->top_k;
       uint8_t* x8 = static_cast<uint8_t*>(x_perm);
-      permute_gather_fp8_kernel<<<grid, 256, 0, cs>>>(
+      const long long wq = cdiv(static_cast<long long>(s->T) * (s->d / 128), 8);
+      const int grid8 = static_cast<int>(wq < sms * 16LL ? wq : sms * 16LL);
+      permute_gather_fp8_kernel<<<grid8, 256, 0, cs>>>(
           static_cast<const __nv_bfloat16*>(u), inv, s->T, s->top_k, s->d, A,
           x8, reinterpret_cast<float*>(x8 + fp8_codes_bytes(A, s->d)));
       MOE_CHECK_LAUNCH();

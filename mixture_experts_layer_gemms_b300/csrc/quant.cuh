@@ -96,40 +96,38 @@ quantize_rows_kernel(const __nv_bfloat16* __restrict__ x, int R, int K,
 }
 
 // Dispatch fused with quantization: x8[inv[t,k]] = codes of u[t] for every
-// k, scales sx[b][inv[t,k]].  One warp per token; each 1 x 128 block of the
-// row is quantized once and written K times.
+// k, scales sx[b][inv[t,k]].  One warp per (token, 1 x 128 block): the block
+// is quantized once and written K times.
 __global__ void __launch_bounds__(256)
 permute_gather_fp8_kernel(const __nv_bfloat16* __restrict__ u,
                           const int* __restrict__ inv, int T, int K, int d,
                           long long total_slots, uint8_t* __restrict__ x8,
                           float* __restrict__ sx) {
   const int lane = threadIdx.x & 31;
-  const int wpb = blockDim.x >> 5;
-  for (int t = blockIdx.x * wpb + (threadIdx.x >> 5); t < T;
-       t += gridDim.x * wpb) {
-    int slot[16];
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      slot[k] = (k < K) ? inv[static_cast<size_t>(t) * K + k] : -1;
-      if (k < K && (slot[k] < 0 || slot[k] >= total_slots)) {
-        if (lane == 0) report_error(ERR_CHECK, KID_QUANT, 2);
-        slot[k] = -1;
-      }
+  const int nb = d / kQBlock;
+  const long long nwarps =
+      static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  for (long long w = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) +
+                     (threadIdx.x >> 5);
+       w < static_cast<long long>(T) * nb; w += nwarps) {
+    const int t = static_cast<int>(w / nb), b = static_cast<int>(w % nb);
+    // lane k < K holds the slot of assignment (t, k)
+    int myslot = lane < K ? inv[static_cast<size_t>(t) * K + lane] : -1;
+    if (lane < K && (myslot < 0 || myslot >= total_slots)) {
+      if (b == 0) report_error(ERR_CHECK, KID_QUANT, 2);
+      myslot = -1;
     }
-    const __nv_bfloat16* src = u + static_cast<size_t>(t) * d;
-    for (int b = 0; b < d / kQBlock; ++b) {
-      float f[4];
-      load4_bf16(src + b * kQBlock + 4 * lane, f);
-      float sc;
-      const uint32_t c = warp_quant_block(f, &sc);
-#pragma unroll
-      for (int k = 0; k < 16; ++k)
-        if (k < K && slot[k] >= 0)
-          *reinterpret_cast<uint32_t*>(
-              x8 + static_cast<size_t>(slot[k]) * d + b * kQBlock + 4 * lane) = c;
-      if (lane < K && slot[lane] >= 0)
-        sx[static_cast<size_t>(b) * total_slots + slot[lane]] = sc;
+    float f[4];
+    load4_bf16(u + static_cast<size_t>(t) * d + b * kQBlock + 4 * lane, f);
+    float sc;
+    const uint32_t c = warp_quant_block(f, &sc);
+    for (int k = 0; k < K; ++k) {
+      const int s = __shfl_sync(0xffffffffu, myslot, k);
+      if (s >= 0)
+        *reinterpret_cast<uint32_t*>(
+            x8 + static_cast<size_t>(s) * d + b * kQBlock + 4 * lane) = c;
     }
+    if (myslot >= 0) sx[static_cast<size_t>(b) * total_slots + myslot] = sc;
   }
 }
 

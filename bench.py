@@ -36,7 +36,7 @@ METRIC = "MoE-layer tokens/s at V3 shape"
 # launches) from an ncu capture of the same kernel on a smaller case of the
 # same shape, scaled by the units processed (see profiles/
 # grouped_gemm_pair_small_v3dims.md).  None where no capture exists.
-MEASURED_TRAFFIC = {}
+MEASURED_TRAFFIC = {"v3_prefill": 25.6e9}
 L2_NOTE = "inputs larger than L2 (22.5 GB of expert weights read per step)"
 
 

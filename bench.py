@@ -128,6 +128,27 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(x: float, device="cpu") -> float:
+    """Largest value of a per-rank float over all ranks of the initialised
+    process group (the value itself without one).  The bench's timers are
+    reduced this way: the job is as slow as its slowest replica."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    if dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world: int, units_per_rank: int, steps: int,
+                   ms_max: float) -> float:
+    """Units per second of the whole job: every replica processes its own
+    units (weak scaling), all within the slowest replica's time."""
+    return world * units_per_rank * steps / (ms_max / 1e3)
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -237,6 +258,9 @@ def run_skew(args, cfg, moe, dev, ws, rank, local):
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
     t0 = torch.cuda.Event(enable_timing=True)
@@ -247,14 +271,16 @@ def run_skew(args, cfg, moe, dev, ws, rank, local):
         loads[s].copy_(bufs.counts)
     t1.record(stream)
     torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
     clk = clocks.stop()
     moe.get_device_error()
-    ms = t0.elapsed_time(t1)
+    ms = max_over_ranks(t0.elapsed_time(t1), dev)
     c = loads.cpu().numpy().astype(np.float64)
     mean = cfg.T * cfg.top_k / cfg.n_routed
     mm = (c.max(axis=1) / mean).tolist()
     peaks = _peaks()
-    line = {"metric": METRIC, "value": ws * cfg.T * steps / (ms / 1e3),
+    line = {"metric": METRIC, "value": whole_job_rate(ws, cfg.T, steps, ms),
             "unit": "tokens/s", "n_gpus": ws, "steps": steps,
             "warmup": max(3, args.warmup), "ms_per_step": ms / steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -352,12 +378,7 @@ def run_ours(args, cfg):
     barrier()
     clk = clocks.stop()
     moe.get_device_error()
-    ms = t0.elapsed_time(t1)
-    if ws > 1:
-        import torch.distributed as dist
-        x = torch.tensor([ms], device=dev)
-        dist.all_reduce(x, op=dist.ReduceOp.MAX)
-        ms = float(x.item())
+    ms = max_over_ranks(t0.elapsed_time(t1), dev)
     ffn_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
     counts = bufs.counts.cpu().numpy()
 
@@ -379,12 +400,7 @@ def run_ours(args, cfg):
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
-    e_ms = e0.elapsed_time(e1) / e_steps
-    if ws > 1:
-        import torch.distributed as dist
-        x = torch.tensor([e_ms], device=dev)
-        dist.all_reduce(x, op=dist.ReduceOp.MAX)
-        e_ms = float(x.item())
+    e_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps, dev)
     moe.get_device_error()
 
     peaks = _peaks()
@@ -395,7 +411,7 @@ def run_ours(args, cfg):
     tc_src = (f"{peaks['source']} bf16_tflops (burst) x 2 (nominal e4m3:bf16)"
               if fp8 else f"{peaks['source']} bf16_tflops (burst)")
     ms_step = ms / args.steps
-    value = ws * cfg.T * args.steps / (ms / 1e3)
+    value = whole_job_rate(ws, cfg.T, args.steps, ms)
     decode = cfg.T * cfg.top_k <= 48 * cfg.n_routed
     if decode:
         ach = ffn_bytes(cfg, counts) / (ffn_ms / 1e3) / 1e9

@@ -99,6 +99,10 @@ moe_status device_setup(int* sm_count) {
     MOE_FP8_SMEM(128, 2, true, false, 4);
     MOE_FP8_SMEM(128, 2, false, false, 6);
 #undef MOE_FP8_SMEM
+    MOE_CHECK_CUDA(allow_smem(grouped_gemm_fp8_tm_kernel<true, 4>,
+                              Fp8TmSmem<4>::alloc));
+    MOE_CHECK_CUDA(allow_smem(grouped_gemm_fp8_tm_kernel<false, 4>,
+                              Fp8TmSmem<4>::alloc));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (di.sm_count / 2));
     cfg.blockDim = dim3(192);
@@ -397,6 +401,27 @@ moe_status launch_gemm_fp8(const CUtensorMap& a_r, const CUtensorMap& b_r,
   return MOE_OK;
 }
 
+// tokens-on-M e4m3 GEMM (prefill-sized groups); maps: weights box 256 rows,
+// tokens box 128 rows
+template <bool SWIGLU, int STAGES>
+moe_status launch_gemm_fp8_tm(const CUtensorMap& w_r, const CUtensorMap& x_r,
+                              const CUtensorMap& w_s, const CUtensorMap& x_s,
+                              const Fp8Params& p, int sms, cudaStream_t cs) {
+  long long items = 0;
+  if (p.shared_rows > 0)
+    items += cdiv(p.shared_rows, kTmTok) * (p.w_rows_shared / kTmRows);
+  if (p.n_groups > 0)
+    items += (cdiv(p.max_routed_rows, kTmTok) + p.n_groups) *
+             (p.w_rows_routed / kTmRows);
+  if (items == 0) return MOE_OK;
+  const int grid = static_cast<int>(items < sms ? items : sms);
+  grouped_gemm_fp8_tm_kernel<SWIGLU, STAGES>
+      <<<grid, Fp8TmSmem<STAGES>::threads, Fp8TmSmem<STAGES>::alloc, cs>>>(
+          w_r, x_r, w_s, x_s, p);
+  MOE_CHECK_LAUNCH();
+  return MOE_OK;
+}
+
 moe_status launch_gemm_pair(const PairMaps& m, const GemmParams& p,
                             cudaStream_t cs) {
   long long items = 0;
@@ -450,10 +475,12 @@ moe_status expert_ffn_fp8(const moe_shape* s, const void* x_perm,
   zero_i32_kernel<<<1, 32, 0, cs>>>(ctr, 2);
   MOE_CHECK_LAUNCH();
   const bool small = A <= 48LL * N;
+  // prefill-sized groups with d % 256 == 0: tokens on M
+  const bool tm = !small && d % 256 == 0;
   const int bn = small ? 32 : 128;
   CUtensorMap a_r, b_r, a_s, b_s;
   Fp8Params p{};
-  // pass 1: gate/up
+  // pass 1: gate/up (a_*: weights, b_*: tokens)
   if ((st = make_map_u8(&a_r, w_gu8, 2LL * N * I, d, 256)) != MOE_OK) return st;
   if ((st = make_map_u8(&b_r, x_perm, A, d, bn)) != MOE_OK) return st;
   if (has_shared) {
@@ -486,10 +513,14 @@ moe_status expert_ffn_fp8(const moe_shape* s, const void* x_perm,
   p.sh_shared = has_shared ? scales(h8s, T, SI) : nullptr;
   p.ldsh_shared = T;
   p.item_counter = ctr;
-  st = small
-           ? launch_gemm_fp8<32, 1, true, true, 6>(a_r, b_r, a_s, b_s, p, sms, cs)
-           : launch_gemm_fp8<128, 2, true, true, 4>(a_r, b_r, a_s, b_s, p, sms,
-                                                    cs);
+  if (tm)
+    st = launch_gemm_fp8_tm<true, 4>(a_r, b_r, a_s, b_s, p, sms, cs);
+  else
+    st = small
+             ? launch_gemm_fp8<32, 1, true, true, 6>(a_r, b_r, a_s, b_s, p, sms,
+                                                     cs)
+             : launch_gemm_fp8<128, 2, true, true, 4>(a_r, b_r, a_s, b_s, p,
+                                                      sms, cs);
   if (st != MOE_OK) return st;
   // pass 2: down, two 128-row tiles of W_down per item when d allows
   const bool two = d % 256 == 0;
@@ -522,6 +553,7 @@ moe_status expert_ffn_fp8(const moe_shape* s, const void* x_perm,
   p.ld_shared = d;
   p.sh_shared = nullptr;
   p.item_counter = ctr + 1;
+  if (tm) return launch_gemm_fp8_tm<false, 4>(a_r, b_r, a_s, b_s, p, sms, cs);
   if (small)
     return two ? launch_gemm_fp8<32, 1, true, false, 6>(a_r, b_r, a_s, b_s, p,
                                                         sms, cs)

@@ -429,7 +429,7 @@ def run_ours(args, cfg):
                 "peak": tc_peak, "unit": "TFLOP/s",
                 "frac": ach / tc_peak,
                 "traffic": MEASURED_TRAFFIC.get(cfg.name),
-                "kernel": ("grouped_gemm_fp8_kernel<128,2,*>" if fp8 else
+                "kernel": ("grouped_gemm_fp8_tm_kernel" if fp8 else
                            "grouped_gemm_pair_kernel") +
                           " (gate/up + down launches of one expert-FFN call)",
                 "peak_source": tc_src,

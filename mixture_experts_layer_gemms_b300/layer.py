@@ -154,6 +154,33 @@ class MoELayer:
 
     __call__ = forward
 
+    def graph(self, u: torch.Tensor, update_bias: bool = False,
+              gamma: float = 1e-3):
+        """Capture one forward on ``u`` (a fixed device buffer) into a CUDA
+        graph and return a function that replays it.  Every call of the step
+        is asynchronous with no host synchronisation, so the whole step --
+        route, permute, expert FFNs, combine (and the bias update when asked)
+        -- replays as one graph launch.  Write new tokens into ``u`` between
+        replays; the result is this layer's buffer for ``u.shape[0]``.  With
+        ``update_bias`` every replay moves the bias once."""
+        T = u.shape[0]
+        self.buffers(T)
+        side = torch.cuda.Stream(device=u.device)
+        side.wait_stream(torch.cuda.current_stream(u.device))
+        with torch.cuda.stream(side):      # first-use set-up outside capture
+            self.forward(u)
+        torch.cuda.current_stream(u.device).wait_stream(side)
+        torch.cuda.synchronize(u.device)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            h = self.forward(u, update_bias=update_bias, gamma=gamma)
+
+        def replay() -> torch.Tensor:
+            g.replay()
+            return h
+        replay.graph = g
+        return replay
+
     # --- checkpoint of the routing bias (the layer's only changing state) --
     def save_state(self, path: str, step: int) -> None:
         """Write the current bias and the index of the next step."""

@@ -582,3 +582,26 @@ def test_wait_timeout_is_reported_and_context_survives(moe):
     idx, gate, counts = _route_gpu(moe, cfg, t["u"].cuda(), t["E"].cuda(),
                                    t["b"].cuda())
     assert counts.sum() == cfg.T * cfg.top_k
+
+
+@pytest.mark.parametrize("name,quant", [("mid", None), ("mid", "fp8")])
+def test_layer_cuda_graph_replay(moe, name, quant):
+    """One captured step replays bit-identically to the eager step, and
+    follows new tokens written into its input buffer."""
+    cfg = get_config(name).with_(T=512)
+    g = make_inputs(cfg)
+    mk = lambda: moe.MoELayer(g["E"], g["b"].clone(), g["w_gate"], g["w_up"],
+                              g["w_down"], g["ws_gate"], g["ws_up"],
+                              g["ws_down"], top_k=cfg.top_k, quant=quant)
+    eager, graphed = mk(), mk()
+    u = g["u"].clone()
+    run = graphed.graph(u)
+    for seed in (0, 1):
+        if seed:
+            u.copy_(torch.randn(u.shape, generator=torch.Generator(
+                device="cuda").manual_seed(7), device="cuda").to(u.dtype))
+        want = eager(u).clone()
+        got = run().clone()
+        torch.cuda.synchronize()
+        moe.get_device_error()
+        assert torch.equal(want, got), seed

@@ -324,32 +324,40 @@ def run_ours(args, cfg):
     bufs = layer.buffers(cfg.T)
     sh = layer.shape(cfg.T)
     stream = torch.cuda.current_stream()
-    ev = [(torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    # events between the calls of every timed step: route | permute |
+    # expert_ffn | combine | update_bias
+    CALLS = ("route", "permute", "expert_ffn", "combine", "update_bias")
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)]
+          for _ in range(args.steps)]
 
     def step(i=None):
         """One step through the C ABI; returns kernels launched."""
+        def mark(j):
+            if i is not None:
+                ev[i][j].record(stream)
         n = 0
+        mark(0)
         moe.route(sh, u, layer.E, layer.bias, bufs.topk_idx, bufs.topk_gate,
                   bufs.counts, bufs.workspace)
         n += moe.last_launch_count()
+        mark(1)
         moe.permute(sh, u, bufs.topk_idx, bufs.counts, bufs.offsets,
                     bufs.perm, bufs.inv, bufs.x_perm, bufs.workspace)
         n += moe.last_launch_count()
-        if i is not None:
-            ev[i][0].record(stream)
+        mark(2)
         moe.expert_ffn(sh, bufs.x_perm, bufs.offsets, layer.w_gu,
                        layer.w_down, u, layer.ws_gu, layer.ws_down,
                        bufs.y_perm, bufs.y_shared, bufs.workspace)
         n += moe.last_launch_count()
-        if i is not None:
-            ev[i][1].record(stream)
+        mark(3)
         moe.combine(sh, u, bufs.y_perm, bufs.y_shared, bufs.inv,
                     bufs.topk_gate, bufs.h)
         n += moe.last_launch_count()
+        mark(4)
         moe.update_bias(cfg.n_routed, bufs.counts, cfg.T * cfg.top_k,
                         cfg.gamma, layer.bias)
         n += moe.last_launch_count()
+        mark(5)
         return n
 
     def barrier():
@@ -379,7 +387,9 @@ def run_ours(args, cfg):
     clk = clocks.stop()
     moe.get_device_error()
     ms = max_over_ranks(t0.elapsed_time(t1), dev)
-    ffn_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    call_ms = {c: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in ev)
+               for j, c in enumerate(CALLS)}
+    ffn_ms = call_ms["expert_ffn"]
     counts = bufs.counts.cpu().numpy()
 
     # end to end through the public API with host buffers: H2D of u from
@@ -453,6 +463,22 @@ def run_ours(args, cfg):
                 "frac_of_sustained": (ach / (sus * (2.0 if fp8 else 1.0))
                                       if sus else None)}
     roof["ms_per_launch_pair"] = ffn_ms
+    # algorithmic bytes of the bandwidth calls (read + write), judged in GB/s
+    A = cfg.T * cfg.top_k
+    es = 2 if cfg.dtype == "bf16" else 4           # u, E, y elements
+    xe = 1.0 + 4.0 / 128 if fp8 else es            # x_perm bytes / element
+    hb = bufs.h.element_size()
+    ys = es if cfg.n_shared else 0
+    call_bytes = {
+        "route": cfg.T * cfg.d * es + cfg.n_routed * cfg.d * es + A * 8 +
+                 cfg.n_routed * 4,
+        "permute": cfg.T * cfg.d * es + A * cfg.d * xe + A * 12,
+        "combine": cfg.T * cfg.d * (es + ys + hb) + A * cfg.d * es + A * 8,
+        "update_bias": cfg.n_routed * 12,
+    }
+    per_call = {c: {"ms": round(call_ms[c], 4)} for c in CALLS}
+    for c, nbytes in call_bytes.items():
+        per_call[c]["gbs"] = round(nbytes / (call_ms[c] / 1e3) / 1e9, 1)
     line = {"metric": METRIC, "value": value, "unit": "tokens/s",
             "n_gpus": ws, "steps": args.steps, "warmup": max(3, args.warmup),
             "ms_per_step": ms_step, "higher_is_better": True,
@@ -469,6 +495,7 @@ def run_ours(args, cfg):
             "roofline": roof,
             "clocks": clk,
             "gpu_launches": launches * ws,
+            "per_call": per_call,
             "graph": {"value": whole_job_rate(ws, cfg.T, args.steps, g_ms),
                       "unit": "tokens/s", "ms_per_step": g_ms / args.steps,
                       "note": "the same step replayed from one CUDA graph"},

@@ -35,8 +35,9 @@ METRIC = "MoE-layer tokens/s at V3 shape"
 # DRAM bytes (read + write) of one expert-FFN call (the grouped GEMM's two
 # launches) from an ncu capture of the same kernel on a smaller case of the
 # same shape, scaled by the units processed (see profiles/
-# grouped_gemm_pair_small_v3dims.md).  None where no capture exists.
-MEASURED_TRAFFIC = {"v3_prefill": 25.6e9}
+# grouped_gemm_pair_small_v3dims.md, grouped_gemm_fp8_tm_small_v3dims.md).
+# None where no capture exists.
+MEASURED_TRAFFIC = {"v3_prefill": 25.6e9, "v3_prefill_fp8": 13.6e9}
 L2_NOTE = "inputs larger than L2 (22.5 GB of expert weights read per step)"
 
 
@@ -156,7 +157,7 @@ def _dist():
     return ws, rank, local
 
 
-def cpu_baseline(cfg, t, budget_s: float = 15.0, max_tokens: int = 64):
+def cpu_baseline(cfg, t, budget_s: float = 15.0, max_tokens: int = 512):
     """The fp64 oracle, as it stands, on a bounded sample of this workload:
     the whole routing of sampled tokens plus their routed and shared FFNs.
     Returns tokens/s and what the sample was."""

@@ -137,6 +137,8 @@ FP8_CASES = {
     "mid_dims_T700": ("mid", dict(T=700)),
     # d % 256 != 0: prefill-sized groups on the weights-on-M kernels
     "fallback_d384_T1200": ("tiny", dict(SMALL, T=1200, d=384, d_ff=256)),
+    "no_shared_T1": ("tiny", dict(SMALL, T=1, n_shared=0)),
+    "no_shared_T900": ("tiny", dict(SMALL, T=900, n_shared=0, d=512)),
 }
 
 
@@ -189,3 +191,13 @@ def test_fp8_full_size_sampled(moe, name, n_sample):
     h_ref, r, u64 = _fp8_oracle_h(g, cfg, idx, rows)
     got = h.float().cpu().numpy()[rows]
     assert_close(got, h_ref, base=u64, what=name)
+
+
+def test_fp8_empty_batch(moe):
+    cfg = get_config("tiny").with_(**dict(SMALL, T=0))
+    g = make_inputs(cfg.with_(T=4))
+    layer = _layer(moe, g, cfg)
+    h = layer(g["u"][:0])
+    torch.cuda.synchronize()
+    moe.get_device_error()
+    assert h.shape == (0, cfg.d)

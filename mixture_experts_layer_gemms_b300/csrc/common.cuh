@@ -120,16 +120,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m,
       : "memory");
 }
 
-// Prefetch of a 2-D tile into L2 (no shared memory, no completion signal).
-__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* m, int x,
-                                                   int y) {
-  asm volatile(
-      "cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-          reinterpret_cast<uint64_t>(m)),
-      "r"(x), "r"(y)
-      : "memory");
-}
-
 // --------------------------------------------------------------- tcgen05 --
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile(
@@ -324,18 +314,9 @@ __device__ __forceinline__ void mbar_drain_cl(uint32_t bar, uint32_t parity) {
   }
 }
 // TMA tile load by one CTA of a pair whose completion is counted on an
-// mbarrier that may live in the peer CTA (cluster address).
-__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst,
-                                                 const CUtensorMap* m, int x,
-                                                 int y, uint32_t bar_cluster) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::"
-      "complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(x), "r"(y)
-      : "memory");
-}
-// 3-D variant (box {64, rows, atoms}: `atoms` 128-byte K-atoms of `rows`
-// rows, stacked atom-major in shared memory).
+// mbarrier that may live in the peer CTA (cluster address): a 3-D box
+// {64, rows, atoms} -- `atoms` 128-byte K-atoms of `rows` rows, stacked
+// atom-major in shared memory.
 __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst,
                                                  const CUtensorMap* m, int row,
                                                  int katom, uint32_t bar_cluster) {

@@ -20,7 +20,8 @@ def moe():
 
 
 def declared_functions():
-    txt = open(HEADER).read()
+    with open(HEADER) as f:
+        txt = f.read()
     return sorted(set(re.findall(r"MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(", txt)))
 
 

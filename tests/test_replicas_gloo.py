@@ -40,7 +40,7 @@ def _worker(rank, world, port, out):
 
 def test_two_replicas_time_and_rate():
     world = 2
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:   # no fork of this process
         out = m.dict()
         mp.spawn(_worker, args=(world, _free_port(), out), nprocs=world,
                  join=True)

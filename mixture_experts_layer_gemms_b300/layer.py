@@ -132,8 +132,10 @@ class MoELayer:
         return b
 
     def forward(self, u: torch.Tensor, update_bias: bool = False,
-                gamma: float = 1e-3, stream=None) -> torch.Tensor:
-        """h for u[T, d]; the result lives in this layer's buffer for T."""
+                gamma: float = 1e-3, stream=None,
+                out: Optional[torch.Tensor] = None) -> torch.Tensor:
+        """h for u[T, d]; the result lives in this layer's buffer for T, or
+        in ``out`` ([T, d], the layer's output dtype) when given."""
         T = u.shape[0]
         b = self.buffers(T)
         sh = self.shape(T)
@@ -145,14 +147,75 @@ class MoELayer:
         _lib.expert_ffn(sh, b.x_perm, b.offsets, self.w_gu, self.w_down, u,
                         self.ws_gu, self.ws_down, b.y_perm, b.y_shared,
                         b.workspace, stream)
-        _lib.combine(sh, u, b.y_perm, b.y_shared, b.inv, b.topk_gate, b.h,
+        h = b.h if out is None else out
+        if h.shape != b.h.shape or h.dtype != b.h.dtype or h.device != u.device:
+            raise ValueError("out must match the layer's output buffer")
+        _lib.combine(sh, u, b.y_perm, b.y_shared, b.inv, b.topk_gate, h,
                      stream)
         if update_bias:
             _lib.update_bias(self.N, b.counts, T * self.K, gamma, self.bias,
                              stream)
-        return b.h
+        return h
 
     __call__ = forward
+
+    def forward_host(self, u_host, h_host, update_bias: bool = False,
+                     gamma: float = 1e-3) -> None:
+        """Run the layer on a sequence of host batches: ``u_host[i]`` (pinned
+        CPU tensors [T, d], the layer's input dtype) -> ``h_host[i]`` (pinned
+        CPU tensors [T, d], the output dtype).  Batch i+1 is uploaded and
+        batch i-1 read back on copy streams while batch i computes: two
+        device input and two device output buffers, ordered by events.
+        Returns once every result is on the host.  With ``update_bias`` each
+        batch is a training step (the bias moves after each batch, in batch
+        order)."""
+        n = len(u_host)
+        if n == 0:
+            return
+        dev = self.E.device
+        T = u_host[0].shape[0]
+        for x, y in zip(u_host, h_host):
+            if x.shape[0] != T or y.shape[0] != T:
+                raise ValueError("all batches must have the same T")
+        b = self.buffers(T)
+        comp = torch.cuda.current_stream(dev)
+        up = torch.cuda.Stream(device=dev)
+        down = torch.cuda.Stream(device=dev)
+        u_dev = [torch.empty((T, self.d), dtype=self.dtype, device=dev)
+                 for _ in range(2)]
+        h_dev = [torch.empty_like(b.h) for _ in range(2)]
+        uploaded = [torch.cuda.Event() for _ in range(2)]
+        consumed = [torch.cuda.Event() for _ in range(2)]   # u buffer free
+        computed = [torch.cuda.Event() for _ in range(2)]
+        read_back = [torch.cuda.Event() for _ in range(2)]  # h buffer free
+        for e in consumed + read_back:
+            e.record(comp)
+
+        def upload(i):
+            j = i % 2
+            up.wait_event(consumed[j])
+            with torch.cuda.stream(up):
+                u_dev[j].copy_(u_host[i], non_blocking=True)
+                uploaded[j].record(up)
+
+        upload(0)
+        for i in range(n):
+            j = i % 2
+            if i + 1 < n:
+                upload(i + 1)
+            comp.wait_event(uploaded[j])
+            comp.wait_event(read_back[j])
+            self.forward(u_dev[j], update_bias=update_bias, gamma=gamma,
+                         out=h_dev[j])
+            consumed[j].record(comp)
+            computed[j].record(comp)
+            down.wait_event(computed[j])
+            with torch.cuda.stream(down):
+                h_host[i].copy_(h_dev[j], non_blocking=True)
+                read_back[j].record(down)
+        down.synchronize()
+        # the caller's stream sees every step's writes (bias, buffers)
+        comp.wait_stream(down)
 
     def graph(self, u: torch.Tensor, update_bias: bool = False,
               gamma: float = 1e-3):

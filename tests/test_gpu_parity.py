@@ -605,3 +605,29 @@ def test_layer_cuda_graph_replay(moe, name, quant):
         torch.cuda.synchronize()
         moe.get_device_error()
         assert torch.equal(want, got), seed
+
+
+def test_forward_host_pipeline(moe):
+    """Host batches through the copy/compute pipeline give the same h as
+    device-side forwards, in batch order (with the bias moving per batch)."""
+    cfg = get_config("mid").with_(T=256)
+    g = make_inputs(cfg)
+    mk = lambda: moe.MoELayer(g["E"], g["b"].clone(), g["w_gate"], g["w_up"],
+                              g["w_down"], g["ws_gate"], g["ws_up"],
+                              g["ws_down"], top_k=cfg.top_k,
+                              h_dtype=torch.bfloat16)
+    gen = torch.Generator(device="cuda").manual_seed(3)
+    us = [torch.randn((cfg.T, cfg.d), generator=gen, device="cuda")
+          .to(torch.bfloat16) for _ in range(5)]
+    ref_layer = mk()
+    want = [ref_layer(x, update_bias=True).cpu() for x in us]
+    layer = mk()
+    ins = [x.cpu().pin_memory() for x in us]
+    outs = [torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16).pin_memory()
+            for _ in us]
+    layer.forward_host(ins, outs, update_bias=True)
+    torch.cuda.synchronize()
+    moe.get_device_error()
+    for i, (a, b) in enumerate(zip(want, outs)):
+        assert torch.equal(a, b), i
+    assert torch.equal(layer.bias, ref_layer.bias)

@@ -203,6 +203,24 @@ MOE_API moe_status moe_expert_ffn(const moe_shape* shape, const void* x_perm,
                           void* y_perm, void* y_shared, void* workspace,
                           size_t workspace_bytes, void* stream);
 
+/* One part of moe_expert_ffn: part 1 = the routed experts only (y_perm),
+ * part 2 = the shared experts only (y_shared; x_perm, offsets, w_gu_packed,
+ * w_down and y_perm may be NULL), part 0 = both (moe_expert_ffn).  A part-2
+ * call uses its own item counters and workspace regions, so it may run on
+ * another stream at the same time as the routing, the permute and a part-1
+ * call on the same workspace (the shared experts need no routing).  bf16
+ * and fp32 shapes; MOE_FP8 takes part 0 only (MOE_ERR_UNSUPPORTED).      */
+MOE_API moe_status moe_expert_ffn_part(const moe_shape* shape, int part,
+                                       const void* x_perm,
+                                       const int32_t* offsets,
+                                       const void* w_gu_packed,
+                                       const void* w_down, const void* u,
+                                       const void* ws_gu_packed,
+                                       const void* ws_down_packed,
+                                       void* y_perm, void* y_shared,
+                                       void* workspace,
+                                       size_t workspace_bytes, void* stream);
+
 /* Combine (FFN-output equation):
  *  h[t] = u[t] + y_shared[t] + sum_k topk_gate[t,k] * y_perm[inv[t,k]],
  * accumulated in fp32 in that order; h is written as h_dtype.  y_shared may

@@ -28,7 +28,7 @@ EXPORTED = ("moe_workspace_size", "moe_pack_weights", "moe_route",
             "moe_last_error_detail", "moe_last_launch_count",
             "moe_route_noalloc", "moe_selftest_wait_timeout",
             "moe_route_grouped", "moe_fp8_weight_bytes",
-            "moe_pack_weights_fp8", "moe_x_perm_bytes")
+            "moe_pack_weights_fp8", "moe_x_perm_bytes", "moe_expert_ffn_part")
 
 
 class MoEError(RuntimeError):
@@ -70,6 +70,7 @@ def _load() -> ctypes.CDLL:
         "moe_fp8_weight_bytes": [SP, I, ctypes.POINTER(ctypes.c_size_t)],
         "moe_pack_weights_fp8": [SP, P, P, P, P, P, P, P, P, P, P, V],
         "moe_x_perm_bytes": [SP, ctypes.POINTER(ctypes.c_size_t)],
+        "moe_expert_ffn_part": [SP, I, P, P, P, P, P, P, P, P, P, P, Z, V],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -207,6 +208,19 @@ def expert_ffn(shape, x_perm, offsets, w_gu_packed, w_down, u, ws_gu_packed,
                               _ptr(y_perm), _ptr(y_shared), _ptr(workspace),
                               workspace.numel() * workspace.element_size(),
                               _stream(stream)), "moe_expert_ffn")
+
+
+def expert_ffn_part(shape, part, x_perm, offsets, w_gu_packed, w_down, u,
+                    ws_gu_packed, ws_down_packed, y_perm, y_shared, workspace,
+                    stream=None) -> None:
+    """part 1: routed experts only; part 2: shared experts only (may run on
+    another stream beside the routing, the permute and a part-1 call)."""
+    _check(LIB.moe_expert_ffn_part(
+        ctypes.byref(shape), int(part), _ptr(x_perm), _ptr(offsets),
+        _ptr(w_gu_packed), _ptr(w_down), _ptr(u), _ptr(ws_gu_packed),
+        _ptr(ws_down_packed), _ptr(y_perm), _ptr(y_shared), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)),
+        "moe_expert_ffn_part")
 
 
 def combine(shape, u, y_perm, y_shared, inv, topk_gate, h, stream=None) -> None:

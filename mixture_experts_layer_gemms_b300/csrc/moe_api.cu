@@ -268,8 +268,8 @@ WsLayout ws_layout(const moe_shape* s) {
   const long long nblk = cdiv(s->T, kRouteTile);
   const long long A = static_cast<long long>(s->T) * s->top_k;
   size_t off = 0;
-  w.sched = off;                      // item counters of the GEMM passes
-  off = round256(off + 2 * sizeof(int));
+  w.sched = off;   // item counters: [0..1] whole / routed call, [2..3] shared
+  off = round256(off + 4 * sizeof(int));
   w.route_hist = off;   // one histogram per router CTA (<= 8 per tile)
   off = round256(off + static_cast<size_t>(nblk) * kRtMaxSplit *
                            s->n_routed * 4);
@@ -882,23 +882,32 @@ moe_status moe_permute(const moe_shape* s, const void* u,
 }
 
 
-moe_status moe_expert_ffn(const moe_shape* s, const void* x_perm,
-                          const int32_t* offsets, const void* w_gu_packed,
-                          const void* w_down, const void* u,
-                          const void* ws_gu_packed, const void* ws_down_packed,
-                          void* y_perm, void* y_shared, void* ws,
-                          size_t ws_bytes, void* stream) {
+static moe_status expert_ffn_impl(const moe_shape* s, int part,
+                                  const void* x_perm, const int32_t* offsets,
+                                  const void* w_gu_packed, const void* w_down,
+                                  const void* u, const void* ws_gu_packed,
+                                  const void* ws_down_packed, void* y_perm,
+                                  void* y_shared, void* ws, size_t ws_bytes,
+                                  void* stream) {
   g_launches = 0;
   moe_status st = check_shape(s);
   if (st != MOE_OK) return st;
-  NEED_PTR(offsets);
-  NEED_PTR(w_gu_packed);
-  NEED_PTR(w_down);
-  if (s->T > 0) {
-    NEED_PTR(x_perm);
-    NEED_PTR(y_perm);
+  if (part < 0 || part > 2)
+    return fail(MOE_ERR_INVALID_ARG, "part=%d (0 both, 1 routed, 2 shared)",
+                part);
+  if (part != 0 && s->dtype == MOE_FP8)
+    return fail(MOE_ERR_UNSUPPORTED, "MOE_FP8: expert FFN parts not split");
+  const bool do_routed = part != 2;
+  if (do_routed) {
+    NEED_PTR(offsets);
+    NEED_PTR(w_gu_packed);
+    NEED_PTR(w_down);
+    if (s->T > 0) {
+      NEED_PTR(x_perm);
+      NEED_PTR(y_perm);
+    }
   }
-  const bool has_shared = s->n_shared > 0 && s->T > 0;
+  const bool has_shared = part != 1 && s->n_shared > 0 && s->T > 0;
   if (has_shared) {
     NEED_PTR(u);
     NEED_PTR(ws_gu_packed);
@@ -922,14 +931,17 @@ moe_status moe_expert_ffn(const moe_shape* s, const void* x_perm,
     const float* xp = static_cast<const float*>(x_perm);
     float* hr = static_cast<float*>(h_r);
     float* hs = static_cast<float*>(h_s);
-    ffn_f32_gate_up_kernel<<<grid2(I, A), 256, 0, cs>>>(
-        xp, static_cast<int>(A), offsets, N,
-        static_cast<const float*>(w_gu_packed), I, d, hr);
-    MOE_CHECK_LAUNCH();
-    ffn_f32_down_kernel<<<grid2(d, A), 256, 0, cs>>>(
-        hr, static_cast<int>(A), offsets, N, static_cast<const float*>(w_down),
-        I, d, static_cast<float*>(y_perm));
-    MOE_CHECK_LAUNCH();
+    if (do_routed) {
+      ffn_f32_gate_up_kernel<<<grid2(I, A), 256, 0, cs>>>(
+          xp, static_cast<int>(A), offsets, N,
+          static_cast<const float*>(w_gu_packed), I, d, hr);
+      MOE_CHECK_LAUNCH();
+      ffn_f32_down_kernel<<<grid2(d, A), 256, 0, cs>>>(
+          hr, static_cast<int>(A), offsets, N,
+          static_cast<const float*>(w_down), I, d,
+          static_cast<float*>(y_perm));
+      MOE_CHECK_LAUNCH();
+    }
     if (has_shared) {
       ffn_f32_gate_up_kernel<<<grid2(SI, s->T), 256, 0, cs>>>(
           static_cast<const float*>(u), s->T, nullptr, 1,
@@ -954,17 +966,26 @@ moe_status moe_expert_ffn(const moe_shape* s, const void* x_perm,
   // CTA pairs (256 weight rows per item) when every weight group splits
   // into 256-row tiles; else the single-SM kernel.
   const bool pair = !small && d % 256 == 0 && I % 128 == 0;
-  int* ctr = reinterpret_cast<int*>(static_cast<char*>(ws) + w.sched);
+  // a shared-only call counts its items apart, so it can run beside a
+  // routed-only call on another stream
+  int* ctr = reinterpret_cast<int*>(static_cast<char*>(ws) + w.sched) +
+             (part == 2 ? 2 : 0);
   zero_i32_kernel<<<1, 32, 0, cs>>>(ctr, 2);
   MOE_CHECK_LAUNCH();
+  if (!do_routed && !has_shared) return MOE_OK;
+  // operands of the part that is not computed stand in for its maps
+  const void* wgu_r = do_routed ? w_gu_packed : ws_gu_packed;
+  const void* xr = do_routed ? x_perm : u;
+  const long long rows_gu_r = do_routed ? 2LL * N * I : 2LL * SI;
+  const long long rows_x_r = do_routed ? A : s->T;
   CUtensorMap a_r, b_r, a_s, b_s;
   const int box = kBoxRows;
   GemmParams p{};
   // pass 1: gate/up + SwiGLU -> H
-  if ((st = make_map(&a_r, w_gu_packed, 2LL * N * I, d, kGemmBM)) != MOE_OK)
+  if ((st = make_map(&a_r, wgu_r, rows_gu_r, d, kGemmBM)) != MOE_OK)
     return st;
   PairMaps pm;
-  if ((st = make_map(&b_r, x_perm, A, d, box)) != MOE_OK) return st;
+  if ((st = make_map(&b_r, xr, rows_x_r, d, box)) != MOE_OK) return st;
   if (has_shared) {
     if ((st = make_map(&a_s, ws_gu_packed, 2LL * SI, d, kGemmBM)) != MOE_OK)
       return st;
@@ -974,7 +995,7 @@ moe_status moe_expert_ffn(const moe_shape* s, const void* x_perm,
     b_s = b_r;
   }
   p.offsets = offsets;
-  p.n_groups = N;
+  p.n_groups = do_routed ? N : 0;
   p.w_rows_routed = 2 * I;
   p.k_routed = d;
   p.max_routed_rows = A;
@@ -988,7 +1009,7 @@ moe_status moe_expert_ffn(const moe_shape* s, const void* x_perm,
   p.swiglu = 1;
   p.item_counter = ctr;
   if (pair) {
-    if ((st = pair_maps(w_gu_packed, 2LL * N * I, x_perm, A, d,
+    if ((st = pair_maps(wgu_r, rows_gu_r, xr, rows_x_r, d,
                         has_shared ? ws_gu_packed : nullptr, 2LL * SI,
                         u, s->T, d, pm)) != MOE_OK)
       return st;
@@ -999,10 +1020,13 @@ moe_status moe_expert_ffn(const moe_shape* s, const void* x_perm,
   }
   if (st != MOE_OK) return st;
   // pass 2: down -> y
-  if ((st = make_map(&a_r, w_down, static_cast<long long>(N) * d, I,
-                     kGemmBM)) != MOE_OK)
+  const void* wd_r = do_routed ? w_down : ws_down_packed;
+  const long long rows_d_r = do_routed ? static_cast<long long>(N) * d : d;
+  const long long k_r2 = do_routed ? I : SI;
+  const void* hr_ = do_routed ? h_r : h_s;
+  if ((st = make_map(&a_r, wd_r, rows_d_r, k_r2, kGemmBM)) != MOE_OK)
     return st;
-  if ((st = make_map(&b_r, h_r, A, I, box)) != MOE_OK) return st;
+  if ((st = make_map(&b_r, hr_, rows_x_r, k_r2, box)) != MOE_OK) return st;
   if (has_shared) {
     if ((st = make_map(&a_s, ws_down_packed, d, SI, kGemmBM)) != MOE_OK)
       return st;
@@ -1023,7 +1047,7 @@ moe_status moe_expert_ffn(const moe_shape* s, const void* x_perm,
   p.y_fp16 = 1;
   p.item_counter = ctr + 1;
   if (pair) {
-    if ((st = pair_maps(w_down, static_cast<long long>(N) * d, h_r, A, I,
+    if ((st = pair_maps(wd_r, rows_d_r, hr_, rows_x_r, k_r2,
                         has_shared ? ws_down_packed : nullptr, d, h_s, s->T,
                         SI, pm)) != MOE_OK)
       return st;
@@ -1031,6 +1055,29 @@ moe_status moe_expert_ffn(const moe_shape* s, const void* x_perm,
   }
   return small ? launch_gemm<32, 10>(a_r, b_r, a_s, b_s, p, sms, cs)
                : launch_gemm<256, 4>(a_r, b_r, a_s, b_s, p, sms, cs);
+}
+
+moe_status moe_expert_ffn(const moe_shape* s, const void* x_perm,
+                          const int32_t* offsets, const void* w_gu_packed,
+                          const void* w_down, const void* u,
+                          const void* ws_gu_packed, const void* ws_down_packed,
+                          void* y_perm, void* y_shared, void* ws,
+                          size_t ws_bytes, void* stream) {
+  return expert_ffn_impl(s, 0, x_perm, offsets, w_gu_packed, w_down, u,
+                         ws_gu_packed, ws_down_packed, y_perm, y_shared, ws,
+                         ws_bytes, stream);
+}
+
+moe_status moe_expert_ffn_part(const moe_shape* s, int part,
+                               const void* x_perm, const int32_t* offsets,
+                               const void* w_gu_packed, const void* w_down,
+                               const void* u, const void* ws_gu_packed,
+                               const void* ws_down_packed, void* y_perm,
+                               void* y_shared, void* ws, size_t ws_bytes,
+                               void* stream) {
+  return expert_ffn_impl(s, part, x_perm, offsets, w_gu_packed, w_down, u,
+                         ws_gu_packed, ws_down_packed, y_perm, y_shared, ws,
+                         ws_bytes, stream);
 }
 
 moe_status moe_combine(const moe_shape* s, const void* u, const void* y_perm,

@@ -43,10 +43,11 @@ class MoELayer:
                  ws_down: Optional[torch.Tensor] = None, top_k: int = 8,
                  h_dtype: torch.dtype = torch.float32, stream=None,
                  n_groups: int = 1, topk_groups: int = 1,
-                 quant: Optional[str] = None):
+                 quant: Optional[str] = None, overlap_shared: bool = False):
         """quant="fp8": bf16 weights are quantized to e4m3 with block scales
         and the expert GEMMs run in e4m3 (activations and router stay
-        bf16)."""
+        bf16).  overlap_shared: run the shared experts on a side stream
+        beside the permute (bf16 layers, T >= 1024, default stream only)."""
         if not E.is_cuda:
             raise ValueError("MoELayer needs CUDA tensors")
         if quant not in (None, "fp8"):
@@ -94,10 +95,22 @@ class MoELayer:
                               ws_down, self.w_gu, self.ws_gu, self.ws_down,
                               stream)
         self._bufs: Dict[int, Buffers] = {}
+        self.overlap_shared = bool(overlap_shared)
+        self._side = None
 
     def shape(self, T: int) -> _lib.MoeShape:
         return _lib.make_shape(T, self.d, self.N, self.K, self.S, self.I,
                                self.code)
+
+    def _shared_side_stream(self, u: torch.Tensor):
+        """Side stream for the shared experts when the overlap is on (bf16
+        layers with shared experts and prefill-sized batches)."""
+        if not (self.overlap_shared and self.S and self.code == self.dtype
+                and self.dtype == torch.bfloat16 and u.shape[0] >= 1024):
+            return None
+        if self._side is None:
+            self._side = torch.cuda.Stream(device=u.device)
+        return self._side
 
     def buffers(self, T: int) -> Buffers:
         b = self._bufs.get(T)
@@ -142,11 +155,28 @@ class MoELayer:
         _lib.route_grouped(sh, self.n_groups, self.topk_groups, u, self.E,
                            self.bias, b.topk_idx, b.topk_gate, b.counts,
                            b.workspace, stream)
+        side = self._shared_side_stream(u) if stream is None else None
+        if side is not None:
+            # the shared experts need no routing: they run on a side stream
+            # beside the permute and join before the routed experts' output
+            # is combined
+            main = torch.cuda.current_stream(u.device)
+            side.wait_stream(main)
+            with torch.cuda.stream(side):
+                _lib.expert_ffn_part(sh, 2, None, None, None, None, u,
+                                     self.ws_gu, self.ws_down, None,
+                                     b.y_shared, b.workspace)
         _lib.permute(sh, u, b.topk_idx, b.counts, b.offsets, b.perm, b.inv,
                      b.x_perm, b.workspace, stream)
-        _lib.expert_ffn(sh, b.x_perm, b.offsets, self.w_gu, self.w_down, u,
-                        self.ws_gu, self.ws_down, b.y_perm, b.y_shared,
-                        b.workspace, stream)
+        if side is not None:
+            _lib.expert_ffn_part(sh, 1, b.x_perm, b.offsets, self.w_gu,
+                                 self.w_down, u, None, None, b.y_perm, None,
+                                 b.workspace)
+            main.wait_stream(side)
+        else:
+            _lib.expert_ffn(sh, b.x_perm, b.offsets, self.w_gu, self.w_down,
+                            u, self.ws_gu, self.ws_down, b.y_perm, b.y_shared,
+                            b.workspace, stream)
         h = b.h if out is None else out
         if h.shape != b.h.shape or h.dtype != b.h.dtype or h.device != u.device:
             raise ValueError("out must match the layer's output buffer")

@@ -172,3 +172,23 @@ def test_fp8_sizes_and_checks(moe):
                                   P(1024), P(1280), P(1536), P(1792),
                                   P(2048), None)
     assert st == 1 and b"moe_pack_weights_fp8" in moe.LIB.moe_last_error_detail()
+
+
+@pytest.mark.parametrize("dtype_name,part,code,detail", [
+    ("MOE_BF16", 3, 1, b"part=3"),
+    ("MOE_BF16", -1, 1, b"part=-1"),
+    ("MOE_FP8", 1, 2, b"not split"),
+    ("MOE_FP8", 2, 2, b"not split"),
+])
+def test_expert_ffn_part_validation(moe, dtype_name, part, code, detail):
+    """A part outside {0, 1, 2}, or a split call of an e4m3 layer, fails
+    before anything is launched."""
+    sh = _shape(moe, dtype=getattr(moe, dtype_name), d_ff=256)
+    _, n = _ws(moe, sh)
+    P = ctypes.c_void_p
+    st = moe.LIB.moe_expert_ffn_part(ctypes.byref(sh), part, P(256), P(512),
+                                     P(768), P(1024), P(1280), P(1536),
+                                     P(1792), P(2048), P(2304), P(4096), n,
+                                     None)
+    assert st == code
+    assert detail in moe.LIB.moe_last_error_detail()

@@ -631,3 +631,32 @@ def test_forward_host_pipeline(moe):
     for i, (a, b) in enumerate(zip(want, outs)):
         assert torch.equal(a, b), i
     assert torch.equal(layer.bias, ref_layer.bias)
+
+
+@pytest.mark.parametrize("name,T", [("mid", 1024), ("mid", 3000),
+                                    ("v3_prefill", 2048)])
+def test_shared_overlap_matches(moe, name, T):
+    """The shared experts on a side stream (beside the permute and the
+    routed experts) give the same h, bit for bit, as the single call, eager
+    and replayed from a CUDA graph."""
+    cfg = get_config(name).with_(T=T)
+    g = make_inputs(cfg) if name != "v3_prefill" else generate(cfg, "cuda")
+    mk = lambda ov: moe.MoELayer(g["E"], g["b"].clone(), g["w_gate"],
+                                 g["w_up"], g["w_down"], g["ws_gate"],
+                                 g["ws_up"], g["ws_down"], top_k=cfg.top_k,
+                                 h_dtype=torch.bfloat16, overlap_shared=ov)
+    plain, side = mk(False), mk(True)
+    u = g["u"].clone()
+    assert side._shared_side_stream(u) is not None
+    want = plain(u, update_bias=True).clone()
+    got = side(u, update_bias=True).clone()
+    torch.cuda.synchronize()
+    moe.get_device_error()
+    assert torch.equal(want, got)
+    assert torch.equal(plain.bias, side.bias)
+    run = side.graph(u)
+    want = plain(u).clone()
+    got = run().clone()
+    torch.cuda.synchronize()
+    moe.get_device_error()
+    assert torch.equal(want, got)

@@ -7,7 +7,8 @@ code.  The one common dependency is ``moe_inputs`` (seeded random inputs,
 no layer arithmetic).
 
 See ``oracle/moe.py`` for the definitions and their sources,
-``oracle/fp8.py`` for the e4m3 block-scaled expert FFN, and
+``oracle/fp8.py`` for the e4m3 block-scaled expert FFN,
+``oracle/backward.py`` for the gradients of the layer (Dgrad / Wgrad), and
 ``oracle/micro.py`` for the pure-Python scalar cross-check.
 """
 from .moe import (  # noqa: F401

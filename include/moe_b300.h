@@ -261,6 +261,51 @@ MOE_API const char* moe_last_error_detail(void);
  * issued (for launch accounting).                                         */
 MOE_API int moe_last_launch_count(void);
 
+/* ----------------------------------------------------------------------
+ * Backward pass (training): the gradients of the layer output h with
+ * respect to u, the centroids E and every expert weight, for an upstream
+ * gradient dh = dL/dh.  The three GEMMs of each linear operator (forward,
+ * activation gradient "Dgrad", weight gradient "Wgrad"): "AI新顶流-DeepSeek
+ * 技术大揭秘" (blog.csdn.net), section "FP8混合精度训练框架"; the layer whose
+ * derivative is taken is the FFN-output equation above.  The chain rule,
+ * per selected expert e of token t (g = topk_gate, x = u_t):
+ *   dY = g dh_t;   dW_down += dY H^T;   dH = W_down^T dY;
+ *   da = dH c SiLU'(a), dc = dH SiLU(a)  (a = W_gate x, c = W_up x);
+ *   dW_gate += da x^T;  dW_up += dc x^T;  du_t += W_gate^T da + W_up^T dc;
+ *   dz = (dh_t . y) g (1 - g)  (y = FFN_e(x), z = u_t . e_e);
+ *   du_t += dz e_e;  dE_e += dz u_t;
+ * shared experts the same with g = 1 and no gate term; du_t += dh_t.  The
+ * selection is piecewise constant and the bias receives no gradient.
+ *
+ * Inputs: the forward's own tensors: u [T, d], centroids [N, d] (bf16),
+ * topk_idx / topk_gate [T, K] (moe_route), offsets [N+1] and inv [T, K]
+ * (moe_permute), y_perm [T*K, d] fp16 (moe_expert_ffn), the packed weights
+ * of moe_pack_weights and w_down; dh [T, d] bf16.
+ * Outputs (overwritten, not accumulated): du [T, d] fp32, dE [N, d] fp32;
+ * dw_gate / dw_up [N, d_ff, d], dw_down [N, d, d_ff] and, when
+ * n_shared > 0, dws_gate / dws_up [S, d_ff, d], dws_down [S, d, d_ff] in
+ * the canonical (unpacked) layouts, as grad_dtype (MOE_F32 or MOE_BF16).
+ * Arithmetic: bf16 GEMM operands (x, dY, H, dA rounded to bf16; a, c
+ * recomputed), fp32 accumulation in TMEM; dH and the input-side products
+ * kept in fp16 between the GEMMs (range checked).  Every call is
+ * asynchronous on `stream`; the workspace (moe_backward_workspace_size,
+ * 256-byte aligned) holds the per-assignment operands in a layout whose
+ * expert segments are padded to 64 rows.
+ * Supported: dtype MOE_BF16 and d_ff a multiple of 128 (else
+ * MOE_ERR_UNSUPPORTED); every pointer 16-byte aligned (else
+ * MOE_ERR_INVALID_ARG).                                                   */
+MOE_API moe_status moe_backward_workspace_size(const moe_shape* shape,
+                                               size_t* bytes);
+MOE_API moe_status moe_backward(
+    const moe_shape* shape, const void* dh, const void* u,
+    const void* centroids, const int32_t* topk_idx, const float* topk_gate,
+    const int32_t* offsets, const int32_t* inv, const void* y_perm,
+    const void* w_gu_packed, const void* w_down, const void* ws_gu_packed,
+    const void* ws_down_packed, float* du, float* dE, void* dw_gate,
+    void* dw_up, void* dw_down, void* dws_gate, void* dws_up, void* dws_down,
+    moe_dtype grad_dtype, void* workspace, size_t workspace_bytes,
+    void* stream);
+
 /* moe_route without a workspace, for callers that cannot allocate device
  * memory at the point of the call: for example a plugin inside an inference
  * engine that is handed only its input and output buffers and may not

@@ -15,7 +15,8 @@ from importlib import import_module
 _FROM_LIB = ("EXPORTED", "LIB", "LIB_PATH", "MOE_BF16", "MOE_F32", "MOE_FP8",
              "MoEError", "fp8_weight_bytes", "pack_weights_fp8",
              "x_perm_bytes",
-             "MoeShape", "combine", "expert_ffn", "expert_ffn_part",
+             "MoeShape", "backward", "backward_workspace_size", "combine",
+             "expert_ffn", "expert_ffn_part",
              "get_device_error",
              "last_launch_count", "make_shape", "pack_weights", "permute",
              "route", "route_grouped", "route_noalloc",

@@ -28,7 +28,8 @@ EXPORTED = ("moe_workspace_size", "moe_pack_weights", "moe_route",
             "moe_last_error_detail", "moe_last_launch_count",
             "moe_route_noalloc", "moe_selftest_wait_timeout",
             "moe_route_grouped", "moe_fp8_weight_bytes",
-            "moe_pack_weights_fp8", "moe_x_perm_bytes", "moe_expert_ffn_part")
+            "moe_pack_weights_fp8", "moe_x_perm_bytes", "moe_expert_ffn_part",
+            "moe_backward_workspace_size", "moe_backward")
 
 
 class MoEError(RuntimeError):
@@ -71,6 +72,8 @@ def _load() -> ctypes.CDLL:
         "moe_pack_weights_fp8": [SP, P, P, P, P, P, P, P, P, P, P, V],
         "moe_x_perm_bytes": [SP, ctypes.POINTER(ctypes.c_size_t)],
         "moe_expert_ffn_part": [SP, I, P, P, P, P, P, P, P, P, P, P, Z, V],
+        "moe_backward_workspace_size": [SP, ctypes.POINTER(ctypes.c_size_t)],
+        "moe_backward": [SP] + [P] * 20 + [I, P, Z, V],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -221,6 +224,30 @@ def expert_ffn_part(shape, part, x_perm, offsets, w_gu_packed, w_down, u,
         _ptr(ws_down_packed), _ptr(y_perm), _ptr(y_shared), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)),
         "moe_expert_ffn_part")
+
+
+def backward_workspace_size(shape: MoeShape) -> int:
+    n = ctypes.c_size_t()
+    _check(LIB.moe_backward_workspace_size(ctypes.byref(shape), ctypes.byref(n)),
+           "moe_backward_workspace_size")
+    return n.value
+
+
+def backward(shape, dh, u, centroids, topk_idx, topk_gate, offsets, inv,
+             y_perm, w_gu_packed, w_down, ws_gu_packed, ws_down_packed, du, dE,
+             dw_gate, dw_up, dw_down, dws_gate, dws_up, dws_down, workspace,
+             stream=None) -> None:
+    """Gradients of the layer for dh; the weight gradients' dtype (fp32 or
+    bf16) is taken from dw_gate."""
+    gd = MOE_BF16 if dw_gate.dtype == torch.bfloat16 else MOE_F32
+    _check(LIB.moe_backward(
+        ctypes.byref(shape), _ptr(dh), _ptr(u), _ptr(centroids),
+        _ptr(topk_idx), _ptr(topk_gate), _ptr(offsets), _ptr(inv),
+        _ptr(y_perm), _ptr(w_gu_packed), _ptr(w_down), _ptr(ws_gu_packed),
+        _ptr(ws_down_packed), _ptr(du), _ptr(dE), _ptr(dw_gate), _ptr(dw_up),
+        _ptr(dw_down), _ptr(dws_gate), _ptr(dws_up), _ptr(dws_down), gd,
+        _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)), "moe_backward")
 
 
 def combine(shape, u, y_perm, y_shared, inv, topk_gate, h, stream=None) -> None:

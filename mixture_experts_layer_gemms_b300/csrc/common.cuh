@@ -408,6 +408,8 @@ enum KernelId : unsigned {
   KID_GEMM = 2,
   KID_GEMM_FP8 = 3,
   KID_QUANT = 4,
+  KID_GEMM_BWD = 5,
+  KID_BWD = 6,
   KID_SELFTEST = 99,
 };
 

@@ -16,6 +16,8 @@
 #include "permute.cuh"
 #include "route.cuh"
 #include "gemm_fp8.cuh"
+#include "bwd.cuh"
+#include "gemm_bwd.cuh"
 #include "moe_b300.h"
 
 using namespace moe;
@@ -103,6 +105,14 @@ moe_status device_setup(int* sm_count) {
                               Fp8TmSmem<4>::alloc));
     MOE_CHECK_CUDA(allow_smem(grouped_gemm_fp8_tm_kernel<false, 4>,
                               Fp8TmSmem<4>::alloc));
+    MOE_CHECK_CUDA(allow_smem(bwd_gemm_kernel<kDgrad, 256, 4>,
+                              BwdSmem<256, 4>::alloc));
+    MOE_CHECK_CUDA(allow_smem(bwd_gemm_kernel<kRecomp, 256, 4>,
+                              BwdSmem<256, 4>::alloc));
+    MOE_CHECK_CUDA(allow_smem(bwd_gemm_kernel<kWgrad, 256, 4>,
+                              BwdSmem<256, 4>::alloc));
+    MOE_CHECK_CUDA(allow_smem(bwd_gemm_kernel<kWgrad, 128, 6>,
+                              BwdSmem<128, 6>::alloc));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (di.sm_count / 2));
     cfg.blockDim = dim3(192);
@@ -1252,6 +1262,337 @@ moe_status moe_route_noalloc(const moe_shape* s, const void* u,
   if (st != MOE_OK) return st;
   return launch_route(s, 1, 1, u, centroids, bias, topk_idx, topk_gate,
                       counts, hist, as_stream(stream));
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Backward pass.
+namespace {
+
+constexpr int kBwdCounters = 8;
+
+// Workspace of moe_backward.  Per-assignment operands live in a padded
+// layout: expert e's rows start at offpad[e] (a multiple of 64) and its
+// segment is a whole number of 64-row blocks, so the layout needs at most
+// A + 63 N rows (A = T K).
+struct BwdLayout {
+  long long A_pad;
+  size_t ctr, offs, offpad, dz, X, dY, dH, H, dA, dX, dH_s, H_s, dA_s, dX_s,
+      total;
+};
+
+BwdLayout bwd_layout(const moe_shape* s) {
+  BwdLayout w;
+  const long long A = static_cast<long long>(s->T) * s->top_k;
+  const long long N = s->n_routed, d = s->d, I = s->d_ff;
+  const long long SI = static_cast<long long>(s->n_shared) * I;
+  w.A_pad = cdiv(A + (kPadRows - 1) * N, kPadRows) * kPadRows;
+  const size_t R = static_cast<size_t>(w.A_pad);
+  const size_t T = static_cast<size_t>(s->T);
+  size_t off = 0;
+  w.ctr = off;     off = round256(off + kBwdCounters * 4);
+  w.offs = off;    off = round256(off + (N + 1) * 4);
+  w.offpad = off;  off = round256(off + (N + 1) * 4);
+  w.dz = off;      off = round256(off + R * 4);
+  w.X = off;       off = round256(off + R * d * 2);
+  w.dY = off;      off = round256(off + R * d * 2);
+  w.dH = off;      off = round256(off + R * I * 2);
+  w.H = off;       off = round256(off + R * I * 2);
+  w.dA = off;      off = round256(off + R * 2 * I * 2);
+  w.dX = off;      off = round256(off + R * d * 2);
+  w.dH_s = off;    off = round256(off + T * SI * 2);
+  w.H_s = off;     off = round256(off + T * SI * 2);
+  w.dA_s = off;    off = round256(off + T * 2 * SI * 2);
+  w.dX_s = off;    off = round256(off + (SI > 0 ? T * d * 2 : 0));
+  w.total = off;
+  return w;
+}
+
+moe_status check_bwd_shape(const moe_shape* s) {
+  moe_status st = check_shape(s);
+  if (st != MOE_OK) return st;
+  if (s->dtype != MOE_BF16)
+    return fail(MOE_ERR_UNSUPPORTED, "backward: bf16 layers only (dtype %d)",
+                static_cast<int>(s->dtype));
+  if (s->d_ff % 128 != 0)
+    return fail(MOE_ERR_UNSUPPORTED,
+                "backward: d_ff=%d must be a multiple of 128", s->d_ff);
+  return MOE_OK;
+}
+
+template <int KIND, int BN, int STAGES>
+moe_status launch_bwd_gemm(const CUtensorMap& a_r, const CUtensorMap& b_r,
+                           const CUtensorMap& a_s, const CUtensorMap& b_s,
+                           const BwdParams& p, long long max_items, int sms,
+                           cudaStream_t cs) {
+  if (max_items <= 0) return MOE_OK;
+  const int grid = static_cast<int>(max_items < sms ? max_items : sms);
+  bwd_gemm_kernel<KIND, BN, STAGES>
+      <<<grid, 192, BwdSmem<BN, STAGES>::alloc, cs>>>(a_r, b_r, a_s, b_s, p);
+  MOE_CHECK_LAUNCH();
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_backward_workspace_size(const moe_shape* s, size_t* bytes) {
+  g_launches = 0;
+  moe_status st = check_bwd_shape(s);
+  if (st != MOE_OK) return st;
+  if (bytes == nullptr) return fail(MOE_ERR_INVALID_ARG, "bytes is NULL");
+  *bytes = bwd_layout(s).total;
+  return MOE_OK;
+}
+
+moe_status moe_backward(const moe_shape* s, const void* dh, const void* u,
+                        const void* centroids, const int32_t* topk_idx,
+                        const float* topk_gate, const int32_t* offsets,
+                        const int32_t* inv, const void* y_perm,
+                        const void* w_gu_packed, const void* w_down,
+                        const void* ws_gu_packed, const void* ws_down_packed,
+                        float* du, float* dE, void* dw_gate, void* dw_up,
+                        void* dw_down, void* dws_gate, void* dws_up,
+                        void* dws_down, moe_dtype grad_dtype, void* ws,
+                        size_t ws_bytes, void* stream) {
+  g_launches = 0;
+  moe_status st = check_bwd_shape(s);
+  if (st != MOE_OK) return st;
+  if (grad_dtype != MOE_F32 && grad_dtype != MOE_BF16)
+    return fail(MOE_ERR_INVALID_ARG, "grad_dtype %d",
+                static_cast<int>(grad_dtype));
+  const int T = s->T, N = s->n_routed, d = s->d, I = s->d_ff,
+            K = s->top_k, S = s->n_shared;
+  const int SI = S * I;
+  NEED_PTR(centroids);
+  NEED_PTR(offsets);
+  NEED_PTR(w_gu_packed);
+  NEED_PTR(w_down);
+  NEED_PTR(dE);
+  NEED_PTR(dw_gate);
+  NEED_PTR(dw_up);
+  NEED_PTR(dw_down);
+  if (T > 0) {
+    NEED_PTR(dh);
+    NEED_PTR(u);
+    NEED_PTR(topk_idx);
+    NEED_PTR(topk_gate);
+    NEED_PTR(inv);
+    NEED_PTR(y_perm);
+    NEED_PTR(du);
+  }
+  if (S > 0) {
+    NEED_PTR(ws_gu_packed);
+    NEED_PTR(ws_down_packed);
+    NEED_PTR(dws_gate);
+    NEED_PTR(dws_up);
+    NEED_PTR(dws_down);
+  }
+  const BwdLayout w = bwd_layout(s);
+  if (ws == nullptr) return fail(MOE_ERR_WORKSPACE, "workspace is NULL");
+  if (ws_bytes < w.total)
+    return fail(MOE_ERR_WORKSPACE, "workspace %zu bytes < %zu needed",
+                ws_bytes, w.total);
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+    return fail(MOE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  cudaStream_t cs = as_stream(stream);
+  const size_t gsz = grad_dtype == MOE_BF16 ? 2 : 4;
+  if (T == 0) {   // no tokens: every gradient is zero
+    const size_t wn = static_cast<size_t>(N) * I * d * gsz;
+    MOE_CHECK_CUDA(cudaMemsetAsync(dE, 0, static_cast<size_t>(N) * d * 4, cs));
+    MOE_CHECK_CUDA(cudaMemsetAsync(dw_gate, 0, wn, cs));
+    MOE_CHECK_CUDA(cudaMemsetAsync(dw_up, 0, wn, cs));
+    MOE_CHECK_CUDA(cudaMemsetAsync(dw_down, 0, wn, cs));
+    if (S > 0) {
+      const size_t sn = static_cast<size_t>(SI) * d * gsz;
+      MOE_CHECK_CUDA(cudaMemsetAsync(dws_gate, 0, sn, cs));
+      MOE_CHECK_CUDA(cudaMemsetAsync(dws_up, 0, sn, cs));
+      MOE_CHECK_CUDA(cudaMemsetAsync(dws_down, 0, sn, cs));
+    }
+    return MOE_OK;
+  }
+  int sms = 0;
+  st = device_setup(&sms);
+  if (st != MOE_OK) return st;
+  char* base = static_cast<char*>(ws);
+  int* ctr = reinterpret_cast<int*>(base + w.ctr);
+  int* offs = reinterpret_cast<int*>(base + w.offs);    // checked offsets
+  int* offpad = reinterpret_cast<int*>(base + w.offpad);
+  float* dz = reinterpret_cast<float*>(base + w.dz);
+  auto* X = reinterpret_cast<__nv_bfloat16*>(base + w.X);
+  auto* dY = reinterpret_cast<__nv_bfloat16*>(base + w.dY);
+  auto* dH = reinterpret_cast<__half*>(base + w.dH);
+  auto* H = reinterpret_cast<__nv_bfloat16*>(base + w.H);
+  auto* dA = reinterpret_cast<__nv_bfloat16*>(base + w.dA);
+  auto* dX = reinterpret_cast<__half*>(base + w.dX);
+  auto* dH_s = reinterpret_cast<__half*>(base + w.dH_s);
+  auto* H_s = reinterpret_cast<__nv_bfloat16*>(base + w.H_s);
+  auto* dA_s = reinterpret_cast<__nv_bfloat16*>(base + w.dA_s);
+  auto* dX_s = reinterpret_cast<__half*>(base + w.dX_s);
+  const long long A = static_cast<long long>(T) * K;
+  const long long R = w.A_pad;
+
+  // 1. checked and padded offsets; item counters
+  bwd_offpad_kernel<<<1, 256, 0, cs>>>(offsets, N, A, offs, offpad, ctr,
+                                       kBwdCounters);
+  MOE_CHECK_LAUNCH();
+  // 2. per-assignment operands and the gate gradient; zero padding rows
+  bwd_gather_kernel<<<T, 128, 0, cs>>>(
+      static_cast<const __nv_bfloat16*>(dh), static_cast<const __nv_bfloat16*>(u),
+      topk_idx, topk_gate, inv, offs, offpad,
+      static_cast<const __half*>(y_perm), d, K, N, A, R, dY, X, dz);
+  MOE_CHECK_LAUNCH();
+  bwd_zero_pad_kernel<<<N, 256, 0, cs>>>(offs, offpad, d, I, X, dY, H, dA,
+                                         dz);
+  MOE_CHECK_LAUNCH();
+
+  const long long tok_items_r = cdiv(A, 256) + N;   // chunk bound
+  const long long tok_items_s = S > 0 ? cdiv(T, 256) : 0;
+  CUtensorMap a_r, b_r, a_s, b_s;
+  BwdParams p{};
+  p.offpad = offpad;
+  p.offsets = offs;
+  p.n_groups = N;
+  p.shared_rows = S > 0 ? T : 0;
+  p.I = I;
+
+  // 3. Dgrad (down): dH = dY W_down, dH_s = dh Ws_down
+  if ((st = make_map(&a_r, w_down, static_cast<long long>(N) * d, I, 64)))
+    return st;
+  if ((st = make_map(&b_r, dY, R, d, kBoxRows))) return st;
+  if (S > 0) {
+    if ((st = make_map(&a_s, ws_down_packed, d, SI, 64))) return st;
+    if ((st = make_map(&b_s, dh, T, d, kBoxRows))) return st;
+  } else {
+    a_s = a_r;
+    b_s = b_r;
+  }
+  p.m_routed = I;  p.m_shared = SI;
+  p.k_routed = d;  p.k_shared = d;
+  p.out_r = dH;    p.ld_r = I;
+  p.out_s = dH_s;  p.ld_s = SI;
+  p.item_counter = ctr + 0;
+  if ((st = launch_bwd_gemm<kDgrad, 256, 4>(
+           a_r, b_r, a_s, b_s, p,
+           tok_items_r * (I / 128) + tok_items_s * (SI / 128), sms, cs)))
+    return st;
+
+  // 4. gate/up recomputed with the SwiGLU backward: H, dA (and shared)
+  if ((st = make_map(&a_r, w_gu_packed, 2LL * N * I, d, kGemmBM))) return st;
+  if ((st = make_map(&b_r, X, R, d, kBoxRows))) return st;
+  if (S > 0) {
+    if ((st = make_map(&a_s, ws_gu_packed, 2LL * SI, d, kGemmBM))) return st;
+    if ((st = make_map(&b_s, u, T, d, kBoxRows))) return st;
+  } else {
+    a_s = a_r;
+    b_s = b_r;
+  }
+  p.m_routed = 2 * I;  p.m_shared = 2 * SI;
+  p.k_routed = d;      p.k_shared = d;
+  p.dh_r = dH;         p.dh_s = dH_s;
+  p.out_r = H;         p.ld_r = I;
+  p.out_s = H_s;       p.ld_s = SI;
+  p.out2_r = dA;       p.ld2_r = 2LL * I;
+  p.out2_s = dA_s;     p.ld2_s = 2LL * SI;
+  p.item_counter = ctr + 1;
+  if ((st = launch_bwd_gemm<kRecomp, 256, 4>(
+           a_r, b_r, a_s, b_s, p,
+           tok_items_r * (2 * I / 128) + tok_items_s * (2 * SI / 128), sms,
+           cs)))
+    return st;
+
+  // 5. Dgrad (gate/up): dX = dA W_gu, dX_s = dA_s Ws_gu
+  if ((st = make_map(&a_r, w_gu_packed, 2LL * N * I, d, 64))) return st;
+  if ((st = make_map(&b_r, dA, R, 2LL * I, kBoxRows))) return st;
+  if (S > 0) {
+    if ((st = make_map(&a_s, ws_gu_packed, 2LL * SI, d, 64))) return st;
+    if ((st = make_map(&b_s, dA_s, T, 2LL * SI, kBoxRows))) return st;
+  } else {
+    a_s = a_r;
+    b_s = b_r;
+  }
+  p.m_routed = d;      p.m_shared = d;
+  p.k_routed = 2 * I;  p.k_shared = 2 * SI;
+  p.out_r = dX;        p.ld_r = d;
+  p.out_s = dX_s;      p.ld_s = d;
+  p.item_counter = ctr + 2;
+  if ((st = launch_bwd_gemm<kDgrad, 256, 4>(
+           a_r, b_r, a_s, b_s, p,
+           tok_items_r * (d / 128) + tok_items_s * (d / 128), sms, cs)))
+    return st;
+
+  // 6. Wgrad (gate/up): dW_gate / dW_up = dA^T X; shared dA_s^T u
+  const bool gb = grad_dtype == MOE_BF16;
+  if ((st = make_map(&a_r, dA, R, 2LL * I, 64))) return st;
+  if ((st = make_map(&b_r, X, R, d, 64))) return st;
+  if (S > 0) {
+    if ((st = make_map(&a_s, dA_s, T, 2LL * SI, 64))) return st;
+    if ((st = make_map(&b_s, u, T, d, 64))) return st;
+  } else {
+    a_s = a_r;
+    b_s = b_r;
+  }
+  p.m_routed = 2 * I;  p.m_shared = 2 * SI;
+  p.n_routed = d;      p.n_shared = d;
+  p.out_r = dw_gate;   p.out2_r = dw_up;   p.ld_r = d;
+  p.out_s = dws_gate;  p.out2_s = dws_up;  p.ld_s = d;
+  p.wgrad_gu = 1;
+  p.out_bf16 = gb ? 1 : 0;
+  p.item_counter = ctr + 3;
+  {
+    const bool b256 = d % 256 == 0;
+    const int bn = b256 ? 256 : 128;
+    const long long items =
+        static_cast<long long>(N) * (2 * I / 128) * cdiv(d, bn) +
+        (S > 0 ? static_cast<long long>(2 * SI / 128) * cdiv(d, bn) : 0);
+    st = b256 ? launch_bwd_gemm<kWgrad, 256, 4>(a_r, b_r, a_s, b_s, p, items,
+                                                sms, cs)
+              : launch_bwd_gemm<kWgrad, 128, 6>(a_r, b_r, a_s, b_s, p, items,
+                                                sms, cs);
+    if (st != MOE_OK) return st;
+  }
+
+  // 7. Wgrad (down): dW_down = dY^T H; shared dh^T H_s
+  if ((st = make_map(&a_r, dY, R, d, 64))) return st;
+  if ((st = make_map(&b_r, H, R, I, 64))) return st;
+  if (S > 0) {
+    if ((st = make_map(&a_s, dh, T, d, 64))) return st;
+    if ((st = make_map(&b_s, H_s, T, SI, 64))) return st;
+  } else {
+    a_s = a_r;
+    b_s = b_r;
+  }
+  p.m_routed = d;   p.m_shared = d;
+  p.n_routed = I;   p.n_shared = SI;
+  p.out_r = dw_down;   p.out2_r = nullptr;  p.ld_r = I;
+  p.out_s = dws_down;  p.out2_s = nullptr;  p.ld_s = I;
+  p.wgrad_gu = 0;
+  p.item_counter = ctr + 4;
+  {
+    const bool b256 = I % 256 == 0 && SI % 256 == 0;
+    const int bn = b256 ? 256 : 128;
+    const long long items =
+        static_cast<long long>(N) * (d / 128) * cdiv(I, bn) +
+        (S > 0 ? static_cast<long long>(d / 128) * cdiv(SI, bn) : 0);
+    st = b256 ? launch_bwd_gemm<kWgrad, 256, 4>(a_r, b_r, a_s, b_s, p, items,
+                                                sms, cs)
+              : launch_bwd_gemm<kWgrad, 128, 6>(a_r, b_r, a_s, b_s, p, items,
+                                                sms, cs);
+    if (st != MOE_OK) return st;
+  }
+
+  // 8. centroid gradient; 9. input gradient
+  bwd_centroid_grad_kernel<<<dim3(N, static_cast<unsigned>(cdiv(d, 1024))),
+                             128, 0, cs>>>(offs, offpad, dz, X, d, dE);
+  MOE_CHECK_LAUNCH();
+  bwd_input_grad_kernel<<<T, 128, 0, cs>>>(
+      static_cast<const __nv_bfloat16*>(dh), S > 0 ? dX_s : nullptr, dX,
+      static_cast<const __nv_bfloat16*>(centroids), dz, topk_idx, inv, offs,
+      offpad, d, K, N, A, du);
+  MOE_CHECK_LAUNCH();
+  return MOE_OK;
 }
 
 }  // extern "C"

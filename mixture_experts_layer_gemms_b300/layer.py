@@ -95,6 +95,7 @@ class MoELayer:
                               ws_down, self.w_gu, self.ws_gu, self.ws_down,
                               stream)
         self._bufs: Dict[int, Buffers] = {}
+        self._grads: Dict = {}
         self.overlap_shared = bool(overlap_shared)
         self._side = None
 
@@ -188,6 +189,50 @@ class MoELayer:
         return h
 
     __call__ = forward
+
+    def backward(self, u: torch.Tensor, dh: torch.Tensor,
+                 grad_dtype: torch.dtype = torch.float32, stream=None):
+        """Gradients of the layer for the upstream gradient dh [T, d] (bf16),
+        after a forward on the same u (its routing, slots and expert outputs
+        are reused).  Returns a dict: du [T, d] and dE [N, d] fp32; dw_gate,
+        dw_up [N, I, d], dw_down [N, d, I] and, with shared experts, dws_gate,
+        dws_up [S, I, d], dws_down [S, d, I] as grad_dtype.  The tensors are
+        this layer's buffers for (T, grad_dtype), overwritten by the next
+        call.  bf16 layers only; the bias gets no gradient (it only selects).
+        """
+        if self.code != torch.bfloat16:
+            raise ValueError("backward: bf16 layers only")
+        T = u.shape[0]
+        if T not in self._bufs:
+            raise ValueError("backward: run the forward on this batch first")
+        b = self._bufs[T]
+        sh = self.shape(T)
+        key = (T, grad_dtype)
+        g = self._grads.get(key)
+        if g is None:
+            dev, N, d, I, S = self.E.device, self.N, self.d, self.I, self.S
+            f32 = dict(dtype=torch.float32, device=dev)
+            gd = dict(dtype=grad_dtype, device=dev)
+            g = dict(du=torch.empty((T, d), **f32),
+                     dE=torch.empty((N, d), **f32),
+                     dw_gate=torch.empty((N, I, d), **gd),
+                     dw_up=torch.empty((N, I, d), **gd),
+                     dw_down=torch.empty((N, d, I), **gd))
+            if S:
+                g.update(dws_gate=torch.empty((S, I, d), **gd),
+                         dws_up=torch.empty((S, I, d), **gd),
+                         dws_down=torch.empty((S, d, I), **gd))
+            ws = torch.empty((_lib.backward_workspace_size(sh) + 256,),
+                             dtype=torch.uint8, device=dev)
+            off = (-ws.data_ptr()) % 256
+            g["_ws"] = ws[off:]
+            self._grads[key] = g
+        _lib.backward(sh, dh, u, self.E, b.topk_idx, b.topk_gate, b.offsets,
+                      b.inv, b.y_perm, self.w_gu, self.w_down, self.ws_gu,
+                      self.ws_down, g["du"], g["dE"], g["dw_gate"],
+                      g["dw_up"], g["dw_down"], g.get("dws_gate"),
+                      g.get("dws_up"), g.get("dws_down"), g["_ws"], stream)
+        return {k: v for k, v in g.items() if not k.startswith("_")}
 
     def forward_host(self, u_host, h_host, update_bias: bool = False,
                      gamma: float = 1e-3) -> None:

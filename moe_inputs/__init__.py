@@ -44,6 +44,7 @@ from typing import Dict, Optional
 import torch
 
 __all__ = ["MoEConfig", "CONFIGS", "get_config", "generate", "step_tokens",
+           "upstream_grad",
            "torch_dtype"]
 
 
@@ -168,6 +169,15 @@ def step_tokens(cfg: MoEConfig, step: int, device="cpu") -> torch.Tensor:
     dev = torch.device(device)
     gen = torch.Generator(device=dev)
     gen.manual_seed(cfg.seed * 1_000_003 + step + 1)
+    return _normal(gen, (cfg.T, cfg.d), 1.0, torch_dtype(cfg), dev)
+
+
+def upstream_grad(cfg: MoEConfig, device="cpu") -> torch.Tensor:
+    """Synthetic upstream gradient dh[T, d] ~ N(0, 1) for the backward pass,
+    in the layer's dtype, from its own seeded stream."""
+    dev = torch.device(device)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(cfg.seed * 1_000_003 + 999_983)
     return _normal(gen, (cfg.T, cfg.d), 1.0, torch_dtype(cfg), dev)
 
 

@@ -192,3 +192,56 @@ def test_expert_ffn_part_validation(moe, dtype_name, part, code, detail):
                                      None)
     assert st == code
     assert detail in moe.LIB.moe_last_error_detail()
+
+
+def _bwd_call(moe, sh, ptrs=None, grad=1, ws=None, nbytes=1 << 40):
+    P = ctypes.c_void_p
+    p = [P(256 * (i + 1)) for i in range(20)] if ptrs is None else ptrs
+    return moe.LIB.moe_backward(ctypes.byref(sh), *p, grad,
+                                P(1 << 20) if ws is None else ws, nbytes, None)
+
+
+@pytest.mark.parametrize("over,code,detail", [
+    (dict(dtype=0), 2, b"bf16 layers only"),      # fp32 layer
+    (dict(dtype=2, d_ff=256), 2, b"bf16 layers only"),   # e4m3 layer
+    (dict(dtype=1, d_ff=192), 2, b"multiple of 128"),
+])
+def test_backward_shape_checks(moe, over, code, detail):
+    sh = _shape(moe, **over)
+    n = ctypes.c_size_t()
+    assert moe.LIB.moe_backward_workspace_size(ctypes.byref(sh),
+                                               ctypes.byref(n)) == code
+    assert _bwd_call(moe, sh) == code
+    assert detail in moe.LIB.moe_last_error_detail()
+
+
+def test_backward_argument_checks(moe):
+    """Every check that needs no GPU: grad dtype, pointers, alignment and
+    the workspace, each refused before anything is launched."""
+    sh = _shape(moe, dtype=moe.MOE_BF16)
+    n = ctypes.c_size_t()
+    assert moe.LIB.moe_backward_workspace_size(ctypes.byref(sh),
+                                               ctypes.byref(n)) == 0
+    # padded rows: at most T*K + 63*N, in 64-row blocks
+    A_pad = (64 * 4 + 63 * 16 + 63) // 64 * 64
+    assert n.value >= A_pad * 256 * 2 * 4 and n.value % 256 == 0
+    P = ctypes.c_void_p
+    assert _bwd_call(moe, sh, grad=2) == 1                   # e4m3 grads
+    for i in range(20):
+        ptrs = [P(256 * (k + 1)) for k in range(20)]
+        ptrs[i] = None
+        assert _bwd_call(moe, sh, ptrs) == 1, i
+        assert b"NULL" in moe.LIB.moe_last_error_detail()
+    ptrs = [P(256 * (k + 1)) for k in range(20)]
+    ptrs[0] = P(258)                                          # dh misaligned
+    assert _bwd_call(moe, sh, ptrs) == 1
+    assert b"aligned" in moe.LIB.moe_last_error_detail()
+    assert _bwd_call(moe, sh, nbytes=n.value - 1) == 3       # too small
+    assert _bwd_call(moe, sh, ws=P(1 << 20 | 8), nbytes=n.value) == 1
+    # without shared experts their weights and gradients may be NULL, so
+    # the first refusal is the workspace's
+    sh0 = _shape(moe, dtype=moe.MOE_BF16, n_shared=0)
+    ptrs = [P(256 * (k + 1)) for k in range(20)]
+    for i in (10, 11, 17, 18, 19):
+        ptrs[i] = None
+    assert _bwd_call(moe, sh0, ptrs, nbytes=0) == 3

@@ -21,6 +21,17 @@ from moe_inputs import as_f64, generate
 NEAR_TIE = 1e-5
 MAX_ABS = 2e-2
 REL_FRO = 5e-3
+# gradients of the backward pass: the relative bar unchanged, the absolute
+# one scaled to the tensor's largest entry
+GRAD_REL_FRO = 5e-3
+GRAD_MAX_ABS_FRAC = 1e-2
+
+
+def grad_max_abs(ref) -> float:
+    """max|err| allowed for a gradient tensor: max(2e-2, 1% of max|ref|)."""
+    ref = np.asarray(ref, dtype=np.float64)
+    top = float(np.abs(ref).max()) if ref.size else 0.0
+    return max(MAX_ABS, GRAD_MAX_ABS_FRAC * top)
 
 
 def half_ulp_bf16(x):

@@ -2,13 +2,15 @@
 (oracle/backward.py), on the GPU's own selection (checked first against the
 oracle's routing rules).
 
-Tolerance.  The pages fix no bar for gradients; the forward's bar (relative
-Frobenius 5e-3, max-abs 2e-2 for bf16 operands with fp32 accumulation) is
-applied with the absolute part scaled by the gradient's own RMS:
-max|err| <= 2e-2 * max(1, rms(ref)).  A gradient entry is a sum over the
-tokens of an expert (or all T for the shared experts) of products of
-bf16-rounded operands, so its rounding error grows with the entry's scale,
-not with a fixed unit.
+Tolerance.  The pages fix no bar for gradients.  The relative part of the
+forward's bar carries over unchanged: relative Frobenius error <= 5e-3.  The
+absolute part is scaled to the tensor: max|err| <= max(2e-2, 1e-2 *
+max|ref|).  A gradient entry is a sum over an expert's tokens (all T for the
+shared experts) of products of bf16-rounded operands (dY = g dh, dA, H;
+unit roundoff 2^-9), so its rounding error grows with the entries' scale.
+A model of this path's rounding points on the CPU
+(tests/test_backward_tolerance.py) stays below 0.5% of max|ref| at these
+sizes; the bar is 1% (about 2.5 bf16 ulps at the largest entry).
 Requires a B300 (sm_103a)."""
 import numpy as np
 import pytest
@@ -17,20 +19,17 @@ import torch
 import oracle.backward as ob
 import oracle.moe as om
 from moe_inputs import as_f64, generate, get_config, upstream_grad
-from parity_utils import check_routing, errors, make_inputs
+from parity_utils import (GRAD_REL_FRO as REL_FRO, check_routing, errors,
+                          grad_max_abs, make_inputs)
 
 pytestmark = pytest.mark.gpu
-
-REL_FRO = 5e-3
-MAX_ABS = 2e-2
 
 
 def grad_close(got, ref, what):
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     e = errors(got, ref)
-    rms = float(np.sqrt(np.mean(ref ** 2))) if ref.size else 0.0
-    lim = MAX_ABS * max(1.0, rms)
+    lim = grad_max_abs(ref)
     assert e["rel_fro"] <= REL_FRO and e["max_abs"] <= lim, (what, e, lim)
     return e
 

@@ -29,7 +29,7 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-from moe_inputs import as_f64, generate, get_config  # noqa: E402
+from moe_inputs import as_f64, generate, get_config, upstream_grad  # noqa: E402
 
 METRIC = "MoE-layer tokens/s at V3 shape"
 # DRAM bytes (read + write) of one expert-FFN call (the grouped GEMM's two
@@ -302,6 +302,58 @@ def run_skew(args, cfg, moe, dev, ws, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def time_backward(args, cfg, layer, u, dev, ws, peaks):
+    """The layer backward (moe_backward: Dgrad and Wgrad GEMMs, gate and
+    centroid gradients) after a forward on the same batch, timed with CUDA
+    events on the launching stream; and a training step (forward + backward)
+    timed over the same number of steps.  Weight gradients in bf16."""
+    import mixture_experts_layer_gemms_b300 as moe
+    dh = upstream_grad(cfg, dev)
+    stream = torch.cuda.current_stream()
+    gd = torch.bfloat16
+    layer.overlap_shared = False
+    for _ in range(max(3, args.warmup)):
+        layer(u)
+        layer.backward(u, dh, grad_dtype=gd)
+    torch.cuda.synchronize()
+    moe.get_device_error()
+    n_launch = moe.last_launch_count()
+    steps = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)]
+          for _ in range(steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(steps):
+        ev[i][0].record(stream)
+        layer(u)
+        ev[i][1].record(stream)
+        layer.backward(u, dh, grad_dtype=gd)
+        ev[i][2].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    moe.get_device_error()
+    bw_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    train_ms = max_over_ranks(t0.elapsed_time(t1), dev) / steps
+    rows = cfg.T * cfg.top_k + cfg.n_shared * cfg.T
+    # algorithmic: twice the expert FFNs' forward FLOPs (Dgrad + Wgrad);
+    # executed adds the recomputed gate/up GEMM
+    alg = 12.0 * cfg.d * cfg.d_ff * rows
+    exe = 16.0 * cfg.d * cfg.d_ff * rows
+    pk = peaks["bf16_tflops"]
+    return {"ms_per_call": bw_ms,
+            "train_step_tokens_per_s": ws * cfg.T / (train_ms / 1e3),
+            "train_step_ms": train_ms,
+            "algorithmic_tflops": alg / (bw_ms / 1e3) / 1e12,
+            "executed_tflops": exe / (bw_ms / 1e3) / 1e12,
+            "executed_frac_of_bf16_peak": exe / (bw_ms / 1e3) / 1e12 / pk,
+            "grad_dtype": "bf16", "gpu_launches_per_call": n_launch,
+            "note": "moe_backward after a forward of the same batch: "
+                    "gather, Dgrad (down, gate/up), gate/up recompute with "
+                    "the SwiGLU backward, Wgrad (gate/up, down), centroid "
+                    "and input gradients"}
+
+
 def run_ours(args, cfg):
     ws, rank, local = _dist()
     torch.cuda.set_device(local)
@@ -469,6 +521,10 @@ def run_ours(args, cfg):
     moe.get_device_error()
 
     peaks = _peaks()
+    bwd = None
+    if (not args.no_backward and cfg.quant is None and cfg.dtype == "bf16"
+            and cfg.d_ff % 128 == 0):
+        bwd = time_backward(args, cfg, layer, u, dev, ws, peaks)
     fp8 = cfg.quant == "fp8"
     # e4m3 contractions: the measured bf16 peak times the nominal dense
     # e4m3 : bf16 ratio (4.5 : 2.25 PFLOP/s)
@@ -546,6 +602,8 @@ def run_ours(args, cfg):
                     "how": "MoELayer(overlap_shared=True).forward_host: "
                            "pinned-host batches, copies on their own streams "
                            "overlapping the neighbouring steps' compute"}}
+    if bwd is not None:
+        line["backward"] = bwd
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, t, budget_s=args.ref_budget)
     if rank == 0:
@@ -563,6 +621,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="v3_prefill")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-backward", action="store_true",
+                    help="skip the backward-pass block of the line")
     ap.add_argument("--overlap-shared", action="store_true",
                     help="shared experts on a side stream in the timed step")
     ap.add_argument("--ref-budget", type=float, default=15.0,

@@ -33,6 +33,9 @@ namespace moe {
 
 enum BwdKind : int { kDgrad = 0, kRecomp = 1, kWgrad = 2 };
 constexpr int kPadRows = 64;   // routed groups are padded to this many rows
+// epilogue staging: four warps x 32 x 33 floats (the Wgrad transpose; the
+// Recomp exchange uses the first 4 x 32 x 17)
+constexpr int kBwdStgBytes = 4 * 32 * 33 * 4;
 
 // Shared-memory descriptor of an MN-major operand that TMA wrote as boxes of
 // {64 MN elements (128 B), 64 K rows} with 128-byte swizzle.  Eight K rows
@@ -84,7 +87,7 @@ struct BwdSmem {
   static constexpr int a_off = 0;
   static constexpr int b_off = a_off + STAGES * a_bytes;
   static constexpr int stg_off = b_off + STAGES * b_bytes;
-  static constexpr int stg_bytes = 4 * 32 * 17 * 4;
+  static constexpr int stg_bytes = kBwdStgBytes;
   static constexpr int bar_off = stg_off + stg_bytes;
   static constexpr int n_bars = 2 * STAGES + 5 + 2 * kSchedDepth;
   static constexpr int misc_off = bar_off + n_bars * 8;
@@ -106,7 +109,9 @@ struct BTile {
   int n_valid;   // tokens kinds: tokens; Wgrad: columns
   int n_mma;     // MMA N
   int k_row0;    // first K row of the MN-major operands (Dgrad A, Wgrad A/B)
-  int nk;        // K blocks of 64
+  int nk;        // K blocks (64 rows; 128 on CTA pairs)
+  int krows;     // CTA-pair Wgrad: K rows to multiply (the last block may
+                 // hold only 64 of its 128)
 };
 
 // Item tables in shared memory: offpad, cnt and (tokens kinds) the prefix
@@ -251,20 +256,62 @@ __device__ __forceinline__ void bwd_ep_recomp(
   }
 }
 
-// kWgrad: row-major store of one 128 x BN tile, columns n0 .. n0+n_valid
-// of this thread's output row `dst_row` (its column 0).  For the shared down
-// gradient the column picks the expert (`col_split` = I: column c goes to
-// expert c / I, at dst_row + (c / I) * s_stride + c % I); else column c is at
-// dst_row + c.
-template <int BN>
-__device__ __forceinline__ void bwd_ep_wgrad(uint32_t taddr, int n0,
-                                             int n_valid, bool zero,
-                                             char* dst_row, int col_split,
-                                             long long s_stride, bool bf16) {
+// kWgrad output row m of a group's M side (gate/up: the packed row index,
+// 128-row blocks of 64 gate then 64 up rows; down: the row of W_down): the
+// address of its column 0, the byte stride to row m + 1 (rows of one warp
+// are consecutive), and the column mapping of the shared down gradient
+// (col_split = I: column c of the [d, S*I] tile is expert c / I's column
+// c % I, s_stride elements apart).
+struct WgradRow {
+  char* p;
+  long long row_bytes;
+  int col_split;
+  long long s_stride;
+};
+__device__ __forceinline__ WgradRow wgrad_row(const BwdParams& p, bool shared,
+                                              int e, int m) {
+  const int esz = p.out_bf16 ? 2 : 4;
+  WgradRow w;
+  w.col_split = 0;
+  w.s_stride = 0;
+  if (p.wgrad_gu) {
+    const int within = m & 127;
+    const long long irow = static_cast<long long>(m >> 7) * 64 + (within & 63);
+    const long long ld = shared ? p.ld_s : p.ld_r;   // = d
+    const long long base = shared ? 0 : static_cast<long long>(e) * p.I;
+    char* g = static_cast<char*>(within < 64 ? (shared ? p.out_s : p.out_r)
+                                             : (shared ? p.out2_s : p.out2_r));
+    w.p = g + (base + irow) * ld * esz;
+    w.row_bytes = ld * esz;
+  } else {
+    const long long ld = shared ? p.ld_s : p.ld_r;   // = I
+    char* g = static_cast<char*>(shared ? p.out_s : p.out_r);
+    if (shared) {       // [S][d][I]
+      w.col_split = p.I;
+      w.s_stride = static_cast<long long>(p.m_shared) * p.I;
+      w.p = g + static_cast<long long>(m) * ld * esz;
+    } else {            // [N][d][I]
+      w.p = g + (static_cast<long long>(e) * p.m_routed + m) * ld * esz;
+    }
+    w.row_bytes = ld * esz;
+  }
+  return w;
+}
+
+// kWgrad epilogue of one warp: its 32 accumulator rows (TMEM lanes) x
+// columns n0 .. n0 + n_valid of the tile, row-major.  Each 32-column chunk
+// goes through a 32 x 33 float block in shared memory so that every store
+// instruction writes whole column runs of one row (fp32: 128 B) or of two
+// rows (bf16: 2 x 64 B).  `zero`: no accumulation happened (the group has
+// no rows); zeros are stored.
+__device__ __forceinline__ void bwd_ep_wgrad_warp(uint32_t taddr, int n0,
+                                                  int n_valid, int bn,
+                                                  bool zero, const WgradRow& w,
+                                                  bool bf16, float* st,
+                                                  int lane) {
   const int esz = bf16 ? 2 : 4;
 #pragma unroll 1
-  for (int c0 = 0; c0 < BN; c0 += 32) {
-    if (c0 >= n_valid) break;
+  for (int c0 = 0; c0 < bn && c0 < n_valid; c0 += 32) {
     uint32_t r[32];
     if (!zero) {
       tmem_ld32(taddr + c0, r);
@@ -273,27 +320,28 @@ __device__ __forceinline__ void bwd_ep_wgrad(uint32_t taddr, int n0,
 #pragma unroll
       for (int j = 0; j < 32; ++j) r[j] = 0u;
     }
+#pragma unroll
+    for (int j = 0; j < 32; ++j) st[lane * 33 + j] = __uint_as_float(r[j]);
+    __syncwarp();
     const long long c = n0 + c0;
     const long long off =
-        col_split > 0 ? (c / col_split) * s_stride + c % col_split : c;
-    char* p = dst_row + off * esz;
+        w.col_split > 0 ? (c / w.col_split) * w.s_stride + c % w.col_split : c;
+    char* base = w.p + off * esz;
     if (bf16) {
-#pragma unroll
-      for (int j = 0; j < 32; j += 8) {
-        uint4 v;
-        v.x = pack_bf16x2(__uint_as_float(r[j]), __uint_as_float(r[j + 1]));
-        v.y = pack_bf16x2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
-        v.z = pack_bf16x2(__uint_as_float(r[j + 4]), __uint_as_float(r[j + 5]));
-        v.w = pack_bf16x2(__uint_as_float(r[j + 6]), __uint_as_float(r[j + 7]));
-        *reinterpret_cast<uint4*>(p + j * 2) = v;
+      const int half = lane >> 4, cc = (lane & 15) * 2;
+#pragma unroll 4
+      for (int rr = 0; rr < 32; rr += 2) {
+        const int row = rr + half;
+        *reinterpret_cast<uint32_t*>(base + row * w.row_bytes + cc * 2) =
+            pack_bf16x2(st[row * 33 + cc], st[row * 33 + cc + 1]);
       }
     } else {
-#pragma unroll
-      for (int j = 0; j < 32; j += 4)
-        *reinterpret_cast<float4*>(p + j * 4) =
-            make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
-                        __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+#pragma unroll 4
+      for (int rr = 0; rr < 32; ++rr)
+        *reinterpret_cast<float*>(base + rr * w.row_bytes + lane * 4) =
+            st[rr * 33 + lane];
     }
+    __syncwarp();
   }
 }
 
@@ -607,35 +655,10 @@ bwd_gemm_kernel(const __grid_constant__ CUtensorMap tmA_r,
                                                            : p.out2_r),
                       t.shared ? p.ld2_s : p.ld2_r, stg, q, lane);
       } else {
-        const int esz = p.out_bf16 ? 2 : 4;
-        char* dst = nullptr;
-        int col_split = 0;
-        long long s_stride = 0;
-        if (p.wgrad_gu) {
-          // packed row m0 + row: gate (row < 64) or up row wt*64 + row % 64
-          // of the group's (concatenated) intermediate index; [.., I, d]
-          const long long irow = static_cast<long long>(t.wt) * 64 + (row & 63);
-          const long long ld = t.shared ? p.ld_s : p.ld_r;   // = d
-          const long long base =
-              t.shared ? 0 : static_cast<long long>(t.e) * p.I;
-          char* gbase = static_cast<char*>(
-              row < 64 ? (t.shared ? p.out_s : p.out_r)
-                       : (t.shared ? p.out2_s : p.out2_r));
-          dst = gbase + (base + irow) * ld * esz;
-        } else {
-          const long long ld = t.shared ? p.ld_s : p.ld_r;   // = I
-          char* gbase = static_cast<char*>(t.shared ? p.out_s : p.out_r);
-          if (t.shared) {   // [S][d][I]: column c -> expert c / I
-            col_split = p.I;
-            s_stride = static_cast<long long>(p.m_shared) * p.I;
-            dst = gbase + static_cast<long long>(t.m0 + row) * ld * esz;
-          } else {          // [N][d][I]
-            dst = gbase + (static_cast<long long>(t.e) * p.m_routed + t.m0 +
-                           row) * ld * esz;
-          }
-        }
-        bwd_ep_wgrad<BN>(ta, t.n0, t.n_valid, t.nk == 0, dst, col_split,
-                         s_stride, p.out_bf16 != 0);
+        // this warp's rows t.m0 + q*32 .. +31
+        const WgradRow w = wgrad_row(p, t.shared != 0, t.e, t.m0 + q * 32);
+        bwd_ep_wgrad_warp(ta, t.n0, t.n_valid, BN, t.nk == 0, w,
+                          p.out_bf16 != 0, stg + q * 32 * 33, lane);
       }
       tc_fence_before();
       mbar_arrive(bar_tempty + 8 * acc);

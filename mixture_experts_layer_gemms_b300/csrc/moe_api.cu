@@ -18,6 +18,7 @@
 #include "gemm_fp8.cuh"
 #include "bwd.cuh"
 #include "gemm_bwd.cuh"
+#include "gemm_bwd2sm.cuh"
 #include "moe_b300.h"
 
 using namespace moe;
@@ -60,6 +61,7 @@ struct DeviceInfo {
   bool init = false;
   int sm_count = 0;
   int pair_clusters = 0;   // co-resident clusters of the CTA-pair GEMM
+  int bwd_pair_clusters = 0;   // same for the backward's CTA-pair GEMM
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -121,10 +123,28 @@ moe_status device_setup(int* sm_count) {
     MOE_CHECK_CUDA(cudaOccupancyMaxActiveClusters(
         &clusters, grouped_gemm_pair_kernel, &cfg));
     di.pair_clusters = clusters;
+    MOE_CHECK_CUDA(allow_smem(bwd_gemm_pair_kernel<kDgrad>,
+                              BwdPairSmem::alloc));
+    MOE_CHECK_CUDA(allow_smem(bwd_gemm_pair_kernel<kRecomp>,
+                              BwdPairSmem::alloc));
+    MOE_CHECK_CUDA(allow_smem(bwd_gemm_pair_kernel<kWgrad>,
+                              BwdPairSmem::alloc));
+    cfg.dynamicSmemBytes = BwdPairSmem::alloc;
+    clusters = 0;
+    MOE_CHECK_CUDA(cudaOccupancyMaxActiveClusters(
+        &clusters, bwd_gemm_pair_kernel<kWgrad>, &cfg));
+    di.bwd_pair_clusters = clusters;
     di.init = true;
   }
   *sm_count = di.sm_count;
   return MOE_OK;
+}
+
+int bwd_pair_clusters() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return 0;
+  return g_dev[dev].bwd_pair_clusters;
 }
 
 int pair_clusters() {
@@ -1334,6 +1354,62 @@ moe_status launch_bwd_gemm(const CUtensorMap& a_r, const CUtensorMap& b_r,
   return MOE_OK;
 }
 
+// 3-D maps of one backward pair launch: every operand as {64, rows,
+// cols/64} with {64, box, 2}-element boxes (make_map3).  The A operands use
+// 128-row boxes whether K-major (weight rows) or MN-major (K rows); the B
+// operand gets 32/64/128-row boxes when it is the token operand, else only
+// the 128-row one.
+struct Op {
+  const void* p;
+  long long rows, cols;
+};
+moe_status bwd_pair_maps(Op a_r, Op b_r, Op a_s, Op b_s, bool shared,
+                         bool tokens, BwdPairMaps& m) {
+  moe_status st;
+  if ((st = make_map3(&m.a_r, a_r.p, a_r.rows, a_r.cols, 128, 2))) return st;
+  if ((st = make_map3(&m.b_r128, b_r.p, b_r.rows, b_r.cols, 128, 2)))
+    return st;
+  if (tokens) {
+    if ((st = make_map3(&m.b_r32, b_r.p, b_r.rows, b_r.cols, 32, 2))) return st;
+    if ((st = make_map3(&m.b_r64, b_r.p, b_r.rows, b_r.cols, 64, 2))) return st;
+  } else {
+    m.b_r32 = m.b_r64 = m.b_r128;
+  }
+  if (shared) {
+    if ((st = make_map3(&m.a_s, a_s.p, a_s.rows, a_s.cols, 128, 2))) return st;
+    if ((st = make_map3(&m.b_s128, b_s.p, b_s.rows, b_s.cols, 128, 2)))
+      return st;
+    if (tokens) {
+      if ((st = make_map3(&m.b_s32, b_s.p, b_s.rows, b_s.cols, 32, 2)))
+        return st;
+      if ((st = make_map3(&m.b_s64, b_s.p, b_s.rows, b_s.cols, 64, 2)))
+        return st;
+    } else {
+      m.b_s32 = m.b_s64 = m.b_s128;
+    }
+  } else {
+    m.a_s = m.a_r;
+    m.b_s32 = m.b_r32;
+    m.b_s64 = m.b_r64;
+    m.b_s128 = m.b_r128;
+  }
+  return MOE_OK;
+}
+
+template <int KIND>
+moe_status launch_bwd_pair(const BwdPairMaps& m, const BwdParams& p,
+                           long long max_items, cudaStream_t cs) {
+  if (max_items <= 0) return MOE_OK;
+  const long long clusters = bwd_pair_clusters();
+  if (clusters <= 0)
+    return fail(MOE_ERR_CUDA, "backward CTA-pair GEMM cannot be resident");
+  const long long n = max_items < clusters ? max_items : clusters;
+  bwd_gemm_pair_kernel<KIND>
+      <<<static_cast<int>(2 * n), 192, BwdPairSmem::alloc, cs>>>(m, p);
+  MOE_CHECK_LAUNCH();
+  return MOE_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -1458,129 +1534,213 @@ moe_status moe_backward(const moe_shape* s, const void* dh, const void* u,
   p.shared_rows = S > 0 ? T : 0;
   p.I = I;
 
-  // 3. Dgrad (down): dH = dY W_down, dH_s = dh Ws_down
-  if ((st = make_map(&a_r, w_down, static_cast<long long>(N) * d, I, 64)))
-    return st;
-  if ((st = make_map(&b_r, dY, R, d, kBoxRows))) return st;
-  if (S > 0) {
-    if ((st = make_map(&a_s, ws_down_packed, d, SI, 64))) return st;
-    if ((st = make_map(&b_s, dh, T, d, kBoxRows))) return st;
+  // CTA pairs (256-row M tiles) when every M and N side splits into 256s
+  const bool pair = d % 256 == 0 && I % 256 == 0;
+  if (pair) {
+    const bool sh = S > 0;
+    const long long ti_r = cdiv(A, 256) + N;           // chunk bound
+    const long long ti_s = sh ? cdiv(T, 256) : 0;
+    const long long NI = static_cast<long long>(N) * I;
+    BwdPairMaps m;
+    // 3. Dgrad (down): dH = dY W_down, dH_s = dh Ws_down
+    if ((st = bwd_pair_maps({w_down, static_cast<long long>(N) * d, I},
+                            {dY, R, d}, {ws_down_packed, d, SI}, {dh, T, d},
+                            sh, true, m)))
+      return st;
+    p.m_routed = I;  p.m_shared = SI;
+    p.k_routed = d;  p.k_shared = d;
+    p.out_r = dH;    p.ld_r = I;
+    p.out_s = dH_s;  p.ld_s = SI;
+    p.item_counter = ctr + 0;
+    if ((st = launch_bwd_pair<kDgrad>(m, p, ti_r * (I / 256) +
+                                                ti_s * (SI / 256), cs)))
+      return st;
+    // 4. gate/up recomputed with the SwiGLU backward: H, dA
+    if ((st = bwd_pair_maps({w_gu_packed, 2 * NI, d}, {X, R, d},
+                            {ws_gu_packed, 2LL * SI, d}, {u, T, d}, sh, true,
+                            m)))
+      return st;
+    p.m_routed = 2 * I;  p.m_shared = 2 * SI;
+    p.k_routed = d;      p.k_shared = d;
+    p.dh_r = dH;         p.dh_s = dH_s;
+    p.out_r = H;         p.ld_r = I;
+    p.out_s = H_s;       p.ld_s = SI;
+    p.out2_r = dA;       p.ld2_r = 2LL * I;
+    p.out2_s = dA_s;     p.ld2_s = 2LL * SI;
+    p.item_counter = ctr + 1;
+    if ((st = launch_bwd_pair<kRecomp>(m, p, ti_r * (2 * I / 256) +
+                                                 ti_s * (2 * SI / 256), cs)))
+      return st;
+    // 5. Dgrad (gate/up): dX = dA W_gu, dX_s = dA_s Ws_gu
+    if ((st = bwd_pair_maps({w_gu_packed, 2 * NI, d}, {dA, R, 2LL * I},
+                            {ws_gu_packed, 2LL * SI, d}, {dA_s, T, 2LL * SI},
+                            sh, true, m)))
+      return st;
+    p.m_routed = d;      p.m_shared = d;
+    p.k_routed = 2 * I;  p.k_shared = 2 * SI;
+    p.out_r = dX;        p.ld_r = d;
+    p.out_s = dX_s;      p.ld_s = d;
+    p.item_counter = ctr + 2;
+    if ((st = launch_bwd_pair<kDgrad>(m, p, (ti_r + ti_s) * (d / 256), cs)))
+      return st;
+    // 6. Wgrad (gate/up): dW_gate / dW_up = dA^T X; shared dA_s^T u
+    if ((st = bwd_pair_maps({dA, R, 2LL * I}, {X, R, d},
+                            {dA_s, T, 2LL * SI}, {u, T, d}, sh, false, m)))
+      return st;
+    p.m_routed = 2 * I;  p.m_shared = 2 * SI;
+    p.n_routed = d;      p.n_shared = d;
+    p.out_r = dw_gate;   p.out2_r = dw_up;   p.ld_r = d;
+    p.out_s = dws_gate;  p.out2_s = dws_up;  p.ld_s = d;
+    p.wgrad_gu = 1;
+    p.out_bf16 = grad_dtype == MOE_BF16 ? 1 : 0;
+    p.item_counter = ctr + 3;
+    if ((st = launch_bwd_pair<kWgrad>(
+             m, p,
+             static_cast<long long>(N) * (2 * I / 256) * (d / 256) +
+                 (sh ? static_cast<long long>(2 * SI / 256) * (d / 256) : 0),
+             cs)))
+      return st;
+    // 7. Wgrad (down): dW_down = dY^T H; shared dh^T H_s
+    if ((st = bwd_pair_maps({dY, R, d}, {H, R, I}, {dh, T, d}, {H_s, T, SI},
+                            sh, false, m)))
+      return st;
+    p.m_routed = d;   p.m_shared = d;
+    p.n_routed = I;   p.n_shared = SI;
+    p.out_r = dw_down;   p.out2_r = nullptr;  p.ld_r = I;
+    p.out_s = dws_down;  p.out2_s = nullptr;  p.ld_s = I;
+    p.wgrad_gu = 0;
+    p.item_counter = ctr + 4;
+    if ((st = launch_bwd_pair<kWgrad>(
+             m, p,
+             static_cast<long long>(N) * (d / 256) * (I / 256) +
+                 (sh ? static_cast<long long>(d / 256) * (SI / 256) : 0),
+             cs)))
+      return st;
   } else {
-    a_s = a_r;
-    b_s = b_r;
-  }
-  p.m_routed = I;  p.m_shared = SI;
-  p.k_routed = d;  p.k_shared = d;
-  p.out_r = dH;    p.ld_r = I;
-  p.out_s = dH_s;  p.ld_s = SI;
-  p.item_counter = ctr + 0;
-  if ((st = launch_bwd_gemm<kDgrad, 256, 4>(
-           a_r, b_r, a_s, b_s, p,
-           tok_items_r * (I / 128) + tok_items_s * (SI / 128), sms, cs)))
-    return st;
+    // 3. Dgrad (down): dH = dY W_down, dH_s = dh Ws_down
+    if ((st = make_map(&a_r, w_down, static_cast<long long>(N) * d, I, 64)))
+      return st;
+    if ((st = make_map(&b_r, dY, R, d, kBoxRows))) return st;
+    if (S > 0) {
+      if ((st = make_map(&a_s, ws_down_packed, d, SI, 64))) return st;
+      if ((st = make_map(&b_s, dh, T, d, kBoxRows))) return st;
+    } else {
+      a_s = a_r;
+      b_s = b_r;
+    }
+    p.m_routed = I;  p.m_shared = SI;
+    p.k_routed = d;  p.k_shared = d;
+    p.out_r = dH;    p.ld_r = I;
+    p.out_s = dH_s;  p.ld_s = SI;
+    p.item_counter = ctr + 0;
+    if ((st = launch_bwd_gemm<kDgrad, 256, 4>(
+             a_r, b_r, a_s, b_s, p,
+             tok_items_r * (I / 128) + tok_items_s * (SI / 128), sms, cs)))
+      return st;
 
-  // 4. gate/up recomputed with the SwiGLU backward: H, dA (and shared)
-  if ((st = make_map(&a_r, w_gu_packed, 2LL * N * I, d, kGemmBM))) return st;
-  if ((st = make_map(&b_r, X, R, d, kBoxRows))) return st;
-  if (S > 0) {
-    if ((st = make_map(&a_s, ws_gu_packed, 2LL * SI, d, kGemmBM))) return st;
-    if ((st = make_map(&b_s, u, T, d, kBoxRows))) return st;
-  } else {
-    a_s = a_r;
-    b_s = b_r;
-  }
-  p.m_routed = 2 * I;  p.m_shared = 2 * SI;
-  p.k_routed = d;      p.k_shared = d;
-  p.dh_r = dH;         p.dh_s = dH_s;
-  p.out_r = H;         p.ld_r = I;
-  p.out_s = H_s;       p.ld_s = SI;
-  p.out2_r = dA;       p.ld2_r = 2LL * I;
-  p.out2_s = dA_s;     p.ld2_s = 2LL * SI;
-  p.item_counter = ctr + 1;
-  if ((st = launch_bwd_gemm<kRecomp, 256, 4>(
-           a_r, b_r, a_s, b_s, p,
-           tok_items_r * (2 * I / 128) + tok_items_s * (2 * SI / 128), sms,
-           cs)))
-    return st;
+    // 4. gate/up recomputed with the SwiGLU backward: H, dA (and shared)
+    if ((st = make_map(&a_r, w_gu_packed, 2LL * N * I, d, kGemmBM))) return st;
+    if ((st = make_map(&b_r, X, R, d, kBoxRows))) return st;
+    if (S > 0) {
+      if ((st = make_map(&a_s, ws_gu_packed, 2LL * SI, d, kGemmBM))) return st;
+      if ((st = make_map(&b_s, u, T, d, kBoxRows))) return st;
+    } else {
+      a_s = a_r;
+      b_s = b_r;
+    }
+    p.m_routed = 2 * I;  p.m_shared = 2 * SI;
+    p.k_routed = d;      p.k_shared = d;
+    p.dh_r = dH;         p.dh_s = dH_s;
+    p.out_r = H;         p.ld_r = I;
+    p.out_s = H_s;       p.ld_s = SI;
+    p.out2_r = dA;       p.ld2_r = 2LL * I;
+    p.out2_s = dA_s;     p.ld2_s = 2LL * SI;
+    p.item_counter = ctr + 1;
+    if ((st = launch_bwd_gemm<kRecomp, 256, 4>(
+             a_r, b_r, a_s, b_s, p,
+             tok_items_r * (2 * I / 128) + tok_items_s * (2 * SI / 128), sms,
+             cs)))
+      return st;
 
-  // 5. Dgrad (gate/up): dX = dA W_gu, dX_s = dA_s Ws_gu
-  if ((st = make_map(&a_r, w_gu_packed, 2LL * N * I, d, 64))) return st;
-  if ((st = make_map(&b_r, dA, R, 2LL * I, kBoxRows))) return st;
-  if (S > 0) {
-    if ((st = make_map(&a_s, ws_gu_packed, 2LL * SI, d, 64))) return st;
-    if ((st = make_map(&b_s, dA_s, T, 2LL * SI, kBoxRows))) return st;
-  } else {
-    a_s = a_r;
-    b_s = b_r;
-  }
-  p.m_routed = d;      p.m_shared = d;
-  p.k_routed = 2 * I;  p.k_shared = 2 * SI;
-  p.out_r = dX;        p.ld_r = d;
-  p.out_s = dX_s;      p.ld_s = d;
-  p.item_counter = ctr + 2;
-  if ((st = launch_bwd_gemm<kDgrad, 256, 4>(
-           a_r, b_r, a_s, b_s, p,
-           tok_items_r * (d / 128) + tok_items_s * (d / 128), sms, cs)))
-    return st;
+    // 5. Dgrad (gate/up): dX = dA W_gu, dX_s = dA_s Ws_gu
+    if ((st = make_map(&a_r, w_gu_packed, 2LL * N * I, d, 64))) return st;
+    if ((st = make_map(&b_r, dA, R, 2LL * I, kBoxRows))) return st;
+    if (S > 0) {
+      if ((st = make_map(&a_s, ws_gu_packed, 2LL * SI, d, 64))) return st;
+      if ((st = make_map(&b_s, dA_s, T, 2LL * SI, kBoxRows))) return st;
+    } else {
+      a_s = a_r;
+      b_s = b_r;
+    }
+    p.m_routed = d;      p.m_shared = d;
+    p.k_routed = 2 * I;  p.k_shared = 2 * SI;
+    p.out_r = dX;        p.ld_r = d;
+    p.out_s = dX_s;      p.ld_s = d;
+    p.item_counter = ctr + 2;
+    if ((st = launch_bwd_gemm<kDgrad, 256, 4>(
+             a_r, b_r, a_s, b_s, p,
+             tok_items_r * (d / 128) + tok_items_s * (d / 128), sms, cs)))
+      return st;
 
-  // 6. Wgrad (gate/up): dW_gate / dW_up = dA^T X; shared dA_s^T u
-  const bool gb = grad_dtype == MOE_BF16;
-  if ((st = make_map(&a_r, dA, R, 2LL * I, 64))) return st;
-  if ((st = make_map(&b_r, X, R, d, 64))) return st;
-  if (S > 0) {
-    if ((st = make_map(&a_s, dA_s, T, 2LL * SI, 64))) return st;
-    if ((st = make_map(&b_s, u, T, d, 64))) return st;
-  } else {
-    a_s = a_r;
-    b_s = b_r;
-  }
-  p.m_routed = 2 * I;  p.m_shared = 2 * SI;
-  p.n_routed = d;      p.n_shared = d;
-  p.out_r = dw_gate;   p.out2_r = dw_up;   p.ld_r = d;
-  p.out_s = dws_gate;  p.out2_s = dws_up;  p.ld_s = d;
-  p.wgrad_gu = 1;
-  p.out_bf16 = gb ? 1 : 0;
-  p.item_counter = ctr + 3;
-  {
-    const bool b256 = d % 256 == 0;
-    const int bn = b256 ? 256 : 128;
-    const long long items =
-        static_cast<long long>(N) * (2 * I / 128) * cdiv(d, bn) +
-        (S > 0 ? static_cast<long long>(2 * SI / 128) * cdiv(d, bn) : 0);
-    st = b256 ? launch_bwd_gemm<kWgrad, 256, 4>(a_r, b_r, a_s, b_s, p, items,
-                                                sms, cs)
-              : launch_bwd_gemm<kWgrad, 128, 6>(a_r, b_r, a_s, b_s, p, items,
-                                                sms, cs);
-    if (st != MOE_OK) return st;
-  }
+    // 6. Wgrad (gate/up): dW_gate / dW_up = dA^T X; shared dA_s^T u
+    const bool gb = grad_dtype == MOE_BF16;
+    if ((st = make_map(&a_r, dA, R, 2LL * I, 64))) return st;
+    if ((st = make_map(&b_r, X, R, d, 64))) return st;
+    if (S > 0) {
+      if ((st = make_map(&a_s, dA_s, T, 2LL * SI, 64))) return st;
+      if ((st = make_map(&b_s, u, T, d, 64))) return st;
+    } else {
+      a_s = a_r;
+      b_s = b_r;
+    }
+    p.m_routed = 2 * I;  p.m_shared = 2 * SI;
+    p.n_routed = d;      p.n_shared = d;
+    p.out_r = dw_gate;   p.out2_r = dw_up;   p.ld_r = d;
+    p.out_s = dws_gate;  p.out2_s = dws_up;  p.ld_s = d;
+    p.wgrad_gu = 1;
+    p.out_bf16 = gb ? 1 : 0;
+    p.item_counter = ctr + 3;
+    {
+      const bool b256 = d % 256 == 0;
+      const int bn = b256 ? 256 : 128;
+      const long long items =
+          static_cast<long long>(N) * (2 * I / 128) * cdiv(d, bn) +
+          (S > 0 ? static_cast<long long>(2 * SI / 128) * cdiv(d, bn) : 0);
+      st = b256 ? launch_bwd_gemm<kWgrad, 256, 4>(a_r, b_r, a_s, b_s, p, items,
+                                                  sms, cs)
+                : launch_bwd_gemm<kWgrad, 128, 6>(a_r, b_r, a_s, b_s, p, items,
+                                                  sms, cs);
+      if (st != MOE_OK) return st;
+    }
 
-  // 7. Wgrad (down): dW_down = dY^T H; shared dh^T H_s
-  if ((st = make_map(&a_r, dY, R, d, 64))) return st;
-  if ((st = make_map(&b_r, H, R, I, 64))) return st;
-  if (S > 0) {
-    if ((st = make_map(&a_s, dh, T, d, 64))) return st;
-    if ((st = make_map(&b_s, H_s, T, SI, 64))) return st;
-  } else {
-    a_s = a_r;
-    b_s = b_r;
-  }
-  p.m_routed = d;   p.m_shared = d;
-  p.n_routed = I;   p.n_shared = SI;
-  p.out_r = dw_down;   p.out2_r = nullptr;  p.ld_r = I;
-  p.out_s = dws_down;  p.out2_s = nullptr;  p.ld_s = I;
-  p.wgrad_gu = 0;
-  p.item_counter = ctr + 4;
-  {
-    const bool b256 = I % 256 == 0 && SI % 256 == 0;
-    const int bn = b256 ? 256 : 128;
-    const long long items =
-        static_cast<long long>(N) * (d / 128) * cdiv(I, bn) +
-        (S > 0 ? static_cast<long long>(d / 128) * cdiv(SI, bn) : 0);
-    st = b256 ? launch_bwd_gemm<kWgrad, 256, 4>(a_r, b_r, a_s, b_s, p, items,
-                                                sms, cs)
-              : launch_bwd_gemm<kWgrad, 128, 6>(a_r, b_r, a_s, b_s, p, items,
-                                                sms, cs);
-    if (st != MOE_OK) return st;
+    // 7. Wgrad (down): dW_down = dY^T H; shared dh^T H_s
+    if ((st = make_map(&a_r, dY, R, d, 64))) return st;
+    if ((st = make_map(&b_r, H, R, I, 64))) return st;
+    if (S > 0) {
+      if ((st = make_map(&a_s, dh, T, d, 64))) return st;
+      if ((st = make_map(&b_s, H_s, T, SI, 64))) return st;
+    } else {
+      a_s = a_r;
+      b_s = b_r;
+    }
+    p.m_routed = d;   p.m_shared = d;
+    p.n_routed = I;   p.n_shared = SI;
+    p.out_r = dw_down;   p.out2_r = nullptr;  p.ld_r = I;
+    p.out_s = dws_down;  p.out2_s = nullptr;  p.ld_s = I;
+    p.wgrad_gu = 0;
+    p.item_counter = ctr + 4;
+    {
+      const bool b256 = I % 256 == 0 && SI % 256 == 0;
+      const int bn = b256 ? 256 : 128;
+      const long long items =
+          static_cast<long long>(N) * (d / 128) * cdiv(I, bn) +
+          (S > 0 ? static_cast<long long>(d / 128) * cdiv(SI, bn) : 0);
+      st = b256 ? launch_bwd_gemm<kWgrad, 256, 4>(a_r, b_r, a_s, b_s, p, items,
+                                                  sms, cs)
+                : launch_bwd_gemm<kWgrad, 128, 6>(a_r, b_r, a_s, b_s, p, items,
+                                                  sms, cs);
+      if (st != MOE_OK) return st;
+    }
   }
 
   // 8. centroid gradient; 9. input gradient

@@ -54,9 +54,85 @@ struct BwdPairSmem {
 // M-atoms} for Dgrad) and the token operand with 32-, 64- and 128-row boxes
 // (the smallest box that covers a CTA's token half is used).  Wgrad: A and
 // B MN-major in the 128-row slots.
+// Wgrad also takes the gradients' output maps: o (W_gate or W_down grads)
+// and o2 (W_up grads), routed and shared, 2-D boxes of 32 x 32 elements
+// with 64-byte (bf16) or 128-byte (fp32) swizzle.
 struct BwdPairMaps {
   CUtensorMap a_r, a_s, b_r32, b_s32, b_r64, b_s64, b_r128, b_s128;
+  CUtensorMap o_r, o2_r, o_s, o2_s;
 };
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a,
+                                             uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a),
+               "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
+// kWgrad epilogue on CTA pairs: one warp's 32 accumulator rows x the tile's
+// 256 columns, 32 columns at a time: TMEM -> registers -> a 32 x 32 box in
+// shared memory laid out as the output map's swizzle expects -> one TMA
+// store issued by lane 0.  The global writes leave as whole boxes, off the
+// load/store path.  bf16 boxes (2 KB, 64-byte rows) alternate between two
+// buffers; fp32 boxes (4 KB, 128-byte rows) use one.  Box (x, y): x = column
+// n0 + c0, y = `y` (the warp's first output row); for the shared down
+// gradient (col_split = I) column c is column c % I of rows y + (c / I)
+// s_rows.  `zero`: the group had no rows, zeros are stored.
+__device__ __forceinline__ void bwd_ep_wgrad_tma(uint32_t taddr, bool zero,
+                                                 const CUtensorMap* map,
+                                                 int n0, int y, int col_split,
+                                                 int s_rows, bool bf16,
+                                                 uint32_t stage, int lane) {
+#pragma unroll 1
+  for (int c0 = 0; c0 < kBwdPairBN; c0 += 32) {
+    uint32_t r[32];
+    if (!zero) {
+      tmem_ld32(taddr + c0, r);
+      tmem_ld_wait();
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) r[j] = 0u;
+    }
+    const uint32_t buf = bf16 ? stage + ((c0 >> 5) & 1) * 2048u : stage;
+    if (lane == 0) {
+      if (bf16)
+        bulk_wait_read<1>();
+      else
+        bulk_wait_read<0>();
+    }
+    __syncwarp();
+    if (bf16) {   // row = lane: 4 chunks of 16 B, 64-byte swizzle
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+#define MOE_F(k) __uint_as_float(r[cc * 8 + (k)])
+        st_shared_v4(buf + lane * 64 + ((cc ^ ((lane >> 1) & 3)) * 16),
+                     pack_bf16x2(MOE_F(0), MOE_F(1)),
+                     pack_bf16x2(MOE_F(2), MOE_F(3)),
+                     pack_bf16x2(MOE_F(4), MOE_F(5)),
+                     pack_bf16x2(MOE_F(6), MOE_F(7)));
+#undef MOE_F
+      }
+    } else {      // row = lane: 8 chunks of 16 B, 128-byte swizzle
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc)
+        st_shared_v4(buf + lane * 128 + ((cc ^ (lane & 7)) * 16),
+                     r[cc * 4], r[cc * 4 + 1], r[cc * 4 + 2], r[cc * 4 + 3]);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      const int c = n0 + c0;
+      int x = c, yy = y;
+      if (col_split > 0) {
+        x = c % col_split;
+        yy = y + (c / col_split) * s_rows;
+      }
+      tma_store_2d(map, x, yy, buf);
+      bulk_commit();
+    }
+  }
+}
 
 // Item -> tile.  Tokens kinds: (group, 256-row M tile, token chunk), chunk
 // fastest; a group's chunks split its tokens evenly (each rounded up to
@@ -466,9 +542,26 @@ bwd_gemm_pair_kernel(const __grid_constant__ BwdPairMaps maps,
                                                            : p.out2_r),
                       t.shared ? p.ld2_s : p.ld2_r, stg, q, lane);
       } else {
-        const WgradRow w = wgrad_row(p, t.shared != 0, t.e, m_cta + q * 32);
-        bwd_ep_wgrad_warp(ta, t.n0, t.n_valid, kBwdPairBN, t.nk == 0, w,
-                          p.out_bf16 != 0, stg + q * 32 * 33, lane);
+        const int m = m_cta + q * 32;       // the warp's first output row
+        const CUtensorMap* om;
+        int y, col_split = 0, s_rows = 0;
+        if (p.wgrad_gu) {   // packed row -> gate / up row of [.., I, d]
+          const int within = m & 127;
+          const int irow = (m >> 7) * 64 + (within & 63);
+          const bool gate = within < 64;
+          om = t.shared ? (gate ? &maps.o_s : &maps.o2_s)
+                        : (gate ? &maps.o_r : &maps.o2_r);
+          y = (t.shared ? 0 : t.e * p.I) + irow;
+        } else {            // [.., d, I]
+          om = t.shared ? &maps.o_s : &maps.o_r;
+          y = (t.shared ? 0 : t.e * p.m_routed) + m;
+          if (t.shared) {
+            col_split = p.I;
+            s_rows = p.m_shared;
+          }
+        }
+        bwd_ep_wgrad_tma(ta, t.nk == 0, om, t.n0, y, col_split, s_rows,
+                         p.out_bf16 != 0, smem_u32(stg) + q * 4096u, lane);
       }
       tc_fence_before();
       __syncwarp();
@@ -479,6 +572,8 @@ bwd_gemm_pair_kernel(const __grid_constant__ BwdPairMaps maps,
       }
     }
     if (ovf) report_error(ERR_CHECK, KID_GEMM_BWD, 200);
+    if constexpr (KIND == kWgrad)
+      if (lane == 0) bulk_wait_all();   // stores done before smem goes away
   }
 
   tc_fence_before();

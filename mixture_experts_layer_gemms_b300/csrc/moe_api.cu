@@ -1393,6 +1393,32 @@ moe_status bwd_pair_maps(Op a_r, Op b_r, Op a_s, Op b_s, bool shared,
     m.b_s64 = m.b_r64;
     m.b_s128 = m.b_r128;
   }
+  m.o_r = m.o2_r = m.o_s = m.o2_s = m.a_r;   // Wgrad sets its own
+  return MOE_OK;
+}
+
+// Output map of a weight gradient [rows, cols] (bf16 or fp32) for the
+// Wgrad TMA stores: boxes of 32 x 32 elements, swizzled to match the
+// epilogue's shared-memory layout (64-byte rows for bf16, 128-byte for
+// fp32).
+moe_status make_map_grad(CUtensorMap* m, const void* ptr, long long rows,
+                         long long cols, bool bf16) {
+  moe_status st = get_encoder();
+  if (st != MOE_OK) return st;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols),
+                        static_cast<cuuint64_t>(rows > 0 ? rows : 1)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * (bf16 ? 2 : 4)};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(
+      m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+      2, const_cast<void*>(ptr), dims, strides, box, estr,
+      CU_TENSOR_MAP_INTERLEAVE_NONE,
+      bf16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+      CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled (gradient) failed (%d) "
+                "rows=%lld cols=%lld", static_cast<int>(r), rows, cols);
   return MOE_OK;
 }
 
@@ -1594,6 +1620,18 @@ moe_status moe_backward(const moe_shape* s, const void* dh, const void* u,
     p.wgrad_gu = 1;
     p.out_bf16 = grad_dtype == MOE_BF16 ? 1 : 0;
     p.item_counter = ctr + 3;
+    {
+      const bool gb = p.out_bf16 != 0;
+      if ((st = make_map_grad(&m.o_r, dw_gate, NI, d, gb))) return st;
+      if ((st = make_map_grad(&m.o2_r, dw_up, NI, d, gb))) return st;
+      if (sh) {
+        if ((st = make_map_grad(&m.o_s, dws_gate, SI, d, gb))) return st;
+        if ((st = make_map_grad(&m.o2_s, dws_up, SI, d, gb))) return st;
+      } else {
+        m.o_s = m.o_r;
+        m.o2_s = m.o2_r;
+      }
+    }
     if ((st = launch_bwd_pair<kWgrad>(
              m, p,
              static_cast<long long>(N) * (2 * I / 256) * (d / 256) +
@@ -1610,6 +1648,21 @@ moe_status moe_backward(const moe_shape* s, const void* dh, const void* u,
     p.out_s = dws_down;  p.out2_s = nullptr;  p.ld_s = I;
     p.wgrad_gu = 0;
     p.item_counter = ctr + 4;
+    {
+      const bool gb = p.out_bf16 != 0;
+      if ((st = make_map_grad(&m.o_r, dw_down, static_cast<long long>(N) * d,
+                              I, gb)))
+        return st;
+      if (sh) {
+        if ((st = make_map_grad(&m.o_s, dws_down,
+                                static_cast<long long>(S) * d, I, gb)))
+          return st;
+      } else {
+        m.o_s = m.o_r;
+      }
+      m.o2_r = m.o_r;
+      m.o2_s = m.o_s;
+    }
     if ((st = launch_bwd_pair<kWgrad>(
              m, p,
              static_cast<long long>(N) * (d / 256) * (I / 256) +

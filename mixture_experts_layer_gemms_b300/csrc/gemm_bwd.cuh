@@ -225,11 +225,22 @@ __device__ __forceinline__ void bwd_ep_recomp(
   const int pair_q = q & 1;
   const int i = wt * 64 + pair_q * 32 + lane;        // column of H / dH
   const int ca = wt * 128 + pair_q * 32 + lane;      // packed column of da
+  const int jbase = gate_warp ? 0 : 16;
   for (int n0 = 0; n0 < n_valid; n0 += 32) {
+    const int nleft = n_valid - n0;
+    // this thread's 16 dH values, loaded before the TMEM read and the
+    // exchange so that their latency overlaps them (the H / dA stores
+    // below could alias dH as far as the compiler knows)
+    float gv[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      gv[j] = jbase + j < nleft
+                  ? __half2float(dH[static_cast<size_t>(b_row + n0 + jbase + j) *
+                                        ld_h + i])
+                  : 0.f;
     uint32_t r[32];
     tmem_ld32(taddr + n0, r);
     tmem_ld_wait();
-    const int nleft = n_valid - n0;
     float* mine = xchg + ((q * 32) + lane) * 17;
 #pragma unroll
     for (int j = 0; j < 16; ++j)
@@ -237,14 +248,13 @@ __device__ __forceinline__ void bwd_ep_recomp(
     named_bar_sync(1, 128);
     const float* theirs =
         xchg + (((gate_warp ? q + 2 : q - 2) * 32) + lane) * 17;
-    const int jbase = gate_warp ? 0 : 16;
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
       if (jbase + j >= nleft) continue;
       const float a = gate_warp ? __uint_as_float(r[j]) : theirs[j];
       const float c = gate_warp ? theirs[j] : __uint_as_float(r[16 + j]);
       const size_t row = static_cast<size_t>(b_row + n0 + jbase + j);
-      const float g = __half2float(dH[row * ld_h + i]);
+      const float g = gv[j];
       const float sg = 1.0f / (1.0f + expf(-a));
       const float si = a * sg;
       H[row * ld_h + i] = __float2bfloat16_rn(si * c);

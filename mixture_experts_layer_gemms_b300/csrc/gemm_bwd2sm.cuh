@@ -41,7 +41,7 @@ struct BwdPairSmem {
   static constexpr int n_bars = 2 * kBwdPairStages + 5 + 2 * kSchedDepth;
   static constexpr int misc_off = bar_off + n_bars * 8;
   static constexpr int epok_off = misc_off + 16;
-  static constexpr int sched_off = epok_off + 16;
+  static constexpr int sched_off = epok_off + 32;     // 8 epilogue verdicts
   static constexpr int tab_off = sched_off + 4 * kSchedDepth;
   static constexpr int total = tab_off + 3 * (kMaxGroups + 1) * 4;
   static constexpr int alloc = total + 1024;
@@ -70,22 +70,38 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a,
                : "memory");
 }
 
-// kWgrad epilogue on CTA pairs: one warp's 32 accumulator rows x the tile's
-// 256 columns, 32 columns at a time: TMEM -> registers -> a 32 x 32 box in
-// shared memory laid out as the output map's swizzle expects -> one TMA
-// store issued by lane 0.  The global writes leave as whole boxes, off the
-// load/store path.  bf16 boxes (2 KB, 64-byte rows) alternate between two
-// buffers; fp32 boxes (4 KB, 128-byte rows) use one.  Box (x, y): x = column
-// n0 + c0, y = `y` (the warp's first output row); for the shared down
-// gradient (col_split = I) column c is column c % I of rows y + (c / I)
-// s_rows.  `zero`: the group had no rows, zeros are stored.
-__device__ __forceinline__ void bwd_ep_wgrad_tma(uint32_t taddr, bool zero,
+// kWgrad epilogue on CTA pairs: one warp's 32 accumulator rows x 128 of
+// the tile's 256 columns (`cbeg` .. +128; two warps share each TMEM lane
+// quarter), 32 columns at a time: TMEM -> registers -> a box in the warp's
+// 2 KB of shared memory, laid out as the output map's 64-byte swizzle
+// expects (rows of 64 bytes: 32 bf16 or 16 fp32 columns) -> one TMA store
+// per box, issued by lane 0.  The global writes leave as whole boxes, off
+// the load/store path.  Box (x, y): x = column n0 + c, y = `y` (the warp's
+// first output row); for the shared down gradient (col_split = I) column c
+// is column c % I of rows y + (c / I) s_rows.  `zero`: the group had no
+// rows, zeros are stored.
+__device__ __forceinline__ void wgrad_store_box(const CUtensorMap* map, int c,
+                                                int y, int col_split,
+                                                int s_rows, uint32_t buf) {
+  int x = c, yy = y;
+  if (col_split > 0) {
+    x = c % col_split;
+    yy = y + (c / col_split) * s_rows;
+  }
+  tma_store_2d(map, x, yy, buf);
+  bulk_commit();
+}
+
+__device__ __forceinline__ void bwd_ep_wgrad_tma(uint32_t taddr, int cbeg,
+                                                 bool zero,
                                                  const CUtensorMap* map,
                                                  int n0, int y, int col_split,
                                                  int s_rows, bool bf16,
-                                                 uint32_t stage, int lane) {
+                                                 uint32_t buf, int lane) {
+  const uint32_t row_addr = buf + lane * 64;
+  const int sw = (lane >> 1) & 3;            // 64-byte swizzle of this row
 #pragma unroll 1
-  for (int c0 = 0; c0 < kBwdPairBN; c0 += 32) {
+  for (int c0 = cbeg; c0 < cbeg + 128; c0 += 32) {
     uint32_t r[32];
     if (!zero) {
       tmem_ld32(taddr + c0, r);
@@ -94,42 +110,37 @@ __device__ __forceinline__ void bwd_ep_wgrad_tma(uint32_t taddr, bool zero,
 #pragma unroll
       for (int j = 0; j < 32; ++j) r[j] = 0u;
     }
-    const uint32_t buf = bf16 ? stage + ((c0 >> 5) & 1) * 2048u : stage;
-    if (lane == 0) {
-      if (bf16)
-        bulk_wait_read<1>();
-      else
-        bulk_wait_read<0>();
-    }
-    __syncwarp();
-    if (bf16) {   // row = lane: 4 chunks of 16 B, 64-byte swizzle
+    if (bf16) {            // one box of 32 columns
+      if (lane == 0) bulk_wait_read<0>();
+      __syncwarp();
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
 #define MOE_F(k) __uint_as_float(r[cc * 8 + (k)])
-        st_shared_v4(buf + lane * 64 + ((cc ^ ((lane >> 1) & 3)) * 16),
+        st_shared_v4(row_addr + ((cc ^ sw) * 16),
                      pack_bf16x2(MOE_F(0), MOE_F(1)),
                      pack_bf16x2(MOE_F(2), MOE_F(3)),
                      pack_bf16x2(MOE_F(4), MOE_F(5)),
                      pack_bf16x2(MOE_F(6), MOE_F(7)));
 #undef MOE_F
       }
-    } else {      // row = lane: 8 chunks of 16 B, 128-byte swizzle
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) wgrad_store_box(map, n0 + c0, y, col_split, s_rows, buf);
+    } else {               // two boxes of 16 columns
 #pragma unroll
-      for (int cc = 0; cc < 8; ++cc)
-        st_shared_v4(buf + lane * 128 + ((cc ^ (lane & 7)) * 16),
-                     r[cc * 4], r[cc * 4 + 1], r[cc * 4 + 2], r[cc * 4 + 3]);
-    }
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) {
-      const int c = n0 + c0;
-      int x = c, yy = y;
-      if (col_split > 0) {
-        x = c % col_split;
-        yy = y + (c / col_split) * s_rows;
+      for (int hb = 0; hb < 2; ++hb) {
+        if (lane == 0) bulk_wait_read<0>();
+        __syncwarp();
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc)
+          st_shared_v4(row_addr + ((cc ^ sw) * 16), r[hb * 16 + cc * 4],
+                       r[hb * 16 + cc * 4 + 1], r[hb * 16 + cc * 4 + 2],
+                       r[hb * 16 + cc * 4 + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0)
+          wgrad_store_box(map, n0 + c0 + hb * 16, y, col_split, s_rows, buf);
       }
-      tma_store_2d(map, x, yy, buf);
-      bulk_commit();
     }
   }
 }
@@ -211,8 +222,20 @@ __device__ __forceinline__ BTile bwd_decode_pair(int item, const BwdParams& p,
   return t;
 }
 
+// Threads: producer warp, MMA warp, then 4 epilogue warps (8 for Wgrad,
+// whose epilogue -- 128 x 256 stores per short K loop -- is its bound).
 template <int KIND>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
+__host__ __device__ constexpr int bwd_pair_epi_warps() {
+  return KIND == kWgrad ? 8 : 4;
+}
+template <int KIND>
+__host__ __device__ constexpr int bwd_pair_threads() {
+  return 64 + 32 * bwd_pair_epi_warps<KIND>();
+}
+
+template <int KIND>
+__global__ void __cluster_dims__(2, 1, 1)
+__launch_bounds__(bwd_pair_threads<KIND>(), 1)
 bwd_gemm_pair_kernel(const __grid_constant__ BwdPairMaps maps,
                      const BwdParams p) {
   using L = BwdPairSmem;
@@ -220,6 +243,7 @@ bwd_gemm_pair_kernel(const __grid_constant__ BwdPairMaps maps,
   constexpr bool kTokens = KIND != kWgrad;
   constexpr bool kAmn = KIND != kRecomp;
   constexpr bool kBmn = KIND == kWgrad;
+  constexpr int NEPI = bwd_pair_epi_warps<KIND>();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -258,12 +282,12 @@ bwd_gemm_pair_kernel(const __grid_constant__ BwdPairMaps maps,
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(bar_tfull + 8 * a, 1);
-      mbar_init(bar_tempty + 8 * a, 8);       // 4 epilogue warps x 2 CTAs
+      mbar_init(bar_tempty + 8 * a, 2 * NEPI);   // epilogue warps x 2 CTAs
     }
     mbar_init(bar_final, 1);
     for (int i = 0; i < kSchedDepth; ++i) {
       mbar_init(bar_sfull + 8 * i, 1);
-      mbar_init(bar_sempty + 8 * i, 10);      // 5 consumers x 2 CTAs
+      mbar_init(bar_sempty + 8 * i, 2 * (1 + NEPI));   // consumers x 2 CTAs
     }
     *abort_flag = 0;
     *bad_flag = 0;
@@ -497,7 +521,7 @@ bwd_gemm_pair_kernel(const __grid_constant__ BwdPairMaps maps,
       mbar_drain_cl(bar_final, 0);
     }
   } else {
-    // ---------------- epilogue (warps 2..5 of both CTAs) ----------------
+    // ---------- epilogue (warps 2 .. 1 + NEPI of both CTAs) ----------
     const int ep = warp - 2;
     const int q = warp & 3;
     int acc = 0;
@@ -521,8 +545,11 @@ bwd_gemm_pair_kernel(const __grid_constant__ BwdPairMaps maps,
                        KID_GEMM_BWD, 108);
       const bool wok = __all_sync(0xffffffffu, ok);
       if (lane == 0) ep_ok[ep] = wok ? 1 : 0;
-      named_bar_sync(1, 128);
-      if (!(ep_ok[0] && ep_ok[1] && ep_ok[2] && ep_ok[3])) break;
+      named_bar_sync(1, 32 * NEPI);
+      bool all_ok = true;
+#pragma unroll
+      for (int w = 0; w < NEPI; ++w) all_ok = all_ok && ep_ok[w] != 0;
+      if (!all_ok) break;
       if (item >= n_items) break;
       const BTile t = bwd_decode_pair<KIND>(item, p, n_items_s, nch_s, offp,
                                             cnt, chunk_pre);
@@ -560,8 +587,9 @@ bwd_gemm_pair_kernel(const __grid_constant__ BwdPairMaps maps,
             s_rows = p.m_shared;
           }
         }
-        bwd_ep_wgrad_tma(ta, t.nk == 0, om, t.n0, y, col_split, s_rows,
-                         p.out_bf16 != 0, smem_u32(stg) + q * 4096u, lane);
+        bwd_ep_wgrad_tma(ta, (ep >> 2) * 128, t.nk == 0, om, t.n0, y,
+                         col_split, s_rows, p.out_bf16 != 0,
+                         smem_u32(stg) + ep * 2048u, lane);
       }
       tc_fence_before();
       __syncwarp();

@@ -130,6 +130,7 @@ moe_status device_setup(int* sm_count) {
     MOE_CHECK_CUDA(allow_smem(bwd_gemm_pair_kernel<kWgrad>,
                               BwdPairSmem::alloc));
     cfg.dynamicSmemBytes = BwdPairSmem::alloc;
+    cfg.blockDim = dim3(bwd_pair_threads<kWgrad>());
     clusters = 0;
     MOE_CHECK_CUDA(cudaOccupancyMaxActiveClusters(
         &clusters, bwd_gemm_pair_kernel<kWgrad>, &cfg));
@@ -1398,9 +1399,8 @@ moe_status bwd_pair_maps(Op a_r, Op b_r, Op a_s, Op b_s, bool shared,
 }
 
 // Output map of a weight gradient [rows, cols] (bf16 or fp32) for the
-// Wgrad TMA stores: boxes of 32 x 32 elements, swizzled to match the
-// epilogue's shared-memory layout (64-byte rows for bf16, 128-byte for
-// fp32).
+// Wgrad TMA stores: boxes of 32 rows x 64 bytes (32 bf16 or 16 fp32
+// columns) with 64-byte swizzle, the epilogue's shared-memory layout.
 moe_status make_map_grad(CUtensorMap* m, const void* ptr, long long rows,
                          long long cols, bool bf16) {
   moe_status st = get_encoder();
@@ -1408,13 +1408,12 @@ moe_status make_map_grad(CUtensorMap* m, const void* ptr, long long rows,
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols),
                         static_cast<cuuint64_t>(rows > 0 ? rows : 1)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * (bf16 ? 2 : 4)};
-  cuuint32_t box[2] = {32, 32};
+  cuuint32_t box[2] = {bf16 ? 32u : 16u, 32u};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(
       m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
       2, const_cast<void*>(ptr), dims, strides, box, estr,
-      CU_TENSOR_MAP_INTERLEAVE_NONE,
-      bf16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
       CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
     return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled (gradient) failed (%d) "
@@ -1431,7 +1430,8 @@ moe_status launch_bwd_pair(const BwdPairMaps& m, const BwdParams& p,
     return fail(MOE_ERR_CUDA, "backward CTA-pair GEMM cannot be resident");
   const long long n = max_items < clusters ? max_items : clusters;
   bwd_gemm_pair_kernel<KIND>
-      <<<static_cast<int>(2 * n), 192, BwdPairSmem::alloc, cs>>>(m, p);
+      <<<static_cast<int>(2 * n), bwd_pair_threads<KIND>(), BwdPairSmem::alloc,
+         cs>>>(m, p);
   MOE_CHECK_LAUNCH();
   return MOE_OK;
 }

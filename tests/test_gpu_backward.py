@@ -70,6 +70,11 @@ CASES = {
                                     d_ff=256)),
     "single_token": ("tiny", dict(BASE, T=1)),
     "mid_dims_T700": ("mid", dict(T=700)),
+    # CTA-pair kernels (d, d_ff multiples of 256) under skewed centroids:
+    # experts with 185..982 tokens -> multi-chunk Dgrad / recompute items
+    # and Wgrad K loops of up to 16 blocks
+    "skew_pair_T2000": ("tiny", dict(BASE, T=2000, d=512, d_ff=256,
+                                     zipf=1.1)),
 }
 
 
@@ -105,10 +110,14 @@ def test_backward_parity(moe, case):
     print(case, out)
 
 
-def test_backward_bf16_gradients(moe):
+@pytest.mark.parametrize("over", [dict(BASE, T=200),
+                                  dict(BASE, T=300, d=512, d_ff=256,
+                                       n_shared=2)],
+                         ids=["single_sm", "cta_pair"])
+def test_backward_bf16_gradients(moe, over):
     """Weight gradients stored as bf16 are the fp32 gradients rounded once
     (to nearest even); du and dE do not depend on the gradient dtype."""
-    cfg = get_config("tiny").with_(**dict(BASE, T=200))
+    cfg = get_config("tiny").with_(**over)
     g, dh, layer, g16 = _run(moe, cfg, torch.bfloat16)
     g16 = {k: v.float().clone() for k, v in g16.items()}
     g32 = layer.backward(g["u"], dh, grad_dtype=torch.float32)

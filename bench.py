@@ -341,7 +341,15 @@ def time_backward(args, cfg, layer, u, dev, ws, peaks):
     alg = 12.0 * cfg.d * cfg.d_ff * rows
     exe = 16.0 * cfg.d * cfg.d_ff * rows
     pk = peaks["bf16_tflops"]
-    return {"ms_per_call": bw_ms,
+    ach = alg / (bw_ms / 1e3) / 1e12
+    roof = {"bound": "tensor", "achieved": ach, "peak": pk,
+            "unit": "TFLOP/s", "frac": ach / pk, "traffic": None,
+            "kernel": "the moe_backward call (Dgrad, recompute and Wgrad "
+                      "CTA-pair GEMMs are 95% of it); algorithmic FLOPs "
+                      "12 d d_ff per token-expert and per shared-expert "
+                      "token",
+            "peak_source": f"{peaks['source']} bf16_tflops (burst)"}
+    return {"ms_per_call": bw_ms, "roofline": roof,
             "train_step_tokens_per_s": ws * cfg.T / (train_ms / 1e3),
             "train_step_ms": train_ms,
             "algorithmic_tflops": alg / (bw_ms / 1e3) / 1e12,

@@ -293,29 +293,37 @@ class MoELayer:
         comp.wait_stream(down)
 
     def graph(self, u: torch.Tensor, update_bias: bool = False,
-              gamma: float = 1e-3):
+              gamma: float = 1e-3, dh: Optional[torch.Tensor] = None,
+              grad_dtype: torch.dtype = torch.float32):
         """Capture one forward on ``u`` (a fixed device buffer) into a CUDA
         graph and return a function that replays it.  Every call of the step
         is asynchronous with no host synchronisation, so the whole step --
         route, permute, expert FFNs, combine (and the bias update when asked)
         -- replays as one graph launch.  Write new tokens into ``u`` between
         replays; the result is this layer's buffer for ``u.shape[0]``.  With
-        ``update_bias`` every replay moves the bias once."""
+        ``update_bias`` every replay moves the bias once.  With ``dh`` (a
+        fixed device buffer of upstream gradients) the backward pass is
+        captured after the forward, and a replay returns (h, gradients) --
+        one training step per graph launch."""
         T = u.shape[0]
         self.buffers(T)
         side = torch.cuda.Stream(device=u.device)
         side.wait_stream(torch.cuda.current_stream(u.device))
         with torch.cuda.stream(side):      # first-use set-up outside capture
             self.forward(u)
+            if dh is not None:
+                self.backward(u, dh, grad_dtype=grad_dtype)
         torch.cuda.current_stream(u.device).wait_stream(side)
         torch.cuda.synchronize(u.device)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             h = self.forward(u, update_bias=update_bias, gamma=gamma)
+            grads = (self.backward(u, dh, grad_dtype=grad_dtype)
+                     if dh is not None else None)
 
-        def replay() -> torch.Tensor:
+        def replay():
             g.replay()
-            return h
+            return h if grads is None else (h, grads)
         replay.graph = g
         return replay
 

@@ -229,3 +229,33 @@ def test_backward_full_v3_prefill_sampled(moe):
     grad_close(gr["dws_gate"][0][R].float().cpu().numpy(), dWg, "dWs_gate")
     grad_close(gr["dws_up"][0][R].float().cpu().numpy(), dWu, "dWs_up")
     grad_close(gr["dws_down"][0][:, R].float().cpu().numpy(), dWd, "dWs_down")
+
+
+def test_training_step_graph(moe):
+    """Forward + bias update + backward captured as one CUDA graph replay
+    the eager step bit for bit, on new tokens and gradients written into the
+    captured buffers."""
+    cfg = get_config("tiny").with_(**dict(BASE, T=300, d=512, d_ff=256))
+    g = make_inputs(cfg)
+    mk = lambda: _layer(moe, g, cfg)
+    eager, graphed = mk(), mk()
+    u = g["u"].clone()
+    dh = upstream_grad(cfg, "cpu").to("cuda")
+    run = graphed.graph(u, update_bias=True, dh=dh, grad_dtype=torch.bfloat16)
+    gen = torch.Generator(device="cuda").manual_seed(11)
+    for step in range(3):
+        if step:
+            u.copy_(torch.randn(u.shape, generator=gen, device="cuda")
+                    .to(u.dtype))
+            dh.copy_(torch.randn(dh.shape, generator=gen, device="cuda")
+                     .to(dh.dtype))
+        want_h = eager(u, update_bias=True).clone()
+        want = {k: v.clone() for k, v in
+                eager.backward(u, dh, grad_dtype=torch.bfloat16).items()}
+        h, grads = run()
+        torch.cuda.synchronize()
+        moe.get_device_error()
+        assert torch.equal(want_h, h), step
+        for k in want:
+            assert torch.equal(want[k], grads[k]), (step, k)
+        assert torch.equal(eager.bias, graphed.bias), step

@@ -259,3 +259,38 @@ def test_training_step_graph(moe):
         for k in want:
             assert torch.equal(want[k], grads[k]), (step, k)
         assert torch.equal(eager.bias, graphed.bias), step
+
+
+def test_backward_after_group_limited_routing(moe):
+    """The backward takes the forward's selection as given: after
+    group-limited routing (4 groups, best 2 kept) its gradients match the
+    oracle's on that selection."""
+    cfg = get_config("tiny").with_(**dict(BASE, T=300, d=512, d_ff=256))
+    g = make_inputs(cfg)
+    dh = upstream_grad(cfg, "cpu").to("cuda")
+    S = cfg.n_shared
+    layer = moe.MoELayer(g["E"], g["b"].clone(), g["w_gate"], g["w_up"],
+                         g["w_down"], g["ws_gate"], g["ws_up"], g["ws_down"],
+                         top_k=cfg.top_k, h_dtype=torch.float32, n_groups=4,
+                         topk_groups=2)
+    layer(g["u"])
+    gr = layer.backward(g["u"], dh)
+    torch.cuda.synchronize()
+    moe.get_device_error()
+    b = layer.buffers(cfg.T)
+    idx = b.topk_idx.cpu().numpy()
+    u64, E64, b64 = as_f64(g["u"]), as_f64(g["E"]), as_f64(g["b"])
+    r = om.route(u64, E64, b64, cfg.top_k, groups=(4, 2))
+    check_routing(r, b64, idx, b.counts.cpu().numpy(), cfg.top_k,
+                  groups=(4, 2))
+    routed = lambda e: tuple(as_f64(g[k][e]) for k in
+                             ("w_gate", "w_up", "w_down"))
+    shared = [tuple(as_f64(g[k][s]) for k in ("ws_gate", "ws_up", "ws_down"))
+              for s in range(S)]
+    ref = ob.layer_backward(u64, E64, b64, cfg.top_k, routed, shared,
+                            as_f64(dh), idx_override=idx)
+    grad_close(gr["du"].cpu().numpy(), ref["du"], "du")
+    grad_close(gr["dE"].cpu().numpy(), ref["dE"], "dE")
+    for j, k in enumerate(("dw_gate", "dw_up", "dw_down")):
+        want = np.stack([ref["dW"][e][j] for e in range(cfg.n_routed)])
+        grad_close(gr[k].float().cpu().numpy(), want, k)

@@ -28,17 +28,34 @@ namespace moe {
 
 constexpr int kBwdPairBM = 256;      // M rows per item (128 per CTA)
 constexpr int kBwdPairBN = 256;      // N per item
-constexpr int kBwdPairBK = 128;      // K per stage
-constexpr int kBwdPairStages = 3;
+// Wgrad's store boxes: a ring of this many 2 KB boxes per epilogue warp
+constexpr int kWgradBoxes = 3;
 
+// K per stage and stages: 128 x 3 for the tokens kinds; 64 x 5 for Wgrad,
+// whose epilogue (not its operand stream) is the bound and takes the shared
+// memory freed for a ring of store boxes.
+template <int KIND>
+__host__ __device__ constexpr int bwd_pair_bk() {
+  return KIND == kWgrad ? 64 : 128;
+}
+template <int KIND>
+__host__ __device__ constexpr int bwd_pair_stages() {
+  return KIND == kWgrad ? 5 : 3;
+}
+
+template <int KIND>
 struct BwdPairSmem {
-  static constexpr int a_bytes = 128 * kBwdPairBK * 2;   // 32 KB
-  static constexpr int b_bytes = 128 * kBwdPairBK * 2;   // 32 KB
+  static constexpr int BK = bwd_pair_bk<KIND>();
+  static constexpr int ST = bwd_pair_stages<KIND>();
+  static constexpr int a_bytes = 128 * BK * 2;   // 32 KB (16 KB for Wgrad)
+  static constexpr int b_bytes = 128 * BK * 2;
   static constexpr int a_off = 0;
-  static constexpr int b_off = a_off + kBwdPairStages * a_bytes;
-  static constexpr int stg_off = b_off + kBwdPairStages * b_bytes;
-  static constexpr int bar_off = stg_off + kBwdStgBytes;
-  static constexpr int n_bars = 2 * kBwdPairStages + 5 + 2 * kSchedDepth;
+  static constexpr int b_off = a_off + ST * a_bytes;
+  static constexpr int stg_off = b_off + ST * b_bytes;
+  static constexpr int stg_bytes =
+      KIND == kWgrad ? 8 * kWgradBoxes * 2048 : kBwdStgBytes;
+  static constexpr int bar_off = stg_off + stg_bytes;
+  static constexpr int n_bars = 2 * ST + 5 + 2 * kSchedDepth;
   static constexpr int misc_off = bar_off + n_bars * 8;
   static constexpr int epok_off = misc_off + 16;
   static constexpr int sched_off = epok_off + 32;     // 8 epilogue verdicts
@@ -97,8 +114,8 @@ __device__ __forceinline__ void bwd_ep_wgrad_tma(uint32_t taddr, int cbeg,
                                                  const CUtensorMap* map,
                                                  int n0, int y, int col_split,
                                                  int s_rows, bool bf16,
-                                                 uint32_t buf, int lane) {
-  const uint32_t row_addr = buf + lane * 64;
+                                                 uint32_t ring_base,
+                                                 int& ring, int lane) {
   const int sw = (lane >> 1) & 3;            // 64-byte swizzle of this row
 #pragma unroll 1
   for (int c0 = cbeg; c0 < cbeg + 128; c0 += 32) {
@@ -111,7 +128,11 @@ __device__ __forceinline__ void bwd_ep_wgrad_tma(uint32_t taddr, int cbeg,
       for (int j = 0; j < 32; ++j) r[j] = 0u;
     }
     if (bf16) {            // one box of 32 columns
-      if (lane == 0) bulk_wait_read<0>();
+      const uint32_t buf = ring_base + (ring % kWgradBoxes) * 2048u;
+      const uint32_t row_addr = buf + lane * 64;
+      ++ring;
+      // the box written kWgradBoxes stores ago has been read
+      if (lane == 0) bulk_wait_read<kWgradBoxes - 1>();
       __syncwarp();
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
@@ -129,7 +150,10 @@ __device__ __forceinline__ void bwd_ep_wgrad_tma(uint32_t taddr, int cbeg,
     } else {               // two boxes of 16 columns
 #pragma unroll
       for (int hb = 0; hb < 2; ++hb) {
-        if (lane == 0) bulk_wait_read<0>();
+        const uint32_t buf = ring_base + (ring % kWgradBoxes) * 2048u;
+        const uint32_t row_addr = buf + lane * 64;
+        ++ring;
+        if (lane == 0) bulk_wait_read<kWgradBoxes - 1>();
         __syncwarp();
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc)
@@ -154,6 +178,7 @@ __device__ __forceinline__ BTile bwd_decode_pair(int item, const BwdParams& p,
                                                  const int* offp,
                                                  const int* cnt,
                                                  const int* chunk_pre) {
+  constexpr int BK = bwd_pair_bk<KIND>();
   BTile t;
   if constexpr (KIND == kWgrad) {
     const int ntn_s = p.n_shared / kBwdPairBN;
@@ -166,8 +191,8 @@ __device__ __forceinline__ BTile bwd_decode_pair(int item, const BwdParams& p,
       local = item;
       ntn = ntn_s;
       t.k_row0 = 0;
-      t.nk = (p.shared_rows + kBwdPairBK - 1) / kBwdPairBK;
-      t.krows = t.nk * kBwdPairBK;            // rows past T read as zero
+      t.nk = (p.shared_rows + BK - 1) / BK;
+      t.krows = t.nk * BK;            // rows past T read as zero
     } else {
       const int j = item - n_items_s;
       t.shared = 0;
@@ -176,7 +201,7 @@ __device__ __forceinline__ BTile bwd_decode_pair(int item, const BwdParams& p,
       ntn = ntn_r;
       t.k_row0 = offp[t.e];
       t.krows = (cnt[t.e] + kPadRows - 1) / kPadRows * kPadRows;
-      t.nk = (t.krows + kBwdPairBK - 1) / kBwdPairBK;
+      t.nk = (t.krows + BK - 1) / BK;
     }
     t.wt = local / ntn;
     t.m0 = t.wt * kBwdPairBM;
@@ -192,7 +217,7 @@ __device__ __forceinline__ BTile bwd_decode_pair(int item, const BwdParams& p,
       t.n0 = ch * kBwdPairBN;
       t.n_valid = min(kBwdPairBN, p.shared_rows - t.n0);
       t.k_row0 = 0;
-      t.nk = p.k_shared / kBwdPairBK;
+      t.nk = p.k_shared / BK;
     } else {
       const int wt_r = p.m_routed / kBwdPairBM;
       const int j = item - n_items_s;
@@ -213,11 +238,11 @@ __device__ __forceinline__ BTile bwd_decode_pair(int item, const BwdParams& p,
       t.n0 = offp[e] + ch * sz;
       t.n_valid = min(sz, m - ch * sz);
       t.k_row0 = e * p.k_routed;
-      t.nk = p.k_routed / kBwdPairBK;
+      t.nk = p.k_routed / BK;
     }
     t.m0 = t.wt * kBwdPairBM;
     t.n_mma = (t.n_valid + 15) & ~15;
-    t.krows = t.nk * kBwdPairBK;
+    t.krows = t.nk * BK;
   }
   return t;
 }
@@ -238,8 +263,11 @@ __global__ void __cluster_dims__(2, 1, 1)
 __launch_bounds__(bwd_pair_threads<KIND>(), 1)
 bwd_gemm_pair_kernel(const __grid_constant__ BwdPairMaps maps,
                      const BwdParams p) {
-  using L = BwdPairSmem;
-  constexpr int ST = kBwdPairStages;
+  using L = BwdPairSmem<KIND>;
+  constexpr int ST = L::ST;
+  constexpr int BK = L::BK;
+  // MN-major operand atoms are BK rows x 128 B; K-major ones 128 rows
+  constexpr uint32_t kMnAtom = BK * 128u;
   constexpr bool kTokens = KIND != kWgrad;
   constexpr bool kAmn = KIND != kRecomp;
   constexpr bool kBmn = KIND == kWgrad;
@@ -397,7 +425,7 @@ bwd_gemm_pair_kernel(const __grid_constant__ BwdPairMaps maps,
                          : (box == 64 ? (t.shared ? &maps.b_s64 : &maps.b_r64)
                                       : (t.shared ? &maps.b_s128
                                                   : &maps.b_r128));
-          b_bytes = static_cast<uint32_t>(box) * kBwdPairBK * 2;
+          b_bytes = static_cast<uint32_t>(box) * BK * 2;
         } else {
           mB = t.shared ? &maps.b_s128 : &maps.b_r128;
           b_bytes = L::b_bytes;
@@ -417,7 +445,7 @@ bwd_gemm_pair_kernel(const __grid_constant__ BwdPairMaps maps,
           const uint32_t fb = full_L + 8 * stage;
           const uint32_t adst = sbase + L::a_off + stage * L::a_bytes;
           const uint32_t bdst = sbase + L::b_off + stage * L::b_bytes;
-          const int krow = t.k_row0 + i * kBwdPairBK;
+          const int krow = t.k_row0 + i * BK;
           if constexpr (kAmn)
             tma_load_3d_pair(adst, mA, krow, m_atom, fb);
           else
@@ -493,14 +521,14 @@ bwd_gemm_pair_kernel(const __grid_constant__ BwdPairMaps maps,
           const uint32_t b0 = sbase + L::b_off + stage * L::b_bytes;
           // 16-row K steps in this stage (a Wgrad group's last block may
           // hold 64 rows)
-          const int nkk = min(kBwdPairBK, t.krows - i * kBwdPairBK) / 16;
+          const int nkk = min(BK, t.krows - i * BK) / 16;
 #pragma unroll
-          for (int kk = 0; kk < kBwdPairBK / 16; ++kk) {
+          for (int kk = 0; kk < BK / 16; ++kk) {
             if (kk >= nkk) break;
             const uint32_t at = kk >> 2, w = (kk & 3) * 32;
-            const uint64_t ad = kAmn ? sdesc_mn128(a0 + kk * 2048, 16384)
+            const uint64_t ad = kAmn ? sdesc_mn128(a0 + kk * 2048, kMnAtom)
                                      : sdesc_k128(a0 + at * 16384u + w);
-            const uint64_t bd = kBmn ? sdesc_mn128(b0 + kk * 2048, 16384)
+            const uint64_t bd = kBmn ? sdesc_mn128(b0 + kk * 2048, kMnAtom)
                                      : sdesc_k128(b0 + at * b_atom + w);
             mma_bf16_pair(d_tmem, ad, bd, idesc, (i | kk) != 0);
           }
@@ -529,6 +557,7 @@ bwd_gemm_pair_kernel(const __grid_constant__ BwdPairMaps maps,
     int slot = 0;
     uint32_t sph = 0;
     bool ovf = false;
+    int ring = 0;          // Wgrad: this warp's next store box
     while (true) {
       const bool got = mbar_wait_cl(bar_sfull + 8 * slot, sph, abort_flag,
                                     KID_GEMM_BWD, 107);
@@ -589,7 +618,8 @@ bwd_gemm_pair_kernel(const __grid_constant__ BwdPairMaps maps,
         }
         bwd_ep_wgrad_tma(ta, (ep >> 2) * 128, t.nk == 0, om, t.n0, y,
                          col_split, s_rows, p.out_bf16 != 0,
-                         smem_u32(stg) + ep * 2048u, lane);
+                         smem_u32(stg) + ep * (kWgradBoxes * 2048u), ring,
+                         lane);
       }
       tc_fence_before();
       __syncwarp();

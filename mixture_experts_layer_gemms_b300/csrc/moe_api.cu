@@ -124,12 +124,12 @@ moe_status device_setup(int* sm_count) {
         &clusters, grouped_gemm_pair_kernel, &cfg));
     di.pair_clusters = clusters;
     MOE_CHECK_CUDA(allow_smem(bwd_gemm_pair_kernel<kDgrad>,
-                              BwdPairSmem::alloc));
+                              BwdPairSmem<kDgrad>::alloc));
     MOE_CHECK_CUDA(allow_smem(bwd_gemm_pair_kernel<kRecomp>,
-                              BwdPairSmem::alloc));
+                              BwdPairSmem<kRecomp>::alloc));
     MOE_CHECK_CUDA(allow_smem(bwd_gemm_pair_kernel<kWgrad>,
-                              BwdPairSmem::alloc));
-    cfg.dynamicSmemBytes = BwdPairSmem::alloc;
+                              BwdPairSmem<kWgrad>::alloc));
+    cfg.dynamicSmemBytes = BwdPairSmem<kWgrad>::alloc;
     cfg.blockDim = dim3(bwd_pair_threads<kWgrad>());
     clusters = 0;
     MOE_CHECK_CUDA(cudaOccupancyMaxActiveClusters(
@@ -1365,10 +1365,13 @@ struct Op {
   long long rows, cols;
 };
 moe_status bwd_pair_maps(Op a_r, Op b_r, Op a_s, Op b_s, bool shared,
-                         bool tokens, BwdPairMaps& m) {
+                         bool tokens, BwdPairMaps& m, int kbox = 128) {
+  // kbox: rows per box of the Wgrad operands (its K per stage); the token
+  // kinds' weight boxes are always 128 rows
   moe_status st;
-  if ((st = make_map3(&m.a_r, a_r.p, a_r.rows, a_r.cols, 128, 2))) return st;
-  if ((st = make_map3(&m.b_r128, b_r.p, b_r.rows, b_r.cols, 128, 2)))
+  if ((st = make_map3(&m.a_r, a_r.p, a_r.rows, a_r.cols, kbox, 2))) return st;
+  if ((st = make_map3(&m.b_r128, b_r.p, b_r.rows, b_r.cols,
+                      tokens ? 128 : kbox, 2)))
     return st;
   if (tokens) {
     if ((st = make_map3(&m.b_r32, b_r.p, b_r.rows, b_r.cols, 32, 2))) return st;
@@ -1377,8 +1380,10 @@ moe_status bwd_pair_maps(Op a_r, Op b_r, Op a_s, Op b_s, bool shared,
     m.b_r32 = m.b_r64 = m.b_r128;
   }
   if (shared) {
-    if ((st = make_map3(&m.a_s, a_s.p, a_s.rows, a_s.cols, 128, 2))) return st;
-    if ((st = make_map3(&m.b_s128, b_s.p, b_s.rows, b_s.cols, 128, 2)))
+    if ((st = make_map3(&m.a_s, a_s.p, a_s.rows, a_s.cols, kbox, 2)))
+      return st;
+    if ((st = make_map3(&m.b_s128, b_s.p, b_s.rows, b_s.cols,
+                        tokens ? 128 : kbox, 2)))
       return st;
     if (tokens) {
       if ((st = make_map3(&m.b_s32, b_s.p, b_s.rows, b_s.cols, 32, 2)))
@@ -1430,8 +1435,8 @@ moe_status launch_bwd_pair(const BwdPairMaps& m, const BwdParams& p,
     return fail(MOE_ERR_CUDA, "backward CTA-pair GEMM cannot be resident");
   const long long n = max_items < clusters ? max_items : clusters;
   bwd_gemm_pair_kernel<KIND>
-      <<<static_cast<int>(2 * n), bwd_pair_threads<KIND>(), BwdPairSmem::alloc,
-         cs>>>(m, p);
+      <<<static_cast<int>(2 * n), bwd_pair_threads<KIND>(),
+         BwdPairSmem<KIND>::alloc, cs>>>(m, p);
   MOE_CHECK_LAUNCH();
   return MOE_OK;
 }
@@ -1610,8 +1615,10 @@ moe_status moe_backward(const moe_shape* s, const void* dh, const void* u,
     if ((st = launch_bwd_pair<kDgrad>(m, p, (ti_r + ti_s) * (d / 256), cs)))
       return st;
     // 6. Wgrad (gate/up): dW_gate / dW_up = dA^T X; shared dA_s^T u
+    constexpr int kWbox = bwd_pair_bk<kWgrad>();
     if ((st = bwd_pair_maps({dA, R, 2LL * I}, {X, R, d},
-                            {dA_s, T, 2LL * SI}, {u, T, d}, sh, false, m)))
+                            {dA_s, T, 2LL * SI}, {u, T, d}, sh, false, m,
+                            kWbox)))
       return st;
     p.m_routed = 2 * I;  p.m_shared = 2 * SI;
     p.n_routed = d;      p.n_shared = d;
@@ -1640,7 +1647,7 @@ moe_status moe_backward(const moe_shape* s, const void* dh, const void* u,
       return st;
     // 7. Wgrad (down): dW_down = dY^T H; shared dh^T H_s
     if ((st = bwd_pair_maps({dY, R, d}, {H, R, I}, {dh, T, d}, {H_s, T, SI},
-                            sh, false, m)))
+                            sh, false, m, kWbox)))
       return st;
     p.m_routed = d;   p.m_shared = d;
     p.n_routed = I;   p.n_shared = SI;

@@ -217,16 +217,19 @@ __device__ __forceinline__ void bwd_ep_dgrad(uint32_t taddr, int n_valid,
 //   dA[token][blk + i']   = dH c SiLU'(a)   (gate half)       (bf16)
 //   dA[token][blk+64+i']  = dH SiLU(a)      (up half)         (bf16)
 // with dH read from dH[token][i] (fp16).
+// The warps of one exchange group (four warps, lane quarters 0..3) take
+// the 32-token chunks n0 = c0, c0 + step, ... and synchronise on named
+// barrier `bar` (several groups may split an item's chunks).
 __device__ __forceinline__ void bwd_ep_recomp(
     uint32_t taddr, int n_valid, int b_row, int wt, const __half* dH,
     long long ld_h, __nv_bfloat16* H, __nv_bfloat16* dA, long long ld_a,
-    float* xchg, int q, int lane) {
+    float* xchg, int q, int lane, int c0 = 0, int step = 32, int bar = 1) {
   const bool gate_warp = q < 2;
   const int pair_q = q & 1;
   const int i = wt * 64 + pair_q * 32 + lane;        // column of H / dH
   const int ca = wt * 128 + pair_q * 32 + lane;      // packed column of da
   const int jbase = gate_warp ? 0 : 16;
-  for (int n0 = 0; n0 < n_valid; n0 += 32) {
+  for (int n0 = c0; n0 < n_valid; n0 += step) {
     const int nleft = n_valid - n0;
     // this thread's 16 dH values, loaded before the TMEM read and the
     // exchange so that their latency overlaps them (the H / dA stores
@@ -245,7 +248,7 @@ __device__ __forceinline__ void bwd_ep_recomp(
 #pragma unroll
     for (int j = 0; j < 16; ++j)
       mine[j] = __uint_as_float(r[gate_warp ? 16 + j : j]);
-    named_bar_sync(1, 128);
+    named_bar_sync(bar, 128);
     const float* theirs =
         xchg + (((gate_warp ? q + 2 : q - 2) * 32) + lane) * 17;
 #pragma unroll
@@ -262,7 +265,7 @@ __device__ __forceinline__ void bwd_ep_recomp(
           __float2bfloat16_rn(g * c * (sg * (1.0f + a * (1.0f - sg))));
       dA[row * ld_a + ca + 64] = __float2bfloat16_rn(g * si);
     }
-    named_bar_sync(1, 128);
+    named_bar_sync(bar, 128);
   }
 }
 

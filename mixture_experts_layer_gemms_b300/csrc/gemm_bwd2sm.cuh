@@ -53,7 +53,8 @@ struct BwdPairSmem {
   static constexpr int b_off = a_off + ST * a_bytes;
   static constexpr int stg_off = b_off + ST * b_bytes;
   static constexpr int stg_bytes =
-      KIND == kWgrad ? 8 * kWgradBoxes * 2048 : kBwdStgBytes;
+      KIND == kWgrad ? 8 * kWgradBoxes * 2048
+                     : (KIND == kRecomp ? 2 * 128 * 17 * 4 : kBwdStgBytes);
   static constexpr int bar_off = stg_off + stg_bytes;
   static constexpr int n_bars = 2 * ST + 5 + 2 * kSchedDepth;
   static constexpr int misc_off = bar_off + n_bars * 8;
@@ -248,10 +249,12 @@ __device__ __forceinline__ BTile bwd_decode_pair(int item, const BwdParams& p,
 }
 
 // Threads: producer warp, MMA warp, then 4 epilogue warps (8 for Wgrad,
-// whose epilogue -- 128 x 256 stores per short K loop -- is its bound).
+// whose epilogue -- 128 x 256 stores per short K loop -- is its bound, and
+// for the recompute, whose SwiGLU-backward epilogue reads dH and writes H
+// and dA: two groups of four warps take alternate 32-token chunks).
 template <int KIND>
 __host__ __device__ constexpr int bwd_pair_epi_warps() {
-  return KIND == kWgrad ? 8 : 4;
+  return KIND == kDgrad ? 4 : 8;
 }
 template <int KIND>
 __host__ __device__ constexpr int bwd_pair_threads() {
@@ -591,12 +594,14 @@ bwd_gemm_pair_kernel(const __grid_constant__ BwdPairMaps maps,
         const long long ld = t.shared ? p.ld_s : p.ld_r;
         bwd_ep_dgrad(ta, t.n_valid, t.n0, out, ld, m_cta + q * 32 + lane, ovf);
       } else if constexpr (KIND == kRecomp) {
+        const int grp = ep >> 2;            // exchange group of 4 warps
         bwd_ep_recomp(ta, t.n_valid, t.n0, m_cta / 128,
                       t.shared ? p.dh_s : p.dh_r, t.shared ? p.ld_s : p.ld_r,
                       static_cast<__nv_bfloat16*>(t.shared ? p.out_s : p.out_r),
                       static_cast<__nv_bfloat16*>(t.shared ? p.out2_s
                                                            : p.out2_r),
-                      t.shared ? p.ld2_s : p.ld2_r, stg, q, lane);
+                      t.shared ? p.ld2_s : p.ld2_r, stg + grp * 128 * 17, q,
+                      lane, 32 * grp, 64, 2 + grp);
       } else {
         const int m = m_cta + q * 32;       // the warp's first output row
         const CUtensorMap* om;

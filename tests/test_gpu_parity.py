@@ -480,26 +480,158 @@ def test_layer_deterministic(moe):
 
 
 # ------------------------------------------- full sizes, sampled outputs --
-@pytest.mark.parametrize("name,n_sample", [("v3_prefill", 6),
-                                           ("v3_decode", 8)])
-def test_layer_full_size_sampled(moe, name, n_sample):
-    """The full V3-shaped layer in the benchmark's launch configuration;
-    routing checked on every token, h on a seeded sample of tokens."""
-    cfg = get_config(name)
+def _full_layer(moe, cfg, g, h_dtype=torch.float32):
+    layer = moe.MoELayer(g["E"], g["b"].clone(), g["w_gate"], g["w_up"],
+                         g["w_down"], g["ws_gate"], g["ws_up"], g["ws_down"],
+                         top_k=cfg.top_k, h_dtype=h_dtype)
+    h = layer(g["u"])
+    torch.cuda.synchronize()
+    moe.get_device_error()
+    return layer, h
+
+
+def _check_h_rows(cfg, g, idx, h, rows):
+    """h on the given token rows against the definition, on the GPU's
+    selection (identical to the oracle's away from near-ties)."""
+    routed, shared = oracle_weights(g)
+    b64 = as_f64(g["b"])
+    sel = torch.from_numpy(np.asarray(rows)).to(g["u"].device)
+    u64 = as_f64(g["u"][sel])
+    h_ref, _ = om.layer_forward(u64, as_f64(g["E"]), b64, cfg.top_k, routed,
+                                shared, idx_override=idx[rows])
+    got = h[sel].float().cpu().numpy()
+    return assert_close(got, h_ref, base=u64, what=cfg.name)
+
+
+def test_layer_full_v3_prefill(moe):
+    """The full V3 prefill layer (T = 8192) in the benchmark's launch
+    configuration (CTA-pair grouped GEMM, d = 7168, d_ff = 2048).
+
+    * routing of every token against the oracle;
+    * h on >= 200 tokens: for every expert a seeded token of its LAST
+      token chunk and the token in its last slot (so the last chunk of every
+      expert's items, ragged tails included, reaches the check), plus a
+      seeded sample and the batch's last token;
+    * y_perm element by element on every row of the four most loaded
+      experts (each over 256 tokens, so split into several chunks)."""
+    cfg = get_config("v3_prefill")
     g = generate(cfg, "cuda")
-    t = g   # the oracle widens per expert from the same tensors
-    rng = np.random.default_rng(cfg.seed)
-    sample = np.sort(rng.choice(cfg.T, size=n_sample, replace=False))
-    sample[-1] = cfg.T - 1          # include the ragged end of the batch
-    e, near, layer = _layer_check(moe, cfg, t, g, tokens=sample)
+    layer, h = _full_layer(moe, cfg, g)
     b = layer.buffers(cfg.T)
-    # routing of all tokens
+    idx = b.topk_idx.cpu().numpy()
+    counts = b.counts.cpu().numpy()
+    off = b.offsets.cpu().numpy().astype(np.int64)
+    perm = b.perm.cpu().numpy().astype(np.int64)
     b64 = as_f64(g["b"])
     r = om.route(as_f64(g["u"]), as_f64(g["E"]), b64, cfg.top_k)
-    check_routing(r, b64, b.topk_idx.cpu().numpy(), b.counts.cpu().numpy(),
-                  cfg.top_k)
-    print(name, e, "near-ties", near)
-    del layer, g, t
+    near = check_routing(r, b64, idx, counts, cfg.top_k)
+    # the permutation is the oracle's on the GPU's own selection
+    o_off, o_perm, _ = om.permute(idx, counts)
+    np.testing.assert_array_equal(off, o_off)
+    np.testing.assert_array_equal(perm, o_perm)
+    # the grouped GEMM splits an expert's m rows into ceil(m / 256) chunks of
+    # equal size (rounded up to 16); take a seeded row of every expert's
+    # last chunk, and the expert's very last row (the ragged tail)
+    rng = np.random.default_rng(cfg.seed)
+    pick = []
+    for e in range(cfg.n_routed):
+        m = int(counts[e])
+        if m == 0:
+            continue
+        ce = -(-m // 256)
+        sz = (-(-m // ce) + 15) // 16 * 16
+        lo = int(off[e]) + (ce - 1) * sz
+        pick += [perm[rng.integers(lo, int(off[e + 1]))], perm[off[e + 1] - 1]]
+    rows = np.unique(np.concatenate([pick, rng.choice(cfg.T, 32, False),
+                                     [cfg.T - 1]]))
+    assert rows.size >= 200, rows.size
+    e_h = _check_h_rows(cfg, g, idx, h, rows)
+    # y_perm of multi-chunk experts, every row
+    big = np.argsort(-counts, kind="stable")[:4]
+    assert counts[big].min() > 256, counts[big]
+    y = b.y_perm
+    errs = []
+    for e in big.tolist():
+        lo, hi = int(off[e]), int(off[e + 1])
+        x = as_f64(g["u"][torch.from_numpy(perm[lo:hi]).cuda()])
+        w = tuple(as_f64(g[k][e]) for k in ("w_gate", "w_up", "w_down"))
+        ref = om.swiglu_ffn(x, *w)
+        errs.append(assert_close(y[lo:hi].float().cpu().numpy(), ref,
+                                 what=f"y_perm expert {e} ({hi - lo} rows)"))
+    print("v3_prefill h", rows.size, "tokens", e_h, "near-ties", near,
+          "y_perm", errs)
+    del layer, g, h
+    torch.cuda.empty_cache()
+
+
+def test_layer_full_v3_decode(moe):
+    """The full V3 decode layer (T = 128, the weight-streaming kernel):
+    routing and h of every token against the oracle."""
+    cfg = get_config("v3_decode")
+    g = generate(cfg, "cuda")
+    layer, h = _full_layer(moe, cfg, g)
+    b = layer.buffers(cfg.T)
+    idx = b.topk_idx.cpu().numpy()
+    b64 = as_f64(g["b"])
+    r = om.route(as_f64(g["u"]), as_f64(g["E"]), b64, cfg.top_k)
+    near = check_routing(r, b64, idx, b.counts.cpu().numpy(), cfg.top_k)
+    e = _check_h_rows(cfg, g, idx, h, np.arange(cfg.T))
+    print("v3_decode", e, "near-ties", near)
+    del layer, g, h
+    torch.cuda.empty_cache()
+
+
+def test_bias_loop_full_size_teacher_forced(moe):
+    """The skewed-load bias loop at its full size, as the benchmark runs it:
+    T = 16384 tokens per step, 50 steps, V3 dimensions, Zipf-scaled
+    centroids, gamma = 1e-3, the whole layer every step (bf16 h) followed by
+    the bias update.  At T = 16384 the router runs one CTA per 128-token
+    tile (the unsplit path: 128 tiles already fill most of the SMs).
+
+    Teacher-forced: every step's routing is compared on every token with
+    the oracle given the GPU's incoming bias, and the bias after the step
+    bit for bit with the oracle's update applied to the GPU's counts (so one
+    near-tied token cannot fork the trajectory).  h is compared with the
+    definition on sampled tokens of the first and the last step."""
+    cfg = get_config("skew")
+    g = generate(cfg, "cuda")
+    layer = moe.MoELayer(g["E"], g["b"].clone(), g["w_gate"], g["w_up"],
+                         g["w_down"], g["ws_gate"], g["ws_up"], g["ws_down"],
+                         top_k=cfg.top_k, h_dtype=torch.bfloat16)
+    b = layer.buffers(cfg.T)
+    E64 = as_f64(g["E"])
+    TK = cfg.T * cfg.top_k
+    rng = np.random.default_rng(cfg.seed)
+    mm, nears = [], []
+    for step in range(cfg.steps):
+        u = step_tokens(cfg, step, "cuda")
+        b_in = layer.bias.cpu().numpy().copy()
+        h = layer(u, update_bias=True, gamma=cfg.gamma)
+        torch.cuda.synchronize()
+        moe.get_device_error()
+        idx = b.topk_idx.cpu().numpy()
+        c = b.counts.cpu().numpy()
+        r = om.route(as_f64(u), E64, b_in.astype(np.float64), cfg.top_k)
+        nears.append(check_routing(r, b_in.astype(np.float64), idx, c,
+                                   cfg.top_k))
+        want = om.update_bias(b_in, c, TK, cfg.gamma)
+        assert layer.bias.cpu().numpy().tobytes() == want.tobytes(), step
+        mm.append(c.max() / (TK / cfg.n_routed))
+        if step in (0, cfg.steps - 1):
+            rows = np.sort(rng.choice(cfg.T, 4, replace=False))
+            sel = torch.from_numpy(rows).cuda()
+            routed, shared = oracle_weights(g)
+            u64 = as_f64(u[sel])
+            h_ref, _ = om.layer_forward(u64, E64, b_in.astype(np.float64),
+                                        cfg.top_k, routed, shared,
+                                        idx_override=idx[rows])
+            got = h[sel].float().cpu().numpy()
+            assert np.all(np.abs(got - h_ref) <= 2e-2 + half_ulp_bf16(h_ref))
+    # the loop moves the load towards balance
+    assert mm[-1] < mm[0], (mm[0], mm[-1])
+    print("skew max/mean load", round(mm[0], 3), "->", round(mm[-1], 3),
+          "near-ties per step", nears)
+    del layer, g
     torch.cuda.empty_cache()
 
 

@@ -302,6 +302,14 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t cluster_addr) {
                : "memory");
   return v;
 }
+__device__ __forceinline__ float4 ld_cluster_v4(uint32_t cluster_addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(cluster_addr)
+               : "memory");
+  return v;
+}
 // try_wait with cluster-scope acquire: for barriers that the peer CTA (or
 // its tensor core) arrives on.
 __device__ __forceinline__ bool mbar_try_wait_cl(uint32_t bar, uint32_t parity) {

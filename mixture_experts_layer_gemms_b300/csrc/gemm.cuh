@@ -48,7 +48,7 @@ struct GemmParams {
   int shared_rows;      // tokens of the shared group (0: none)
   int w_rows_shared;    // weight rows of the shared group
   int k_shared;         // reduction length of the shared pass
-  void* out_routed;     // swiglu: H bf16; else: Y fp32
+  void* out_routed;     // swiglu: H bf16; else: Y (fp16 for bf16 layers, fp32 for fp32)
   long long ld_routed;
   void* out_shared;
   long long ld_shared;

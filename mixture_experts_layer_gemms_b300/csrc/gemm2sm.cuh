@@ -3,9 +3,9 @@
 // selected expert and FFN^(s) of every shared expert, as in gemm.cuh.)
 //
 // Same work as grouped_gemm_kernel (weights on M, tokens on N, fused SwiGLU
-// or fp32 down epilogue, shared group first, item table from the device
-// offsets, dynamic claim order), but each item is a 256-row weight tile x up
-// to 256 tokens computed by a cluster of two CTAs on two SMs:
+// or down epilogue with fp16 Y, shared group first, item table from the
+// device offsets, dynamic claim order), but each item is a 256-row weight
+// tile x up to 256 tokens computed by a cluster of two CTAs on two SMs:
 //
 //   CTA r (r = 0, 1) holds weight rows a_row + 128 r .. +128 (its half of
 //   A) and token rows b_row + r N/2 .. + N/2 (its half of B) in its own
@@ -59,6 +59,13 @@ struct PairSmem {
   static_assert(alloc <= 227 * 1024, "shared memory");
 };
 
+// Rows of the TMA box that loads a CTA's token half-tile of `half` rows:
+// the smallest of 32, 64, 96, 128 that covers it.  Each K-atom of the box
+// is box * 128 bytes, a multiple of the 1024-byte swizzle-atom alignment.
+__host__ __device__ __forceinline__ int pair_token_box(int half) {
+  return half <= 32 ? 32 : (half <= 64 ? 64 : (half <= 96 ? 96 : 128));
+}
+
 // Item -> (pair weight tile, token chunk); chunk index fastest.
 __device__ __forceinline__ Tile decode_pair_item(int item, const GemmParams& p,
                                                  int n_items_s, int nch_s,
@@ -109,6 +116,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA_r,
                          const __grid_constant__ CUtensorMap tmB_s,
                          const __grid_constant__ CUtensorMap tmB_r64,
                          const __grid_constant__ CUtensorMap tmB_s64,
+                         const __grid_constant__ CUtensorMap tmB_r96,
+                         const __grid_constant__ CUtensorMap tmB_s96,
                          const __grid_constant__ CUtensorMap tmB_r128,
                          const __grid_constant__ CUtensorMap tmB_s128,
                          const GemmParams p) {
@@ -258,16 +267,17 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA_r,
         const Tile t = decode_pair_item(item, p, n_items_s, nch_s, off_s,
                                         chunk_pre);
         const CUtensorMap* mA = t.shared ? &tmA_s : &tmA_r;
-        // The CTA's token half-tile comes in ONE TMA box of 32, 64 or 128
-        // rows (the smallest that covers it; rows past the half are loaded
-        // and ignored): the TMA instruction count per stage, not the bytes,
-        // is what costs here.
+        // The CTA's token half-tile comes in ONE TMA box of 32, 64, 96 or
+        // 128 rows (the smallest that covers it; rows past the half are
+        // loaded and ignored): one TMA instruction per operand and stage,
+        // and no more token bytes than the next multiple of 32 rows.
         const int half = t.n_mma >> 1;                 // token rows per CTA
-        const int box = half <= 32 ? 32 : (half <= 64 ? 64 : 128);
+        const int box = pair_token_box(half);
         const CUtensorMap* mB =
-            box == 32 ? (t.shared ? &tmB_s : &tmB_r)
-                      : (box == 64 ? (t.shared ? &tmB_s64 : &tmB_r64)
-                                   : (t.shared ? &tmB_s128 : &tmB_r128));
+            box == 32    ? (t.shared ? &tmB_s : &tmB_r)
+            : box == 64  ? (t.shared ? &tmB_s64 : &tmB_r64)
+            : box == 96  ? (t.shared ? &tmB_s96 : &tmB_r96)
+                         : (t.shared ? &tmB_s128 : &tmB_r128);
         const int a_row = t.a_row + static_cast<int>(rank) * 128;
         const int b_row = t.b_row + static_cast<int>(rank) * half;
         const uint32_t pair_bytes = 2u * (L::a_bytes + box * kPairBK * 2);
@@ -339,7 +349,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA_r,
         // token box rows of this item (the K-atom stride of its B stage)
         const int half = t.n_mma >> 1;
         const uint32_t b_atom =
-            (half <= 32 ? 32u : (half <= 64 ? 64u : 128u)) * 128u;
+            static_cast<uint32_t>(pair_token_box(half)) * 128u;
         bool ok = true;
         for (int i = 0; i < nk; ++i) {
           if (!mbar_wait(bar_full + 8 * stage, phase, abort_flag, KID_GEMM,

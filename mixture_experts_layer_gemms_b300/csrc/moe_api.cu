@@ -371,7 +371,8 @@ moe_status launch_gemm(const CUtensorMap& a_r, const CUtensorMap& b_r,
 // Tensor maps of the CTA-pair GEMM: 3-D views (two K-atoms per box) of the
 // weights (128-row boxes) and tokens (32/64/128-row boxes), routed/shared.
 struct PairMaps {
-  CUtensorMap a_r, a_s, b_r32, b_s32, b_r64, b_s64, b_r128, b_s128;
+  CUtensorMap a_r, a_s, b_r32, b_s32, b_r64, b_s64, b_r96, b_s96, b_r128,
+      b_s128;
 };
 
 // k_r / k_s: reduction length (row length) of the routed / shared operands.
@@ -387,6 +388,8 @@ moe_status pair_maps(const void* w_r, long long w_r_rows, const void* x_r,
     return st;
   if ((st = make_map3(&m.b_r64, x_r, x_r_rows, k_r, 64, at)) != MOE_OK)
     return st;
+  if ((st = make_map3(&m.b_r96, x_r, x_r_rows, k_r, 96, at)) != MOE_OK)
+    return st;
   if ((st = make_map3(&m.b_r128, x_r, x_r_rows, k_r, 128, at)) != MOE_OK)
     return st;
   if (w_s != nullptr) {
@@ -396,12 +399,15 @@ moe_status pair_maps(const void* w_r, long long w_r_rows, const void* x_r,
       return st;
     if ((st = make_map3(&m.b_s64, x_s, x_s_rows, k_s, 64, at)) != MOE_OK)
       return st;
+    if ((st = make_map3(&m.b_s96, x_s, x_s_rows, k_s, 96, at)) != MOE_OK)
+      return st;
     if ((st = make_map3(&m.b_s128, x_s, x_s_rows, k_s, 128, at)) != MOE_OK)
       return st;
   } else {
     m.a_s = m.a_r;
     m.b_s32 = m.b_r32;
     m.b_s64 = m.b_r64;
+    m.b_s96 = m.b_r96;
     m.b_s128 = m.b_r128;
   }
   return MOE_OK;
@@ -468,7 +474,8 @@ moe_status launch_gemm_pair(const PairMaps& m, const GemmParams& p,
   const long long n = items < clusters ? items : clusters;
   grouped_gemm_pair_kernel<<<static_cast<int>(2 * n), 192, PairSmem::alloc,
                              cs>>>(m.a_r, m.b_r32, m.a_s, m.b_s32, m.b_r64,
-                                   m.b_s64, m.b_r128, m.b_s128, p);
+                                   m.b_s64, m.b_r96, m.b_s96, m.b_r128,
+                                   m.b_s128, p);
   MOE_CHECK_LAUNCH();
   return MOE_OK;
 }

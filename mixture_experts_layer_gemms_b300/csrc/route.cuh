@@ -51,26 +51,40 @@ __device__ __forceinline__ unsigned long long warp_group_mask(
   return (static_cast<unsigned long long>(hi) << 32) | lo;
 }
 
+// Order-preserving map of a biased score to an unsigned key: a larger score
+// gives a larger key, -0 is folded onto +0 (they compare equal as floats),
+// and NaN maps to 0, below every real score, so it is never selected.
+// Keys at or below kKeyNegInf (-inf) are not candidates.
+constexpr uint32_t kKeyNegInf = 0x007FFFFFu;
+__device__ __forceinline__ uint32_t score_key(float b) {
+  uint32_t u = __float_as_uint(b);
+  if (u == 0x80000000u) u = 0u;
+  if (b != b) return 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
 // Biased top-K of one token by one warp ("【推理llm論文精讀】DeepSeek V3
 // 技術論文", section 2.2: selection over s + b, gate = s).  s[e] (e < N <=
 // 32 PER) are the token's affinities in shared memory; lane j holds experts
-// j, j + 32, ... (conflict-free reads).  K rounds: every lane offers its best
-// remaining candidate, a butterfly max in the order (beta desc, index asc)
-// gives every lane the winner, and its owner retires it -- so the result is
-// sorted and the lowest index wins ties.  With M < G only experts of the
-// token's M best groups compete.  Lanes 0..K-1 write the winners of rounds
-// 0..K-1 and count them in the CTA histogram.  A round without a finite
-// candidate (only with non-finite inputs) writes expert -1 and reports it.
+// j, j + 32, ... (conflict-free reads) as score keys.  K rounds: every lane
+// offers its best remaining candidate (highest key, lowest index among
+// equal keys), a warp max-reduction (redux.sync) finds the highest key and a
+// min-reduction the lowest expert index holding it, and the owner retires
+// that expert -- so the result is sorted by (s + b desc, index asc) and the
+// lowest index wins ties.  With M < G only experts of the token's M best
+// groups compete.  Lanes 0..K-1 write the winners of rounds 0..K-1 and count
+// them in the CTA histogram.  A round without a finite candidate (only with
+// non-finite inputs) writes expert -1 and reports it.
 template <int PER>
 __device__ __forceinline__ void warp_select(const float* s, const float* bias,
                                             int N, int K, int G, int M, int t,
                                             int lane, int* topk_idx,
                                             float* topk_gate, int* hist) {
-  float beta[PER];
+  uint32_t key[PER];
 #pragma unroll
   for (int i = 0; i < PER; ++i) {
     const int e = lane + 32 * i;
-    beta[i] = e < N ? __fadd_rn(s[e], bias[e]) : -INFINITY;
+    key[i] = e < N ? score_key(__fadd_rn(s[e], bias[e])) : kKeyNegInf;
   }
   if (M < G) {
     const unsigned long long keep = warp_group_mask(s, bias, N, G, M, lane);
@@ -78,32 +92,28 @@ __device__ __forceinline__ void warp_select(const float* s, const float* bias,
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
       const int e = lane + 32 * i;
-      if (e < N && !((keep >> (e / per)) & 1ull)) beta[i] = -INFINITY;
+      if (e < N && !((keep >> (e / per)) & 1ull)) key[i] = kKeyNegInf;
     }
   }
   int mine = -1;
   for (int k = 0; k < K; ++k) {
-    float bb = -INFINITY;
-    int bi = 0x7fffffff;
+    uint32_t bk = 0u;
+    int bi = 0;
 #pragma unroll
     for (int i = 0; i < PER; ++i)       // ascending index: '>' keeps the lowest
-      if (beta[i] > bb) {
-        bb = beta[i];
-        bi = lane + 32 * i;
+      if (key[i] > bk) {
+        bk = key[i];
+        bi = i;
       }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ob = __shfl_xor_sync(0xffffffffu, bb, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (ranks_above(ob, oi, bb, bi)) {
-        bb = ob;
-        bi = oi;
-      }
-    }
-    if (lane == k) mine = bi;
+    const uint32_t top = __reduce_max_sync(0xffffffffu, bk);
+    const uint32_t cand = (bk == top && top > kKeyNegInf)
+                              ? static_cast<uint32_t>(lane + 32 * bi)
+                              : 0xffffffffu;
+    const int win = static_cast<int>(__reduce_min_sync(0xffffffffu, cand));
+    if (lane == k) mine = win;          // -1 when no candidate was left
 #pragma unroll
     for (int i = 0; i < PER; ++i)
-      if (lane + 32 * i == bi) beta[i] = -INFINITY;
+      if (lane + 32 * i == win) key[i] = 0u;
   }
   if (lane < K) {
     int e = mine;
@@ -154,12 +164,20 @@ struct RouteTcSmemLayout {
   static constexpr int a_off = 0;
   static constexpr int b_off = a_off + kRtStages * a_bytes;
   static constexpr int ring_end = b_off + kRtStages * b_bytes_max;
-  // split epilogue, over the freed ring: partial z [128][N+1] fp32, then
-  // the affinities of this CTA's token slice [128/S][N+1] (S >= 2)
+  // epilogue, over the freed ring: z [128][P] fp32 (affinities when S = 1,
+  // this CTA's partial when S > 1), then the affinities of this CTA's token
+  // slice [128/S][P] (S >= 2); P = row_stride(N)
+  static constexpr int kMaxP = 260;
   static constexpr int zpart_off = 0;
-  static constexpr int zpart_bytes = kRouteTile * 257 * 4;
+  static constexpr int zpart_bytes = kRouteTile * kMaxP * 4;
   static constexpr int slice_off = zpart_off + zpart_bytes;
-  static constexpr int slice_end = slice_off + (kRouteTile / 2) * 257 * 4;
+  static constexpr int slice_end = slice_off + (kRouteTile / 2) * kMaxP * 4;
+  // Row stride (floats) of the epilogue's score rows: a multiple of 4 above
+  // N, so rows start on 16-byte boundaries (vector stores and loads) and the
+  // 16-byte stores of 8 consecutive rows cover all 32 banks.
+  __host__ __device__ static constexpr int row_stride(int n) {
+    return (n + 4) & ~3;
+  }
   static constexpr int bar_off =
       ((ring_end > slice_end ? ring_end : slice_end) + 15) & ~15;
   static constexpr int misc_off = bar_off + (2 * kRtStages + 1) * 8;
@@ -278,17 +296,18 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tm_u,
   // Epilogue.  Warp w reads TMEM lane quarter w % 4 (32 token rows, one per
   // lane) and every fourth 32-column chunk from chunk w / 4, and stores z
   // summed over the accumulators to shared memory (the pipeline buffers are
-  // free by now), row-major with a padded stride so a warp's stores hit
-  // distinct banks: as affinities s = sigmoid(z) when S = 1, as the raw
-  // partial when S > 1.  Then one warp per token selects (warp_select).
+  // free by now), row-major with stride P in 16-byte vectors: as affinities
+  // s = sigmoid(z) when S = 1, as the raw partial when S > 1.  Then one warp
+  // per token selects (warp_select).
   const bool done_ok = mbar_wait(bar_done, 0, abort_flag, KID_ROUTE_TC, 3);
   tc_fence_after();
   const bool go = __all_sync(0xffffffffu, done_ok && !*abort_flag);
   constexpr int kWarps = kRouteThreads / 32;
+  const int P = L::row_stride(N);
   {
     const int q = warp & 3;
     const int row = q * 32 + lane;
-    float* srow = reinterpret_cast<float*>(smem) + row * (N + 1);
+    float* srow = reinterpret_cast<float*>(smem) + row * P;
     if (go) {
       const int used = min(n_acc, nk);
       for (int c0 = (warp >> 2) * 32; c0 < N; c0 += 32 * (kWarps / 4)) {
@@ -305,9 +324,15 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tm_u,
 #pragma unroll
           for (int j = 0; j < 32; ++j) z[j] += __uint_as_float(r[j]);
         }
+        if (S == 1) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (c0 + j < N) srow[c0 + j] = S == 1 ? sigmoid_f32(z[j]) : z[j];
+          for (int j = 0; j < 32; ++j) z[j] = sigmoid_f32(z[j]);
+        }
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+          if (c0 + j < N)
+            *reinterpret_cast<float4*>(srow + c0 + j) =
+                make_float4(z[j], z[j + 1], z[j + 2], z[j + 3]);
       }
     }
   }
@@ -317,7 +342,7 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tm_u,
     for (int r = warp; r < kRouteTile; r += kWarps) {
       const int t = tile * kRouteTile + r;
       if (go && t < T)
-        warp_select<8>(sfull + r * (N + 1), bias_s, N, K, G, M, t, lane,
+        warp_select<8>(sfull + r * P, bias_s, N, K, G, M, t, lane,
                        topk_idx, topk_gate, hist);
     }
   } else {
@@ -328,30 +353,60 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tm_u,
     const int r0 = rank * R;
     float* slice = reinterpret_cast<float*>(smem + L::slice_off);
     if (go) {
-      // z = the S partials summed in rank order; the loads of one element
-      // are all issued before they are added
+      // z = the S partials summed in rank order, four experts per 16-byte
+      // vector: the own partial from local shared memory, the others
+      // through distributed shared memory.  Each thread takes four vectors
+      // at a time and issues all four loads of a rank before adding them.
       const uint32_t zbase = sbase + L::zpart_off;
-      for (int i = threadIdx.x; i < R * N; i += blockDim.x) {
-        const int rl = i / N, c = i - rl * N;
-        const uint32_t off =
-            static_cast<uint32_t>(((r0 + rl) * (N + 1) + c) * 4);
-        float v[kRtMaxSplit];
+      const float* zloc = reinterpret_cast<const float*>(smem + L::zpart_off);
+      const int n4 = (N + 3) >> 2;
+      const int items = R * n4;
+      const int nthr = static_cast<int>(blockDim.x);
+      for (int i0 = threadIdx.x; i0 < items; i0 += 4 * nthr) {
+        float4 acc[4], x[4];
+        int w[4];
 #pragma unroll
-        for (int q = 0; q < kRtMaxSplit; ++q)
-          if (q < S) v[q] = ld_cluster_f32(mapa_shared(zbase + off, q));
-        float z = v[0];
+        for (int u = 0; u < 4; ++u) {
+          const int i = min(i0 + u * nthr, items - 1);
+          const int rl = i / n4;
+          w[u] = (r0 + rl) * P + (i - rl * n4) * 4;
+        }
+        for (int q = 0; q < S; ++q) {
 #pragma unroll
-        for (int q = 1; q < kRtMaxSplit; ++q)
-          if (q < S) z += v[q];
-        slice[rl * (N + 1) + c] = sigmoid_f32(z);
+          for (int u = 0; u < 4; ++u)
+            x[u] = q == rank
+                       ? *reinterpret_cast<const float4*>(zloc + w[u])
+                       : ld_cluster_v4(mapa_shared(zbase + 4u * w[u], q));
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            if (q == 0) {
+              acc[u] = x[u];
+            } else {
+              acc[u].x = __fadd_rn(acc[u].x, x[u].x);
+              acc[u].y = __fadd_rn(acc[u].y, x[u].y);
+              acc[u].z = __fadd_rn(acc[u].z, x[u].z);
+              acc[u].w = __fadd_rn(acc[u].w, x[u].w);
+            }
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = i0 + u * nthr;
+          if (i < items) {
+            const int rl = i / n4;
+            *reinterpret_cast<float4*>(slice + rl * P + (i - rl * n4) * 4) =
+                make_float4(sigmoid_f32(acc[u].x), sigmoid_f32(acc[u].y),
+                            sigmoid_f32(acc[u].z), sigmoid_f32(acc[u].w));
+          }
+        }
       }
     }
     __syncthreads();
     for (int r = warp; r < R; r += kWarps) {
       const int t = tile * kRouteTile + r0 + r;
       if (go && t < T)
-        warp_select<8>(slice + r * (N + 1), bias_s, N, K, G, M, t, lane,
-                       topk_idx, topk_gate, hist);
+        warp_select<8>(slice + r * P, bias_s, N, K, G, M, t, lane, topk_idx,
+                       topk_gate, hist);
     }
     cluster_sync();                     // no CTA leaves while read remotely
   }

@@ -462,7 +462,7 @@ def ffn_roofline(cfg, counts, ffn_ms, peaks, traffic_key):
                 "unit": "TFLOP/s", "frac": ach / tc_peak,
                 "traffic": traffic,
                 "algorithmic_bytes": alg_bytes,
-                "kernel": ("grouped_gemm_fp8_tm_kernel" if fp8 else
+                "kernel": ("grouped_gemm_fp8_pair_kernel" if fp8 else
                            "grouped_gemm_pair_kernel") +
                           " (gate/up + down launches of one expert-FFN call)",
                 "peak_source": (f"{peaks['source']} bf16_tflops (burst)"

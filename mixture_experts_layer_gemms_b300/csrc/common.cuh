@@ -363,6 +363,42 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst,
       : "memory");
 }
 
+// 2-D tiled load by one CTA of a pair, completion counted on an mbarrier that
+// may live in the peer CTA (cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst,
+                                                 const CUtensorMap* m, int x,
+                                                 int y, uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::"
+      "complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(x), "r"(y)
+      : "memory");
+}
+
+// 4-D tiled load by one CTA of a pair (completion on a possibly remote
+// mbarrier).
+__device__ __forceinline__ void tma_load_4d_pair(uint32_t dst,
+                                                 const CUtensorMap* m, int x,
+                                                 int y, int z, int w,
+                                                 uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::"
+      "complete_tx::bytes [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(x), "r"(y),
+      "r"(z), "r"(w)
+      : "memory");
+}
+// Contiguous global -> shared bulk copy into this CTA, completion counted on
+// one of its own mbarriers; address and size multiples of 16 bytes.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src,
+                                          uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 // TMEM allocation shared by a CTA pair: one warp of each CTA executes it.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem,
                                                 uint32_t ncols) {
@@ -407,6 +443,74 @@ __device__ __forceinline__ void mma_commit_pair_mc(uint32_t bar,
       "multicast::cluster.b64 [%0], %1;" ::"r"(bar),
       "h"(mask)
       : "memory");
+}
+
+// 4-byte asynchronous copy global -> shared (completion: cp.async groups or
+// an mbarrier arrival below).
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst),
+               "l"(src)
+               : "memory");
+}
+// Arrive on a CTA-local mbarrier once every cp.async this thread issued so
+// far has landed (the barrier's count includes this arrival).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+
+// ---------------------------------------------- block-scaled e4m3 MMA --
+// tcgen05.mma kind::mxf8f6f4 with block scaling (scale_vec::1X): every 32
+// elements of the reduction carry one UE8M0 scale (an 8-bit biased power of
+// two) per row of A and per row of B, read from TMEM.  Issued by the even
+// CTA of a pair: M = 256 (128 rows of A in each CTA), N rows of B split N/2
+// per CTA, both e4m3 and K-major, fp32 accumulation.
+//
+// Scale layout in TMEM (one 32-bit column holds four scale bytes; the
+// instruction descriptor's scale-id fields pick the byte):
+//   A row m of CTA r: that CTA's TMEM, lane m % 128, column sfa + (m % 128)/32;
+//   B row n (0 <= n < N): in EVERY lane quarter q of BOTH CTAs, lane
+//   32 q + n % 32, column sfb + n / 32.
+__host__ __device__ constexpr uint32_t idesc_mxf8_pair(int N, int sf_id) {
+  return (static_cast<uint32_t>(sf_id & 3) << 4)     // B scale byte
+         | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+         | (1u << 23)                                // scales are UE8M0
+         | (static_cast<uint32_t>(256 >> 4) << 24)   // M / 16
+         | (static_cast<uint32_t>(sf_id & 3) << 29); // A scale byte
+}
+__device__ __forceinline__ void mma_mxf8_pair(uint32_t d_tmem, uint64_t a_desc,
+                                              uint64_t b_desc, uint32_t idesc,
+                                              uint32_t sfa_tmem,
+                                              uint32_t sfb_tmem,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X "
+      "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem),
+      "r"(accumulate)
+      : "memory");
+}
+// Register -> TMEM stores of the warp's lane quarter: thread i writes lane
+// (quarter base + i), columns [col, col + n).
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr),
+               "r"(v)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr,
+                                         const uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, "
+      "%7, %8};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
+      "r"(r[6]), "r"(r[7])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // ----------------------------------------------------------------- misc --

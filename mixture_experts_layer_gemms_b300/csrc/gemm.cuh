@@ -143,7 +143,8 @@ __device__ __forceinline__ void epilogue_store(uint32_t taddr, int n_valid,
                                                long long ld, int col0,
                                                bool swiglu, float* xchg, int q,
                                                int ep, int lane,
-                                               bool y_fp16 = false) {
+                                               bool y_fp16 = false,
+                                               bool h_fp32 = false) {
   (void)ep;
   bool overflow = false;
   for (int n0 = 0; n0 < n_valid; n0 += 32) {
@@ -183,15 +184,25 @@ __device__ __forceinline__ void epilogue_store(uint32_t taddr, int n_valid,
     named_bar_sync(1, 128);
     const float* theirs = xchg + (((gate_warp ? q + 2 : q - 2) * 32) + lane) * 17;
     const int jbase = gate_warp ? 0 : 16;
-    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(out) +
-                         static_cast<size_t>(b_row + n0 + jbase) * ld + col0 +
-                         pair_q * 32 + lane;
+    const size_t o = static_cast<size_t>(b_row + n0 + jbase) * ld + col0 +
+                     pair_q * 32 + lane;
+    if (h_fp32) {   // fp32 H (requantized to e4m3 by the caller)
+      float* dst = static_cast<float*>(out) + o;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const float g = gate_warp ? __uint_as_float(r[j]) : theirs[j];
-      const float u = gate_warp ? theirs[j] : __uint_as_float(r[16 + j]);
-      if (jbase + j < nleft)
-        dst[static_cast<size_t>(j) * ld] = __float2bfloat16_rn(silu_f32(g) * u);
+      for (int j = 0; j < 16; ++j) {
+        const float g = gate_warp ? __uint_as_float(r[j]) : theirs[j];
+        const float u = gate_warp ? theirs[j] : __uint_as_float(r[16 + j]);
+        if (jbase + j < nleft) dst[static_cast<size_t>(j) * ld] = silu_f32(g) * u;
+      }
+    } else {
+      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(out) + o;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float g = gate_warp ? __uint_as_float(r[j]) : theirs[j];
+        const float u = gate_warp ? theirs[j] : __uint_as_float(r[16 + j]);
+        if (jbase + j < nleft)
+          dst[static_cast<size_t>(j) * ld] = __float2bfloat16_rn(silu_f32(g) * u);
+      }
     }
     named_bar_sync(1, 128);
   }

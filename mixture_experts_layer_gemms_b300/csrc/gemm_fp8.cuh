@@ -553,469 +553,4 @@ grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA_r,
   }
 }
 
-// ---------------------------------------------------------------------------
-// Prefill-sized groups: tokens on the MMA's M side (128 per item), weights on
-// N (256 packed rows per item: gate/up = the 128 gate and 128 up rows of 128
-// intermediate indices; down = 256 output channels).  A TMEM lane is then a
-// token, so the promotion of a 128-wide block multiplies a thread's whole
-// partial row by one scalar (weight-block scale x the token's scale): no
-// per-column scale traffic, one FFMA per element.  One M=128 x N=256 MMA per
-// K-step of 32.  16 epilogue warps: warp w reads lane quarter w % 4 and
-// column group (w-2)/4; for gate/up a column group holds 32 gate and the 32
-// up columns of the same intermediate indices, for down 64 channels.
-constexpr int kTmTok = 128;    // tokens per item (MMA M)
-constexpr int kTmRows = 256;   // packed weight rows per item (MMA N)
-constexpr int kTmCG = 4;       // epilogue column groups
-constexpr int kTmNW = 4 * kTmCG;
-
-template <int STAGES>
-struct Fp8TmSmem {
-  static constexpr int a_bytes = kTmTok * kQBlock;     // tokens, 16 KB
-  static constexpr int b_bytes = kTmRows * kQBlock;    // weights, 32 KB
-  static constexpr int a_off = 0;
-  static constexpr int b_off = a_off + STAGES * a_bytes;
-  static constexpr int amax_off = b_off + STAGES * b_bytes;   // [CG][128]
-  static constexpr int bar_off = amax_off + kTmCG * kTmTok * 4;
-  static constexpr int n_bars = 2 * STAGES + 4 + 1 + 2 * kSchedDepth;
-  static constexpr int misc_off = bar_off + n_bars * 8;
-  static constexpr int epok_off = misc_off + 16;
-  static constexpr int sched_off = epok_off + 4 * kTmNW;
-  static constexpr int tab_off = sched_off + 4 * kSchedDepth;
-  static constexpr int total = tab_off + 2 * (kMaxGroups + 1) * 4;
-  static constexpr int alloc = total + 1024;
-  static constexpr int tmem_cols = 512;                  // 2 partials x 256
-  static constexpr int threads = 64 + 32 * kTmNW;
-  static_assert(alloc <= 227 * 1024, "shared memory");
-};
-
-__device__ __forceinline__ Tile decode_item_tm(int item, const Fp8Params& p,
-                                               int n_items_s, int nch_s,
-                                               const int* off_s,
-                                               const int* chunk_pre) {
-  Tile t;
-  if (item < n_items_s) {
-    const int wt = item / nch_s, ch = item % nch_s;
-    t.shared = 1;
-    t.wt = wt;
-    t.a_row = wt * kTmRows;
-    t.b_row = ch * kTmTok;
-    t.n_valid = min(kTmTok, p.shared_rows - t.b_row);
-    t.k = p.k_shared;
-  } else {
-    const int wt_r = p.w_rows_routed / kTmRows;
-    const int j = item - n_items_s;
-    int lo = 0, hi = p.n_groups;
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (chunk_pre[mid] * wt_r <= j) lo = mid; else hi = mid;
-    }
-    const int e = lo;
-    const int ce = chunk_pre[e + 1] - chunk_pre[e];
-    const int local = j - chunk_pre[e] * wt_r;
-    const int wt = local / ce, ch = local % ce;
-    t.shared = 0;
-    t.wt = wt;
-    t.a_row = e * p.w_rows_routed + wt * kTmRows;
-    t.b_row = off_s[e] + ch * kTmTok;
-    t.n_valid = min(kTmTok, off_s[e + 1] - t.b_row);
-    t.k = p.k_routed;
-  }
-  t.n_mma = kTmRows;
-  return t;
-}
-
-// tmX_*: token codes (box 128 rows), tmW_*: packed weight codes (box 256).
-template <bool SWIGLU, int STAGES>
-__global__ void __launch_bounds__(64 + 32 * kTmNW, 1)
-grouped_gemm_fp8_tm_kernel(const __grid_constant__ CUtensorMap tmW_r,
-                           const __grid_constant__ CUtensorMap tmX_r,
-                           const __grid_constant__ CUtensorMap tmW_s,
-                           const __grid_constant__ CUtensorMap tmX_s,
-                           const Fp8Params p) {
-  using L = Fp8TmSmem<STAGES>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t sbase = smem_u32(smem);
-  const uint32_t bar_full = sbase + L::bar_off;
-  const uint32_t bar_empty = bar_full + 8 * STAGES;
-  const uint32_t bar_pfull = bar_empty + 8 * STAGES;     // [2]
-  const uint32_t bar_pempty = bar_pfull + 16;            // [2]
-  const uint32_t bar_final = bar_pempty + 16;
-  const uint32_t bar_sfull = bar_final + 8;              // [kSchedDepth]
-  const uint32_t bar_sempty = bar_sfull + 8 * kSchedDepth;
-  volatile uint32_t* tmem_slot =
-      reinterpret_cast<volatile uint32_t*>(smem + L::misc_off);
-  volatile int* abort_flag =
-      reinterpret_cast<volatile int*>(smem + L::misc_off + 4);
-  volatile int* bad_flag =
-      reinterpret_cast<volatile int*>(smem + L::misc_off + 8);
-  volatile int* ep_ok = reinterpret_cast<volatile int*>(smem + L::epok_off);
-  volatile int* sched = reinterpret_cast<volatile int*>(smem + L::sched_off);
-  int* off_s = reinterpret_cast<int*>(smem + L::tab_off);
-  int* chunk_pre = off_s + (kMaxGroups + 1);
-  float* amax_s = reinterpret_cast<float*>(smem + L::amax_off);
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int G = p.n_groups;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, 1);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(bar_pfull + 8 * b, 1);
-      mbar_init(bar_pempty + 8 * b, kTmNW);
-    }
-    mbar_init(bar_final, 1);
-    for (int i = 0; i < kSchedDepth; ++i) {
-      mbar_init(bar_sfull + 8 * i, 1);
-      mbar_init(bar_sempty + 8 * i, 1 + kTmNW);
-    }
-    *abort_flag = 0;
-    *bad_flag = 0;
-    fence_mbar_init();
-    if (G > 0) {
-      tma_prefetch_desc(&tmW_r);
-      tma_prefetch_desc(&tmX_r);
-    }
-    if (p.shared_rows > 0) {
-      tma_prefetch_desc(&tmW_s);
-      tma_prefetch_desc(&tmX_s);
-    }
-  }
-  if (warp == 1) {
-    tmem_alloc(sbase + L::misc_off, L::tmem_cols);
-    tmem_relinquish();
-  }
-  if (G > 0)
-    for (int e = threadIdx.x; e <= G; e += blockDim.x) off_s[e] = p.offsets[e];
-  __syncthreads();
-  for (int e = threadIdx.x; e < G; e += blockDim.x) {
-    const int m = off_s[e + 1] - off_s[e];
-    if (m < 0 || off_s[e] < 0) *bad_flag = 1;
-    chunk_pre[e + 1] = m > 0 ? (m + kTmTok - 1) / kTmTok : 0;
-  }
-  if (threadIdx.x == 0) {
-    chunk_pre[0] = 0;
-    if (G > 0 && static_cast<long long>(off_s[G]) > p.max_routed_rows)
-      *bad_flag = 1;
-  }
-  __syncthreads();
-  if (warp == 0) {
-    int carry = 0;
-    for (int base = 1; base <= G; base += 32) {
-      const int i = base + lane;
-      int v = (i <= G) ? chunk_pre[i] : 0;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o) v += y;
-      }
-      if (i <= G) chunk_pre[i] = v + carry;
-      carry += __shfl_sync(0xffffffffu, v, 31);
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  const bool bad = *bad_flag != 0;
-  if (bad && threadIdx.x == 0) report_error(ERR_CHECK, KID_GEMM_FP8, 300);
-
-  const int nch_s =
-      p.shared_rows > 0 ? (p.shared_rows + kTmTok - 1) / kTmTok : 0;
-  const int n_items_s = nch_s * (p.w_rows_shared / kTmRows);
-  const int n_items =
-      bad ? 0
-          : n_items_s +
-                (G > 0 ? chunk_pre[G] * (p.w_rows_routed / kTmRows) : 0);
-
-  if (warp == 0) {
-    if (lane == 0) {
-      // ---------------- TMA producer + scheduler ----------------
-      int stage = 0;
-      uint32_t phase = 0;
-      int issued = 0;
-      int slot = 0;
-      uint32_t sph = 0;
-      int item = bad ? n_items : atomicAdd(p.item_counter, 1);
-      while (!*abort_flag) {
-        if (!mbar_wait(bar_sempty + 8 * slot, sph ^ 1, abort_flag,
-                       KID_GEMM_FP8, 301))
-          break;
-        sched[slot] = item;
-        mbar_arrive(bar_sfull + 8 * slot);
-        if (++slot == kSchedDepth) {
-          slot = 0;
-          sph ^= 1;
-        }
-        if (item >= n_items) break;
-        const int next = atomicAdd(p.item_counter, 1);
-        const Tile t = decode_item_tm(item, p, n_items_s, nch_s, off_s,
-                                      chunk_pre);
-        const CUtensorMap* mW = t.shared ? &tmW_s : &tmW_r;
-        const CUtensorMap* mX = t.shared ? &tmX_s : &tmX_r;
-        const int nk = t.k / kQBlock;
-        bool ok = true;
-        for (int i = 0; i < nk; ++i) {
-          if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag,
-                         KID_GEMM_FP8, 302)) {
-            ok = false;
-            break;
-          }
-          const uint32_t fb = bar_full + 8 * stage;
-          mbar_arrive_expect_tx(fb, L::a_bytes + L::b_bytes);
-          tma_load_2d(sbase + L::a_off + stage * L::a_bytes, mX, i * kQBlock,
-                      t.b_row, fb);
-          tma_load_2d(sbase + L::b_off + stage * L::b_bytes, mW, i * kQBlock,
-                      t.a_row, fb);
-          ++issued;
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1;
-          }
-        }
-        if (!ok) break;
-        item = next;
-      }
-      if (*abort_flag) {
-        for (int j = 0; j < STAGES && j < issued; ++j) {
-          int st = stage - 1 - j;
-          uint32_t ph = phase;
-          if (st < 0) {
-            st += STAGES;
-            ph ^= 1;
-          }
-          mbar_drain(bar_full + 8 * st, ph);
-        }
-      }
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer ----------------
-      int stage = 0;
-      uint32_t phase = 0;
-      int buf = 0;
-      uint32_t bph = 0;
-      int slot = 0;
-      uint32_t sph = 0;
-      const uint32_t idesc = idesc_e4m3_f32(kTmTok, kTmRows);
-      while (!*abort_flag) {
-        if (!mbar_wait(bar_sfull + 8 * slot, sph, abort_flag, KID_GEMM_FP8,
-                       303))
-          break;
-        const int item = sched[slot];
-        mbar_arrive(bar_sempty + 8 * slot);
-        if (++slot == kSchedDepth) {
-          slot = 0;
-          sph ^= 1;
-        }
-        if (item >= n_items) break;
-        const Tile t = decode_item_tm(item, p, n_items_s, nch_s, off_s,
-                                      chunk_pre);
-        const int nk = t.k / kQBlock;
-        bool ok = true;
-        for (int i = 0; i < nk; ++i) {
-          if (!mbar_wait(bar_pempty + 8 * buf, bph ^ 1, abort_flag,
-                         KID_GEMM_FP8, 304) ||
-              !mbar_wait(bar_full + 8 * stage, phase, abort_flag, KID_GEMM_FP8,
-                         305)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a0 = sbase + L::a_off + stage * L::a_bytes;
-          const uint32_t b0 = sbase + L::b_off + stage * L::b_bytes;
-#pragma unroll
-          for (int kk = 0; kk < kQBlock / 32; ++kk)
-            mma_e4m3(tmem + buf * kTmRows, sdesc_k128(a0 + kk * 32),
-                     sdesc_k128(b0 + kk * 32), idesc, kk > 0);
-          mma_commit(bar_empty + 8 * stage);
-          mma_commit(bar_pfull + 8 * buf);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1;
-          }
-          if (++buf == 2) {
-            buf = 0;
-            bph ^= 1;
-          }
-        }
-        if (!ok) break;
-      }
-      mma_commit(bar_final);
-      mbar_drain(bar_final, 0);
-    }
-  } else {
-    // ---------------- epilogue: promotion + finish ----------------
-    const int ep = warp - 2;
-    const int q = warp & 3;            // TMEM lane quarter = 32 tokens
-    const int cg = ep >> 2;            // column group
-    const int row = q * 32 + lane;     // token row of the item
-    // columns read by this thread: SwiGLU: gate [32cg, +32) and up
-    // [128 + 32cg, +32); down: [64cg, +64)
-    const uint32_t c_lo = SWIGLU ? 32u * cg : 64u * cg;
-    const uint32_t c_hi = SWIGLU ? 128u + 32u * cg : 64u * cg + 32u;
-    int buf = 0;
-    uint32_t bph = 0;
-    int slot = 0;
-    uint32_t sph = 0;
-    bool overflow = false;
-    while (true) {
-      const bool got = mbar_wait(bar_sfull + 8 * slot, sph, abort_flag,
-                                 KID_GEMM_FP8, 306);
-      const int item = got ? sched[slot] : n_items;
-      __syncwarp();
-      if (got && lane == 0) mbar_arrive(bar_sempty + 8 * slot);
-      if (++slot == kSchedDepth) {
-        slot = 0;
-        sph ^= 1;
-      }
-      const bool wok = __all_sync(0xffffffffu, got);
-      if (lane == 0) ep_ok[ep] = wok ? 1 : 0;
-      named_bar_sync(1, 32 * kTmNW);
-      bool all_ok = true;
-      for (int w = 0; w < kTmNW; ++w) all_ok = all_ok && ep_ok[w];
-      named_bar_sync(1, 32 * kTmNW);
-      if (!all_ok || item >= n_items) break;
-      const Tile t = decode_item_tm(item, p, n_items_s, nch_s, off_s,
-                                    chunk_pre);
-      const float* sw = t.shared ? p.sw_shared : p.sw_routed;
-      const float* sx = t.shared ? p.sx_shared : p.sx_routed;
-      const long long ldsx = t.shared ? p.ldsx_shared : p.ldsx_routed;
-      const int nk = t.k / kQBlock;
-      const int rb = t.a_row / 128;
-      // weight blocks of the two column ranges this thread reads
-      const int rb_lo = SWIGLU ? rb : rb + (cg >> 1);
-      const int rb_hi = SWIGLU ? rb + 1 : rb + (cg >> 1);
-      const bool live = row < t.n_valid;
-      float acc_lo[32], acc_hi[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        acc_lo[j] = 0.f;
-        acc_hi[j] = 0.f;
-      }
-      auto scales_of = [&](int i, float& mlo, float& mhi) {
-        const float st =
-            live ? __ldg(sx + static_cast<size_t>(i) * ldsx + t.b_row + row)
-                 : 0.f;
-        mlo = __ldg(sw + static_cast<size_t>(rb_lo) * nk + i) * st;
-        mhi = __ldg(sw + static_cast<size_t>(rb_hi) * nk + i) * st;
-      };
-      float nlo, nhi;
-      scales_of(0, nlo, nhi);
-      for (int i = 0; i < nk; ++i) {
-        const float mlo = nlo, mhi = nhi;
-        if (i + 1 < nk) scales_of(i + 1, nlo, nhi);
-        mbar_wait(bar_pfull + 8 * buf, bph, abort_flag, KID_GEMM_FP8, 307);
-        tc_fence_after();
-        const uint32_t ta = tmem + (static_cast<uint32_t>(q * 32) << 16) +
-                            buf * kTmRows;
-        // 16 columns at a time: the register budget of 18 warps per SM
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t r[16];
-          tmem_ld16(ta + c_lo + 16 * h, r);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            acc_lo[16 * h + j] =
-                fmaf(__uint_as_float(r[j]), mlo, acc_lo[16 * h + j]);
-          tmem_ld16(ta + c_hi + 16 * h, r);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            acc_hi[16 * h + j] =
-                fmaf(__uint_as_float(r[j]), mhi, acc_hi[16 * h + j]);
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_pempty + 8 * buf);
-        if (++buf == 2) {
-          buf = 0;
-          bph ^= 1;
-        }
-      }
-      if constexpr (SWIGLU) {
-        // H for intermediate indices wt*128 + 32cg + j of this token; the
-        // 1 x 128 block spans the four column groups
-        float a = 0.f;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          acc_lo[j] = silu_f32(acc_lo[j]) * acc_hi[j];
-          a = fmaxf(a, fabsf(acc_lo[j]));
-        }
-        amax_s[cg * kTmTok + row] = a;
-        named_bar_sync(1, 32 * kTmNW);
-        const float am = fmaxf(fmaxf(amax_s[row], amax_s[kTmTok + row]),
-                               fmaxf(amax_s[2 * kTmTok + row],
-                                     amax_s[3 * kTmTok + row]));
-        const int e = e4m3_scale_exp(am);
-        const bool eok = e >= -126 && e <= 126;
-        overflow |= live && !eok;
-        if (live) {
-          uint8_t* H = static_cast<uint8_t*>(t.shared ? p.out_shared
-                                                       : p.out_routed);
-          const long long ldh = t.shared ? p.ld_shared : p.ld_routed;
-          const float inv = eok ? pow2f(-e) : 0.f;
-          uint4 w0, w1;
-          w0.x = quant4(acc_lo + 0, inv);
-          w0.y = quant4(acc_lo + 4, inv);
-          w0.z = quant4(acc_lo + 8, inv);
-          w0.w = quant4(acc_lo + 12, inv);
-          w1.x = quant4(acc_lo + 16, inv);
-          w1.y = quant4(acc_lo + 20, inv);
-          w1.z = quant4(acc_lo + 24, inv);
-          w1.w = quant4(acc_lo + 28, inv);
-          uint4* dst = reinterpret_cast<uint4*>(
-              H + static_cast<size_t>(t.b_row + row) * ldh + t.wt * 128 +
-              32 * cg);
-          dst[0] = w0;
-          dst[1] = w1;
-          if (cg == 0) {
-            float* sh = t.shared ? p.sh_shared : p.sh_routed;
-            const long long ldsh = t.shared ? p.ldsh_shared : p.ldsh_routed;
-            sh[static_cast<size_t>(t.wt) * ldsh + t.b_row + row] =
-                eok ? pow2f(e) : 0.f;
-          }
-        }
-        named_bar_sync(1, 32 * kTmNW);   // amax_s is reused next item
-      } else {
-        if (live) {
-          __half* Y = static_cast<__half*>(t.shared ? p.out_shared
-                                                    : p.out_routed);
-          const long long ldy = t.shared ? p.ld_shared : p.ld_routed;
-          uint4* dst = reinterpret_cast<uint4*>(
-              Y + static_cast<size_t>(t.b_row + row) * ldy + t.wt * kTmRows +
-              64 * cg);
-#pragma unroll
-          for (int v = 0; v < 8; ++v) {
-            const float* src = v < 4 ? acc_lo + 8 * v : acc_hi + 8 * (v - 4);
-            uint4 o;
-            uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
-#pragma unroll
-            for (int k2 = 0; k2 < 4; ++k2) {
-              overflow |= !(fabsf(src[2 * k2]) <= 65504.f) ||
-                          !(fabsf(src[2 * k2 + 1]) <= 65504.f);
-              const __half2 hv = __floats2half2_rn(src[2 * k2], src[2 * k2 + 1]);
-              ow[k2] = *reinterpret_cast<const uint32_t*>(&hv);
-            }
-            dst[v] = o;
-          }
-        }
-      }
-    }
-    if (overflow) report_error(ERR_CHECK, KID_GEMM_FP8, 310);
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, L::tmem_cols);
-  }
-}
-
 }  // namespace moe

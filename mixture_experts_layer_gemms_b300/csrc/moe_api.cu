@@ -16,6 +16,7 @@
 #include "permute.cuh"
 #include "route.cuh"
 #include "gemm_fp8.cuh"
+#include "gemm_fp8_pair.cuh"
 #include "bwd.cuh"
 #include "gemm_bwd.cuh"
 #include "gemm_bwd2sm.cuh"
@@ -62,6 +63,7 @@ struct DeviceInfo {
   int sm_count = 0;
   int pair_clusters = 0;   // co-resident clusters of the CTA-pair GEMM
   int bwd_pair_clusters = 0;   // same for the backward's CTA-pair GEMM
+  int f8_pair_clusters = 0;    // same for the e4m3 CTA-pair GEMM
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -103,10 +105,6 @@ moe_status device_setup(int* sm_count) {
     MOE_FP8_SMEM(128, 2, true, false, 4);
     MOE_FP8_SMEM(128, 2, false, false, 6);
 #undef MOE_FP8_SMEM
-    MOE_CHECK_CUDA(allow_smem(grouped_gemm_fp8_tm_kernel<true, 4>,
-                              Fp8TmSmem<4>::alloc));
-    MOE_CHECK_CUDA(allow_smem(grouped_gemm_fp8_tm_kernel<false, 4>,
-                              Fp8TmSmem<4>::alloc));
     MOE_CHECK_CUDA(allow_smem(bwd_gemm_kernel<kDgrad, 256, 4>,
                               BwdSmem<256, 4>::alloc));
     MOE_CHECK_CUDA(allow_smem(bwd_gemm_kernel<kRecomp, 256, 4>,
@@ -135,6 +133,13 @@ moe_status device_setup(int* sm_count) {
     MOE_CHECK_CUDA(cudaOccupancyMaxActiveClusters(
         &clusters, bwd_gemm_pair_kernel<kWgrad>, &cfg));
     di.bwd_pair_clusters = clusters;
+    MOE_CHECK_CUDA(allow_smem(grouped_gemm_fp8_pair_kernel, F8PairSmem::alloc));
+    cfg.dynamicSmemBytes = F8PairSmem::alloc;
+    cfg.blockDim = dim3(kF8PThreads);
+    clusters = 0;
+    MOE_CHECK_CUDA(cudaOccupancyMaxActiveClusters(
+        &clusters, grouped_gemm_fp8_pair_kernel, &cfg));
+    di.f8_pair_clusters = clusters;
     di.init = true;
   }
   *sm_count = di.sm_count;
@@ -146,6 +151,13 @@ int bwd_pair_clusters() {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
     return 0;
   return g_dev[dev].bwd_pair_clusters;
+}
+
+int f8_pair_clusters() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return 0;
+  return g_dev[dev].f8_pair_clusters;
 }
 
 int pair_clusters() {
@@ -251,6 +263,32 @@ bool aligned16(const void* p) {
 inline long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
 inline size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// e4m3 operand buffers [rows, cols] (cols = the reduction): the codes, then
+// at the next 256-byte boundary the fp32 scales, then at the next 256-byte
+// boundary the same scales as a UE8M0 table [R][ue8_pitch(cols)].
+// Activations: scales [cols/128][rows], R = rows.  Weights: scales
+// [rows/128][cols/128], R = rows/128.
+inline size_t fp8_codes_bytes(long long rows, long long cols) {
+  return round256(static_cast<size_t>(rows) * cols);
+}
+inline size_t fp8_scales_bytes(long long rows, long long cols, bool weights) {
+  return round256(static_cast<size_t>(weights ? rows / 128 : rows) *
+                  (cols / 128) * 4);
+}
+inline size_t fp8_ue8_bytes(long long rows, long long cols, bool weights) {
+  return round256(static_cast<size_t>(weights ? rows / 128 : rows) *
+                  ue8_pitch(cols));
+}
+inline size_t fp8_buf_bytes(long long rows, long long cols, bool weights) {
+  return fp8_codes_bytes(rows, cols) + fp8_scales_bytes(rows, cols, weights) +
+         fp8_ue8_bytes(rows, cols, weights);
+}
+inline uint8_t* fp8_ue8(const void* base, long long rows, long long cols,
+                        bool weights) {
+  return static_cast<uint8_t*>(const_cast<void*>(base)) +
+         fp8_codes_bytes(rows, cols) + fp8_scales_bytes(rows, cols, weights);
+}
+
 moe_status check_shape(const moe_shape* s) {
   if (s == nullptr) return fail(MOE_ERR_INVALID_ARG, "shape is NULL");
   if (s->dtype != MOE_F32 && s->dtype != MOE_BF16 && s->dtype != MOE_FP8)
@@ -290,7 +328,8 @@ moe_status check_shape(const moe_shape* s) {
 }
 
 struct WsLayout {
-  size_t sched, route_hist, perm_hist, h_routed, h_shared, u_q, total;
+  size_t sched, route_hist, perm_hist, h_routed, h_shared, u_q, h8_routed,
+      h8_shared, total;
 };
 
 WsLayout ws_layout(const moe_shape* s) {
@@ -307,14 +346,23 @@ WsLayout ws_layout(const moe_shape* s) {
   w.perm_hist = off;
   off = round256(off + static_cast<size_t>(cdiv(s->T, kPermChunk)) *
                            s->n_routed * 4);
+  // H between the passes (MOE_FP8: fp32, requantized to e4m3 below)
+  const size_t hs = s->dtype == MOE_FP8 ? 4 : es;
   w.h_routed = off;
-  off = round256(off + static_cast<size_t>(A) * s->d_ff * es);
+  off = round256(off + static_cast<size_t>(A) * s->d_ff * hs);
   w.h_shared = off;
-  off = round256(off + static_cast<size_t>(s->T) * s->n_shared * s->d_ff * es);
+  off = round256(off + static_cast<size_t>(s->T) * s->n_shared * s->d_ff * hs);
   w.u_q = off;          // MOE_FP8: e4m3 codes of u and their block scales
   if (s->dtype == MOE_FP8 && s->n_shared > 0)
-    off = round256(round256(off + static_cast<size_t>(s->T) * s->d) +
-                   static_cast<size_t>(s->d / 128) * s->T * 4);
+    off += fp8_buf_bytes(s->T, s->d, false);
+  // MOE_FP8 prefill path: H as e4m3 codes and scales (requantized from the
+  // fp32 H that the gate/up pass leaves in h_routed / h_shared)
+  w.h8_routed = off;
+  if (s->dtype == MOE_FP8) off += fp8_buf_bytes(A, s->d_ff, false);
+  w.h8_shared = off;
+  if (s->dtype == MOE_FP8 && s->n_shared > 0)
+    off += fp8_buf_bytes(s->T, static_cast<long long>(s->n_shared) * s->d_ff,
+                         false);
   w.total = off;
   return w;
 }
@@ -413,11 +461,6 @@ moe_status pair_maps(const void* w_r, long long w_r_rows, const void* x_r,
   return MOE_OK;
 }
 
-// Packed e4m3 operand: codes [rows, cols] then, at the next 256-byte
-// boundary, fp32 scales.
-inline size_t fp8_codes_bytes(long long rows, long long cols) {
-  return round256(static_cast<size_t>(rows) * cols);
-}
 
 template <int BN, int CW, bool TWO, bool SWIGLU, int STAGES>
 moe_status launch_gemm_fp8(const CUtensorMap& a_r, const CUtensorMap& b_r,
@@ -434,27 +477,6 @@ moe_status launch_gemm_fp8(const CUtensorMap& a_r, const CUtensorMap& b_r,
   const int grid = static_cast<int>(items < sms ? items : sms);
   grouped_gemm_fp8_kernel<BN, CW, TWO, SWIGLU, STAGES>
       <<<grid, L::threads, L::alloc, cs>>>(a_r, b_r, a_s, b_s, p);
-  MOE_CHECK_LAUNCH();
-  return MOE_OK;
-}
-
-// tokens-on-M e4m3 GEMM (prefill-sized groups); maps: weights box 256 rows,
-// tokens box 128 rows
-template <bool SWIGLU, int STAGES>
-moe_status launch_gemm_fp8_tm(const CUtensorMap& w_r, const CUtensorMap& x_r,
-                              const CUtensorMap& w_s, const CUtensorMap& x_s,
-                              const Fp8Params& p, int sms, cudaStream_t cs) {
-  long long items = 0;
-  if (p.shared_rows > 0)
-    items += cdiv(p.shared_rows, kTmTok) * (p.w_rows_shared / kTmRows);
-  if (p.n_groups > 0)
-    items += (cdiv(p.max_routed_rows, kTmTok) + p.n_groups) *
-             (p.w_rows_routed / kTmRows);
-  if (items == 0) return MOE_OK;
-  const int grid = static_cast<int>(items < sms ? items : sms);
-  grouped_gemm_fp8_tm_kernel<SWIGLU, STAGES>
-      <<<grid, Fp8TmSmem<STAGES>::threads, Fp8TmSmem<STAGES>::alloc, cs>>>(
-          w_r, x_r, w_s, x_s, p);
   MOE_CHECK_LAUNCH();
   return MOE_OK;
 }
@@ -476,6 +498,89 @@ moe_status launch_gemm_pair(const PairMaps& m, const GemmParams& p,
                              cs>>>(m.a_r, m.b_r32, m.a_s, m.b_s32, m.b_r64,
                                    m.b_s64, m.b_r96, m.b_s96, m.b_r128,
                                    m.b_s128, p);
+  MOE_CHECK_LAUNCH();
+  return MOE_OK;
+}
+
+// 4-D view of a packed e4m3 gate/up operand [rows, cols] as {cols, 64
+// rows, 2 halves, rows / 128 blocks} with a box of {128 bytes, 64, 1, 2}:
+// one load brings half h of row block w (gate) and the same half of block
+// w + 1 (up), 128-byte swizzle.
+moe_status make_map_u8_gu4d(CUtensorMap* m, const void* ptr, long long rows,
+                            long long cols) {
+  moe_status st = get_encoder();
+  if (st != MOE_OK) return st;
+  const long long blocks = rows / 128 > 0 ? rows / 128 : 1;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(cols), 64, 2,
+                        static_cast<cuuint64_t>(blocks)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(cols),
+                           static_cast<cuuint64_t>(64 * cols),
+                           static_cast<cuuint64_t>(128 * cols)};
+  cuuint32_t box[4] = {128, 64, 1, 2};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4,
+                        const_cast<void*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled (4-D u8) failed (%d) "
+                "rows=%lld cols=%lld", static_cast<int>(r), rows, cols);
+  return MOE_OK;
+}
+
+// Tensor maps of the e4m3 CTA-pair GEMM: weights (the 4-D gate/up view, or
+// 128-row boxes for the down pass) and tokens (32 / 64 / 96-row boxes),
+// routed and shared; 128-byte rows of e4m3 codes.
+struct F8PairMaps {
+  CUtensorMap a_r, a_s, b_r32, b_s32, b_r64, b_s64, b_r96, b_s96;
+};
+
+moe_status f8_pair_maps(const void* w_r, long long w_r_rows, const void* x_r,
+                        long long x_r_rows, long long k_r, const void* w_s,
+                        long long w_s_rows, const void* x_s, long long x_s_rows,
+                        long long k_s, int a_box, F8PairMaps& m) {
+  moe_status st;
+  auto wmap = [&](CUtensorMap* mm, const void* w, long long rows,
+                  long long k) {
+    return a_box == 64 ? make_map_u8_gu4d(mm, w, rows, k)
+                       : make_map_u8(mm, w, rows, k, a_box);
+  };
+  if ((st = wmap(&m.a_r, w_r, w_r_rows, k_r)) != MOE_OK) return st;
+  CUtensorMap* br[3] = {&m.b_r32, &m.b_r64, &m.b_r96};
+  CUtensorMap* bs[3] = {&m.b_s32, &m.b_s64, &m.b_s96};
+  const int boxes[3] = {32, 64, 96};
+  for (int i = 0; i < 3; ++i)
+    if ((st = make_map_u8(br[i], x_r, x_r_rows, k_r, boxes[i])) != MOE_OK)
+      return st;
+  if (w_s != nullptr) {
+    if ((st = wmap(&m.a_s, w_s, w_s_rows, k_s)) != MOE_OK) return st;
+    for (int i = 0; i < 3; ++i)
+      if ((st = make_map_u8(bs[i], x_s, x_s_rows, k_s, boxes[i])) != MOE_OK)
+        return st;
+  } else {
+    m.a_s = m.a_r;
+    for (int i = 0; i < 3; ++i) *bs[i] = *br[i];
+  }
+  return MOE_OK;
+}
+
+moe_status launch_gemm_fp8_pair(const F8PairMaps& m, const F8PairParams& p,
+                                cudaStream_t cs) {
+  long long items = 0;
+  if (p.shared_rows > 0)
+    items += cdiv(p.shared_rows, kF8PBN) * (p.w_rows_shared / kF8PBM);
+  if (p.n_groups > 0)
+    items += (cdiv(p.max_routed_rows, kF8PBN) + p.n_groups) *
+             (p.w_rows_routed / kF8PBM);
+  if (items == 0) return MOE_OK;
+  const long long clusters = f8_pair_clusters();
+  if (clusters <= 0)
+    return fail(MOE_ERR_CUDA, "e4m3 CTA-pair GEMM cannot be resident");
+  const long long n = items < clusters ? items : clusters;
+  grouped_gemm_fp8_pair_kernel<<<static_cast<int>(2 * n), kF8PThreads,
+                                 F8PairSmem::alloc, cs>>>(
+      m.a_r, m.a_s, m.b_r32, m.b_s32, m.b_r64, m.b_s64, m.b_r96, m.b_s96, p);
   MOE_CHECK_LAUNCH();
   return MOE_OK;
 }
@@ -506,15 +611,88 @@ moe_status expert_ffn_fp8(const moe_shape* s, const void* x_perm,
   if (has_shared) {
     const long long warps = T * (d / kQBlock);
     quantize_rows_kernel<<<static_cast<unsigned>(cdiv(warps, 8)), 256, 0, cs>>>(
-        static_cast<const __nv_bfloat16*>(u), s->T, d, u8, scales(u8, T, d), T);
+        static_cast<const __nv_bfloat16*>(u), s->T, d, u8, scales(u8, T, d), T,
+        fp8_ue8(u8, T, d, false));
     MOE_CHECK_LAUNCH();
   }
   int* ctr = reinterpret_cast<int*>(wsb + w.sched);
   zero_i32_kernel<<<1, 32, 0, cs>>>(ctr, 2);
   MOE_CHECK_LAUNCH();
   const bool small = A <= 48LL * N;
-  // prefill-sized groups with d % 256 == 0: tokens on M
-  const bool tm = !small && d % 256 == 0;
+  if (!small && d % 256 == 0 && ue8_pitch(d) <= kF8PMaxPitch &&
+      ue8_pitch(I) <= kF8PMaxPitch && ue8_pitch(SI) <= kF8PMaxPitch) {
+    // Prefill-sized groups: e4m3 CTA pairs with the block scales applied in
+    // the tensor core.  H leaves the gate/up pass as fp32 and is requantized
+    // to e4m3 1 x 128 blocks (the same rule as every activation) for the
+    // down pass.
+    float* hb = reinterpret_cast<float*>(wsb + w.h_routed);
+    float* hbs = reinterpret_cast<float*>(wsb + w.h_shared);
+    uint8_t* q8 = reinterpret_cast<uint8_t*>(wsb + w.h8_routed);
+    uint8_t* q8s = reinterpret_cast<uint8_t*>(wsb + w.h8_shared);
+    F8PairMaps m;
+    F8PairParams q{};
+    if ((st = f8_pair_maps(w_gu8, 2LL * N * I, x_perm, A, d,
+                           has_shared ? ws_gu8 : nullptr, 2LL * SI, u8, T, d,
+                           64, m)) != MOE_OK)
+      return st;
+    q.offsets = offsets;
+    q.n_groups = N;
+    q.max_routed_rows = A;
+    q.shared_rows = has_shared ? s->T : 0;
+    q.w_rows_routed = 2 * I;
+    q.w_rows_shared = 2 * SI;
+    q.k_routed = d;
+    q.k_shared = d;
+    q.gate_up = 1;
+    q.sw_routed = fp8_ue8(w_gu8, 2LL * N * I, d, true);
+    q.sw_shared = has_shared ? fp8_ue8(ws_gu8, 2LL * SI, d, true) : nullptr;
+    q.sx_routed = fp8_ue8(x_perm, A, d, false);
+    q.sx_shared = has_shared ? fp8_ue8(u8, T, d, false) : nullptr;
+    q.pitch_routed = ue8_pitch(d);
+    q.pitch_shared = ue8_pitch(d);
+    q.out_routed = hb;
+    q.ld_routed = I;
+    q.out_shared = hbs;
+    q.ld_shared = SI;
+    q.item_counter = ctr;
+    if ((st = launch_gemm_fp8_pair(m, q, cs)) != MOE_OK) return st;
+    if (A > 0) {
+      const long long warps = A * (I / kQBlock);
+      quantize_rows_kernel<<<static_cast<unsigned>(cdiv(warps, 8)), 256, 0,
+                             cs>>>(hb, static_cast<int>(A), I, q8,
+                                   scales(q8, A, I), A,
+                                   fp8_ue8(q8, A, I, false));
+      MOE_CHECK_LAUNCH();
+    }
+    if (has_shared) {
+      const long long warps = T * (SI / kQBlock);
+      quantize_rows_kernel<<<static_cast<unsigned>(cdiv(warps, 8)), 256, 0,
+                             cs>>>(hbs, s->T, SI, q8s, scales(q8s, T, SI), T,
+                                   fp8_ue8(q8s, T, SI, false));
+      MOE_CHECK_LAUNCH();
+    }
+    if ((st = f8_pair_maps(w_down8, static_cast<long long>(N) * d, q8, A, I,
+                           has_shared ? ws_down8 : nullptr, d, q8s, T, SI, 128,
+                           m)) != MOE_OK)
+      return st;
+    q.w_rows_routed = d;
+    q.w_rows_shared = d;
+    q.k_routed = I;
+    q.k_shared = SI;
+    q.gate_up = 0;
+    q.sw_routed = fp8_ue8(w_down8, static_cast<long long>(N) * d, I, true);
+    q.sw_shared = has_shared ? fp8_ue8(ws_down8, d, SI, true) : nullptr;
+    q.sx_routed = fp8_ue8(q8, A, I, false);
+    q.sx_shared = has_shared ? fp8_ue8(q8s, T, SI, false) : nullptr;
+    q.pitch_routed = ue8_pitch(I);
+    q.pitch_shared = ue8_pitch(SI);
+    q.out_routed = y_perm;
+    q.ld_routed = d;
+    q.out_shared = y_shared;
+    q.ld_shared = d;
+    q.item_counter = ctr + 1;
+    return launch_gemm_fp8_pair(m, q, cs);
+  }
   const int bn = small ? 32 : 128;
   CUtensorMap a_r, b_r, a_s, b_s;
   Fp8Params p{};
@@ -551,10 +729,7 @@ moe_status expert_ffn_fp8(const moe_shape* s, const void* x_perm,
   p.sh_shared = has_shared ? scales(h8s, T, SI) : nullptr;
   p.ldsh_shared = T;
   p.item_counter = ctr;
-  if (tm)
-    st = launch_gemm_fp8_tm<true, 4>(a_r, b_r, a_s, b_s, p, sms, cs);
-  else
-    st = small
+  st = small
              ? launch_gemm_fp8<32, 1, true, true, 6>(a_r, b_r, a_s, b_s, p, sms,
                                                      cs)
              : launch_gemm_fp8<128, 2, true, true, 4>(a_r, b_r, a_s, b_s, p,
@@ -591,7 +766,6 @@ moe_status expert_ffn_fp8(const moe_shape* s, const void* x_perm,
   p.ld_shared = d;
   p.sh_shared = nullptr;
   p.item_counter = ctr + 1;
-  if (tm) return launch_gemm_fp8_tm<false, 4>(a_r, b_r, a_s, b_s, p, sms, cs);
   if (small)
     return two ? launch_gemm_fp8<32, 1, true, false, 6>(a_r, b_r, a_s, b_s, p,
                                                         sms, cs)
@@ -721,8 +895,7 @@ moe_status moe_fp8_weight_bytes(const moe_shape* s, int which,
     default:
       return fail(MOE_ERR_INVALID_ARG, "which=%d (0..3)", which);
   }
-  *bytes = fp8_codes_bytes(rows, cols) +
-           round256(static_cast<size_t>(rows / 128) * (cols / 128) * 4);
+  *bytes = fp8_buf_bytes(rows, cols, true);
   return MOE_OK;
 }
 
@@ -732,8 +905,7 @@ moe_status moe_x_perm_bytes(const moe_shape* s, size_t* bytes) {
   if (bytes == nullptr) return fail(MOE_ERR_INVALID_ARG, "bytes is NULL");
   const long long A = static_cast<long long>(s->T) * s->top_k;
   if (s->dtype == MOE_FP8)
-    *bytes = fp8_codes_bytes(A, s->d) +
-             round256(static_cast<size_t>(s->d / 128) * A * 4);
+    *bytes = fp8_buf_bytes(A, s->d, false);
   else
     *bytes = static_cast<size_t>(A) * s->d * elem_size(s->dtype);
   return MOE_OK;
@@ -772,7 +944,8 @@ moe_status moe_pack_weights_fp8(const moe_shape* s, const void* w_gate,
                     static_cast<unsigned>(rows / kQBlock));
     quantize_weight_blocks_kernel<<<grid, 256, 0, cs>>>(
         static_cast<const __nv_bfloat16*>(a),
-        static_cast<const __nv_bfloat16*>(b), mode, K, I, d, q, sc);
+        static_cast<const __nv_bfloat16*>(b), mode, K, I, d, q, sc,
+        fp8_ue8(q, rows, K, true));
     MOE_CHECK_LAUNCH();
     return MOE_OK;
   };
@@ -907,7 +1080,8 @@ moe_status moe_permute(const moe_shape* s, const void* u,
       const int grid8 = static_cast<int>(wq < sms * 16LL ? wq : sms * 16LL);
       permute_gather_fp8_kernel<<<grid8, 256, 0, cs>>>(
           static_cast<const __nv_bfloat16*>(u), inv, s->T, s->top_k, s->d, A,
-          x8, reinterpret_cast<float*>(x8 + fp8_codes_bytes(A, s->d)));
+          x8, reinterpret_cast<float*>(x8 + fp8_codes_bytes(A, s->d)),
+          fp8_ue8(x8, A, s->d, false));
       MOE_CHECK_LAUNCH();
       return MOE_OK;
     }

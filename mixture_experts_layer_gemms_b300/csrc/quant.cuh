@@ -9,9 +9,14 @@
 // (e = 0 for an all-zero block); its codes are e4m3(x * 2^-e), rounded to
 // nearest even and saturated at +-448 (the conversion instruction's
 // satfinite mode).  x * 2^-e is exact, so GPU and CPU codes agree bit for
-// bit.  Scales are stored as fp32 powers of two.  Exponents outside
-// [-126, 126] (block maxima beyond the fp32 power-of-two range) are
-// reported as a device check and the block is written as zeros.
+// bit.  Scales are stored as fp32 powers of two and, for the block-scaled
+// tensor-core kernels, once more as UE8M0 bytes (the biased exponent,
+// 127 + e) in a row-major [R][P] table: R = rows for activations (one byte
+// per row and 128-block of the reduction), R = row blocks for weights;
+// P = the block count rounded up to 16, the padding bytes 127 (2^0), so a
+// row of the table is a 16-byte multiple.  Exponents outside [-126, 126]
+// (block maxima beyond the fp32 power-of-two range) are reported as a
+// device check and the block is written as zeros.
 #pragma once
 #include <cuda_fp8.h>
 #include "common.cuh"
@@ -29,6 +34,16 @@ __device__ __forceinline__ int e4m3_scale_exp(float amax) {
 
 __device__ __forceinline__ float pow2f(int e) {   // exact for |e| <= 126
   return __int_as_float((127 + e) << 23);
+}
+
+// Row stride (bytes) of a UE8M0 scale table for a reduction of k elements.
+__host__ __device__ __forceinline__ int ue8_pitch(long long k) {
+  return static_cast<int>(((k / kQBlock) + 15) / 16 * 16);
+}
+// UE8M0 byte of a stored fp32 power-of-two scale (0 for the zero written
+// after a reported bad exponent).
+__device__ __forceinline__ uint8_t ue8_of(float s) {
+  return static_cast<uint8_t>((__float_as_uint(s) >> 23) & 0xFFu);
 }
 
 __device__ __forceinline__ uint32_t e4m3_code(float x, float inv_scale) {
@@ -73,12 +88,25 @@ __device__ __forceinline__ uint32_t warp_quant_block(const float* f,
   return quant4(f, pow2f(-e));
 }
 
-// Activations: x bf16 [R, K] row-major -> codes [R, K] and scales
+__device__ __forceinline__ void load4_f32(const float* p, float* f) {
+  const float4 v = __ldg(reinterpret_cast<const float4*>(p));
+  f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
+}
+__device__ __forceinline__ void load4(const __nv_bfloat16* p, float* f) {
+  load4_bf16(p, f);
+}
+__device__ __forceinline__ void load4(const float* p, float* f) {
+  load4_f32(p, f);
+}
+
+// Activations: x (bf16 or fp32) [R, K] row-major -> codes [R, K] and scales
 // [K/128][ld_s] (column index = row), one warp per (row, block).
+// ue8 (optional): UE8M0 table [R][ue8_pitch(K)].
+template <typename TX>
 __global__ void __launch_bounds__(256)
-quantize_rows_kernel(const __nv_bfloat16* __restrict__ x, int R, int K,
+quantize_rows_kernel(const TX* __restrict__ x, int R, int K,
                      uint8_t* __restrict__ q, float* __restrict__ scales,
-                     long long ld_s) {
+                     long long ld_s, uint8_t* __restrict__ ue8 = nullptr) {
   const int nb = K / kQBlock;
   const long long w = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) +
                       (threadIdx.x >> 5);
@@ -88,11 +116,18 @@ quantize_rows_kernel(const __nv_bfloat16* __restrict__ x, int R, int K,
   const int b = static_cast<int>(w % nb);
   const size_t off = static_cast<size_t>(r) * K + b * kQBlock + 4 * lane;
   float f[4];
-  load4_bf16(x + off, f);
+  load4(x + off, f);
   float sc;
   const uint32_t c = warp_quant_block(f, &sc);
   *reinterpret_cast<uint32_t*>(q + off) = c;
   if (lane == 0) scales[static_cast<size_t>(b) * ld_s + r] = sc;
+  if (ue8 != nullptr) {
+    const int P = ue8_pitch(K);
+    uint8_t* row = ue8 + static_cast<size_t>(r) * P;
+    if (lane == 0) row[b] = ue8_of(sc);
+    if (b == nb - 1)                       // padding of the row
+      for (int j = nb + lane; j < P; j += 32) row[j] = 127;
+  }
 }
 
 // Dispatch fused with quantization: x8[inv[t,k]] = codes of u[t] for every
@@ -102,7 +137,8 @@ __global__ void __launch_bounds__(256)
 permute_gather_fp8_kernel(const __nv_bfloat16* __restrict__ u,
                           const int* __restrict__ inv, int T, int K, int d,
                           long long total_slots, uint8_t* __restrict__ x8,
-                          float* __restrict__ sx) {
+                          float* __restrict__ sx,
+                          uint8_t* __restrict__ ue8 = nullptr) {
   const int lane = threadIdx.x & 31;
   const int nb = d / kQBlock;
   const long long nwarps =
@@ -128,6 +164,17 @@ permute_gather_fp8_kernel(const __nv_bfloat16* __restrict__ u,
             x8 + static_cast<size_t>(s) * d + b * kQBlock + 4 * lane) = c;
     }
     if (myslot >= 0) sx[static_cast<size_t>(b) * total_slots + myslot] = sc;
+    if (ue8 != nullptr) {
+      const int P = ue8_pitch(d);
+      for (int k = 0; k < K; ++k) {
+        const int s = __shfl_sync(0xffffffffu, myslot, k);
+        if (s < 0) continue;
+        uint8_t* row = ue8 + static_cast<size_t>(s) * P;
+        if (lane == 0) row[b] = ue8_of(sc);
+        if (b == nb - 1)
+          for (int j = nb + lane; j < P; j += 32) row[j] = 127;
+      }
+    }
   }
 }
 
@@ -148,7 +195,8 @@ quantize_weight_blocks_kernel(const __nv_bfloat16* __restrict__ src0,
                               const __nv_bfloat16* __restrict__ src1,
                               int mode, int K, int I, int d,
                               uint8_t* __restrict__ q,
-                              float* __restrict__ scales) {
+                              float* __restrict__ scales,
+                              uint8_t* __restrict__ ue8 = nullptr) {
   __shared__ float red[8];
   const int cb = blockIdx.x, rb = blockIdx.y;
   const int nkb = K / kQBlock;
@@ -199,6 +247,15 @@ quantize_weight_blocks_kernel(const __nv_bfloat16* __restrict__ src0,
   }
   if (threadIdx.x == 0)
     scales[static_cast<size_t>(rb) * nkb + cb] = ok ? pow2f(e) : 0.f;
+  if (ue8 != nullptr) {
+    const int P = ue8_pitch(K);
+    uint8_t* row = ue8 + static_cast<size_t>(rb) * P;
+    if (threadIdx.x == 0) row[cb] = ue8_of(ok ? pow2f(e) : 0.f);
+    if (cb == nkb - 1)
+      for (int j = nkb + static_cast<int>(threadIdx.x); j < P;
+           j += static_cast<int>(blockDim.x))
+        row[j] = 127;
+  }
 }
 
 }  // namespace moe

@@ -153,18 +153,20 @@ def test_route_grouped_validation(moe, G, M, K, code):
 def test_fp8_sizes_and_checks(moe):
     sh = _shape(moe, dtype=moe.MOE_FP8, d_ff=256)
     n = ctypes.c_size_t()
-    # routed gate/up: 2*N*I x d codes + (2NI/128)*(d/128) fp32 scales
+    r256 = lambda x: (x + 255) // 256 * 256       # noqa: E731
+    # routed gate/up: 2*N*I x d codes, (2NI/128) x (d/128) fp32 scales, and
+    # the same scales as UE8M0 bytes with rows padded to 16
     assert moe.LIB.moe_fp8_weight_bytes(ctypes.byref(sh), 0,
                                         ctypes.byref(n)) == 0
-    assert n.value == 2 * 16 * 256 * 256 + 512     # 64 x 2 scales
+    assert n.value == 2 * 16 * 256 * 256 + r256(64 * 2 * 4) + r256(64 * 16)
     assert moe.LIB.moe_fp8_weight_bytes(ctypes.byref(sh), 3,
                                         ctypes.byref(n)) == 0
-    assert n.value == 256 * 256 + 256
+    assert n.value == 256 * 256 + r256(2 * 2 * 4) + r256(2 * 16)
     assert moe.LIB.moe_fp8_weight_bytes(ctypes.byref(sh), 4,
                                         ctypes.byref(n)) == 1
     assert moe.LIB.moe_x_perm_bytes(ctypes.byref(sh), ctypes.byref(n)) == 0
-    A = 64 * 4
-    assert n.value == A * 256 + ((2 * A * 4 + 255) // 256) * 256
+    A = 64 * 4     # activations: codes, [d/128][A] scales, [A][16] UE8M0
+    assert n.value == A * 256 + r256(2 * A * 4) + r256(A * 16)
     bad = _shape(moe, dtype=moe.MOE_FP8, d_ff=192)     # d_ff % 128
     assert _ws(moe, bad)[0] == 2
     P = ctypes.c_void_p

@@ -45,6 +45,25 @@ def _codes_scales(buf, rows, cols):
     return codes, sc.reshape(rows // 128, cols // 128)
 
 
+def _ue8(buf, rows, cols, weights):
+    """The UE8M0 scale table after the codes and fp32 scales: [R][P] bytes,
+    R = rows / 128 for weights, rows for activations; P = cols / 128 rounded
+    up to 16."""
+    b = buf.cpu().numpy()
+    r256 = lambda x: (x + 255) // 256 * 256      # noqa: E731
+    R = rows // 128 if weights else rows
+    off = r256(rows * cols) + r256(R * (cols // 128) * 4)
+    P = ((cols // 128) + 15) // 16 * 16
+    return b[off:off + R * P].reshape(R, P)
+
+
+def _expect_ue8(e, P):
+    """127 + e for every block, 127 (2^0) in the padding."""
+    t = np.full((e.shape[0], P), 127, dtype=np.uint8)
+    t[:, :e.shape[1]] = (127 + e).astype(np.uint8)
+    return t
+
+
 def _expect(q, e):
     return of.e4m3_encode(q), np.exp2(e).astype(np.float32)
 
@@ -72,6 +91,15 @@ def test_fp8_pack_bit_exact(moe):
                 assert np.array_equal(codes[r0 + 128 * part:
                                             r0 + 128 * part + 128], wc)
                 assert np.array_equal(sc[r0 // 128 + part], ws[0])
+    # the UE8M0 table of the same scales (rows = packed row blocks)
+    ue = _ue8(layer.w_gu, 2 * N * I, d, True)
+    exps = []
+    for e in range(N):
+        _, eg = of.quantize_blocks(as_f64(g["w_gate"][e]))
+        _, eu = of.quantize_blocks(as_f64(g["w_up"][e]))
+        for j in range(I // 128):
+            exps += [eg[j], eu[j]]
+    assert np.array_equal(ue, _expect_ue8(np.array(exps), ue.shape[1]))
     # routed down: [N*d, I]
     codes, sc = _codes_scales(layer.w_down, N * d, I)
     for e in range(N):
@@ -105,6 +133,8 @@ def test_fp8_permute_bit_exact(moe):
     q, e = of.quantize_rows(as_f64(g["u"])[perm])
     assert np.array_equal(codes, of.e4m3_encode(q))
     assert np.array_equal(sx, np.exp2(e).T.astype(np.float32))
+    ue = _ue8(b.x_perm, A, d, False)
+    assert np.array_equal(ue, _expect_ue8(e, ue.shape[1]))
 
 
 def _fp8_oracle_h(g, cfg, idx, rows=None):
@@ -135,6 +165,9 @@ FP8_CASES = {
     "chunked_T1000_d512": ("tiny", dict(SMALL, T=1000, d=512, d_ff=256,
                                         n_shared=2)),
     "mid_dims_T700": ("mid", dict(T=700)),
+    # the block-scaled CTA-pair kernel with reductions of 6 and 3 128-blocks
+    # (scale groups of four stages, the last one partly used)
+    "pair_d768_I384_T1200": ("tiny", dict(SMALL, T=1200, d=768, d_ff=384)),
     # d % 256 != 0: prefill-sized groups on the weights-on-M kernels
     "fallback_d384_T1200": ("tiny", dict(SMALL, T=1200, d=384, d_ff=256)),
     "no_shared_T1": ("tiny", dict(SMALL, T=1, n_shared=0)),
@@ -157,6 +190,29 @@ def test_fp8_layer_parity(moe, case):
     check_routing(r, as_f64(g["b"]), idx, b.counts.cpu().numpy(), cfg.top_k)
     e = assert_close(h.float().cpu().numpy(), h_ref, base=u64, what=case)
     print(case, e)
+
+
+def test_fp8_skewed_multi_chunk(moe):
+    """A bias that sends every token to the same K experts: on the e4m3
+    CTA-pair kernel each of them splits into chunks of at most 192 tokens
+    (4 chunks of 150, rounded up to 160 MMA columns, here), and the other
+    experts are empty."""
+    cfg = get_config("mid").with_(T=600)
+    g = make_inputs(cfg)
+    b = torch.zeros(cfg.n_routed)
+    b[[5, 17, 33, 40, 41, 63]] = 2.0
+    g["b"] = b.cuda()
+    layer = _layer(moe, g, cfg)
+    h = layer(g["u"])
+    torch.cuda.synchronize()
+    moe.get_device_error()
+    buf = layer.buffers(cfg.T)
+    counts = buf.counts.cpu().numpy()
+    assert sorted(np.nonzero(counts)[0].tolist()) == [5, 17, 33, 40, 41, 63]
+    idx = buf.topk_idx.cpu().numpy()
+    h_ref, r, u64 = _fp8_oracle_h(g, cfg, idx)
+    e = assert_close(h.float().cpu().numpy(), h_ref, base=u64, what="skew")
+    print("fp8 skewed", e)
 
 
 def test_fp8_close_to_bf16_layer(moe):

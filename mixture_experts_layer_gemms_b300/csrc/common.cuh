@@ -375,17 +375,17 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst,
       : "memory");
 }
 
-// 4-D tiled load by one CTA of a pair (completion on a possibly remote
+// 5-D tiled load by one CTA of a pair (completion on a possibly remote
 // mbarrier).
-__device__ __forceinline__ void tma_load_4d_pair(uint32_t dst,
+__device__ __forceinline__ void tma_load_5d_pair(uint32_t dst,
                                                  const CUtensorMap* m, int x,
-                                                 int y, int z, int w,
+                                                 int y, int z, int w, int v,
                                                  uint32_t bar_cluster) {
   asm volatile(
-      "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::"
-      "complete_tx::bytes [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+      "cp.async.bulk.tensor.5d.cta_group::2.shared::cluster.global.mbarrier::"
+      "complete_tx::bytes [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(x), "r"(y),
-      "r"(z), "r"(w)
+      "r"(z), "r"(w), "r"(v)
       : "memory");
 }
 // Contiguous global -> shared bulk copy into this CTA, completion counted on

@@ -18,10 +18,11 @@
 // Items, orientation and schedule follow the bf16 CTA-pair kernel: weight
 // rows on M (256 per item, 128 per CTA), tokens on N (at most 192 per item,
 // in equal chunks), shared experts first, dynamic claim order, item table
-// from the device offsets.  A stage is 128 of the reduction: 128-byte rows
-// of e4m3, 16 KB of weights and <= 12 KB of tokens per CTA, six stages.
-// Gate/up items load each CTA's weight half as one 4-D box (the CTA's 64
-// gate rows and the 64 up rows of the same intermediates), so SwiGLU pairs
+// from the device offsets.  A stage is 256 of the reduction: two 128-byte
+// K-atoms per row of e4m3, 32 KB of weights and <= 24 KB of tokens per CTA,
+// three stages (each K-atom is a 128-byte-swizzled block of its rows).
+// Gate/up items load each CTA's weight half as one 5-D box (per K-atom the
+// CTA's 64 gate rows and the 64 up rows of the same intermediates), so SwiGLU pairs
 // TMEM lanes l and l + 64 as in the bf16 kernel, and H leaves as fp32 (the
 // host requantizes it to e4m3 1 x 128 blocks for the down pass, from the
 // same fp32 values as the other e4m3 kernels; a bf16 H would round twice).
@@ -29,8 +30,9 @@
 // TMEM (512 columns per CTA): accumulators at columns 0 and 256 (192
 // columns each), four scale groups at columns 192, 224, 448 and 480 (A
 // scales 4 columns at +0, B scales 6 columns at +16).  One group holds the
-// scales of four consecutive stages: stage i of an item uses group i / 4 and
-// scale byte i % 4; the scale warps run up to three groups ahead.
+// scales of four consecutive 128-blocks of the reduction (two stages): the
+// MMAs of block kb use group kb / 4 and scale byte kb % 4; the scale warps
+// run up to three groups ahead.
 //
 // Scales travel apart from the operands, as UE8M0 tables written by the
 // quantizers (one byte per row and 128-block of the reduction, rows padded
@@ -56,7 +58,8 @@ namespace moe {
 
 constexpr int kF8PBM = 256;       // packed weight rows per item (128 per CTA)
 constexpr int kF8PBN = 192;       // max tokens per item
-constexpr int kF8PStages = 6;
+constexpr int kF8PStages = 3;
+constexpr int kF8PAtoms = 2;      // 128-byte K-atoms per stage
 constexpr int kF8PSfGroups = 4;   // scale groups in TMEM
 constexpr int kF8PMaxPitch = 64;  // UE8M0 row bytes (reductions <= 8192)
 // TMEM columns: accumulator a at a * 256; scale group g at 192 + 32 (g % 2)
@@ -96,8 +99,9 @@ struct F8PairParams {
 };
 
 struct F8PairSmem {
-  static constexpr int a_bytes = 128 * 128;        // 16 KB
-  static constexpr int b_bytes = 96 * 128;         // <= 96 token rows
+  static constexpr int a_atom = 128 * 128;         // 16 KB per K-atom
+  static constexpr int a_bytes = kF8PAtoms * a_atom;
+  static constexpr int b_bytes = kF8PAtoms * 96 * 128;   // <= 96 token rows
   static constexpr int a_off = 0;
   static constexpr int b_off = a_off + kF8PStages * a_bytes;
   static constexpr int stg_off = b_off + kF8PStages * b_bytes;
@@ -379,9 +383,9 @@ grouped_gemm_fp8_pair_kernel(const __grid_constant__ CUtensorMap tmA_r,
             : box == 64 ? (t.shared ? &tmB_s64 : &tmB_r64)
                         : (t.shared ? &tmB_s96 : &tmB_r96);
         const int b_row = t.b_row + static_cast<int>(rank) * half;
-        const uint32_t pair_bytes =
-            2u * static_cast<uint32_t>(L::a_bytes + box * 128);
-        const int nk = t.k / 128;
+        const uint32_t pair_bytes = 2u * static_cast<uint32_t>(
+                                        L::a_bytes + kF8PAtoms * box * 128);
+        const int nk = (t.k / 128 + kF8PAtoms - 1) / kF8PAtoms;   // stages
         bool ok = true;
         for (int i = 0; i < nk; ++i) {
           if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1, abort_flag,
@@ -393,17 +397,17 @@ grouped_gemm_fp8_pair_kernel(const __grid_constant__ CUtensorMap tmA_r,
           const uint32_t fb = full_L + 8 * stage;
           const uint32_t adst = sbase + L::a_off + stage * L::a_bytes;
           if (p.gate_up) {
-            // one 4-D box: the CTA's 64 gate rows (block a_row / 128, half
-            // `rank`) then the 64 up rows of the same intermediates (the
-            // next block, same half)
-            tma_load_4d_pair(adst, mA, i * 128, 0, static_cast<int>(rank),
-                             t.a_row >> 7, fb);
+            // one 5-D box: per K-atom, the CTA's 64 gate rows (block
+            // a_row / 128, half `rank`) then the 64 up rows of the same
+            // intermediates (the next block, same half)
+            tma_load_5d_pair(adst, mA, 0, 0, static_cast<int>(rank),
+                             t.a_row >> 7, kF8PAtoms * i, fb);
           } else {
-            tma_load_2d_pair(adst, mA, i * 128,
-                             t.a_row + static_cast<int>(rank) * 128, fb);
+            tma_load_3d_pair(adst, mA, t.a_row + static_cast<int>(rank) * 128,
+                             kF8PAtoms * i, fb);
           }
-          tma_load_2d_pair(sbase + L::b_off + stage * L::b_bytes, mB, i * 128,
-                           b_row, fb);
+          tma_load_3d_pair(sbase + L::b_off + stage * L::b_bytes, mB, b_row,
+                           kF8PAtoms * i, fb);
           ++issued;
           if (++stage == ST) {
             stage = 0;
@@ -457,10 +461,13 @@ grouped_gemm_fp8_pair_kernel(const __grid_constant__ CUtensorMap tmA_r,
           break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + f8p_acc_col(acc);
-        const int nk = t.k / 128;
+        const int nkb = t.k / 128;                              // blocks
+        const int nk = (nkb + kF8PAtoms - 1) / kF8PAtoms;       // stages
+        const uint32_t b_atom = static_cast<uint32_t>(
+            f8p_token_box(t.n_mma >> 1) * 128);
         bool ok = true;
         for (int i = 0; i < nk; ++i) {
-          if ((i & 3) == 0) {
+          if (((kF8PAtoms * i) & 3) == 0) {
             if (!mbar_wait_cl(bar_sffull + 8 * sfg, sf_phase, abort_flag,
                               KID_GEMM_FP8, 106)) {
               ok = false;
@@ -476,18 +483,26 @@ grouped_gemm_fp8_pair_kernel(const __grid_constant__ CUtensorMap tmA_r,
           const uint32_t a0 = sbase + L::a_off + stage * L::a_bytes;
           const uint32_t b0 = sbase + L::b_off + stage * L::b_bytes;
           const uint32_t sfa = tmem + f8p_sf_col(sfg);
-          const uint32_t idesc = idesc_mxf8_pair(t.n_mma, i & 3);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_mxf8_pair(d_tmem, sdesc_k128(a0 + 32 * kk),
-                          sdesc_k128(b0 + 32 * kk), idesc, sfa, sfa + 16,
-                          (i | kk) != 0);
+          for (int at = 0; at < kF8PAtoms; ++at) {
+            const int kb = kF8PAtoms * i + at;   // 128-block of the reduction
+            if (kb < nkb) {
+              const uint32_t idesc = idesc_mxf8_pair(t.n_mma, kb & 3);
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_mxf8_pair(d_tmem,
+                              sdesc_k128(a0 + at * L::a_atom + 32 * kk),
+                              sdesc_k128(b0 + at * b_atom + 32 * kk), idesc,
+                              sfa, sfa + 16, (kb | kk) != 0);
+            }
+          }
           mma_commit_pair_mc(bar_empty + 8 * stage, 0x3);
           if (++stage == ST) {
             stage = 0;
             phase ^= 1;
           }
-          if ((i & 3) == 3 || i == nk - 1) {   // the group's last stage
+          if (((kF8PAtoms * i + kF8PAtoms - 1) & 3) == 3 ||
+              i == nk - 1) {                   // the group's last stage
             mma_commit_pair_mc(bar_sfempty + 8 * sfg, 0x3);
             if (++sfg == kF8PSfGroups) {
               sfg = 0;

@@ -502,36 +502,51 @@ moe_status launch_gemm_pair(const PairMaps& m, const GemmParams& p,
   return MOE_OK;
 }
 
-// 4-D view of a packed e4m3 gate/up operand [rows, cols] as {cols, 64
-// rows, 2 halves, rows / 128 blocks} with a box of {128 bytes, 64, 1, 2}:
-// one load brings half h of row block w (gate) and the same half of block
-// w + 1 (up), 128-byte swizzle.
-moe_status make_map_u8_gu4d(CUtensorMap* m, const void* ptr, long long rows,
-                            long long cols) {
+// Tiled maps of e4m3 operands [rows, cols] (cols = the reduction) in
+// 128-byte K-atoms with 128-byte swizzle, two atoms per box:
+//   3-D {128, rows, cols/128}, box {128, box_rows, 2};
+//   5-D gate/up view {128, 64 rows, 2 halves, rows/128 blocks, cols/128}
+//   with a box of {128, 64, 1, 2, 2}: per atom, half h of row block w (gate)
+//   and the same half of block w + 1 (up).
+moe_status encode_u8(CUtensorMap* m, const void* ptr, int rank,
+                     const cuuint64_t* dims, const cuuint64_t* strides,
+                     const cuuint32_t* box) {
   moe_status st = get_encoder();
   if (st != MOE_OK) return st;
-  const long long blocks = rows / 128 > 0 ? rows / 128 : 1;
-  cuuint64_t dims[4] = {static_cast<cuuint64_t>(cols), 64, 2,
-                        static_cast<cuuint64_t>(blocks)};
-  cuuint64_t strides[3] = {static_cast<cuuint64_t>(cols),
-                           static_cast<cuuint64_t>(64 * cols),
-                           static_cast<cuuint64_t>(128 * cols)};
-  cuuint32_t box[4] = {128, 64, 1, 2};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4,
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, rank,
                         const_cast<void*>(ptr), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
-    return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled (4-D u8) failed (%d) "
-                "rows=%lld cols=%lld", static_cast<int>(r), rows, cols);
+    return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled (%d-D u8) failed (%d)",
+                rank, static_cast<int>(r));
   return MOE_OK;
 }
+moe_status make_map3_u8(CUtensorMap* m, const void* ptr, long long rows,
+                        long long cols, int box_rows) {
+  cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(rows > 0 ? rows : 1),
+                        static_cast<cuuint64_t>(cols / 128)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols), 128};
+  cuuint32_t box[3] = {128, static_cast<cuuint32_t>(box_rows), 2};
+  return encode_u8(m, ptr, 3, dims, strides, box);
+}
+moe_status make_map_u8_gu5d(CUtensorMap* m, const void* ptr, long long rows,
+                            long long cols) {
+  const long long blocks = rows / 128 > 0 ? rows / 128 : 1;
+  cuuint64_t dims[5] = {128, 64, 2, static_cast<cuuint64_t>(blocks),
+                        static_cast<cuuint64_t>(cols / 128)};
+  cuuint64_t strides[4] = {static_cast<cuuint64_t>(cols),
+                           static_cast<cuuint64_t>(64 * cols),
+                           static_cast<cuuint64_t>(128 * cols), 128};
+  cuuint32_t box[5] = {128, 64, 1, 2, 2};
+  return encode_u8(m, ptr, 5, dims, strides, box);
+}
 
-// Tensor maps of the e4m3 CTA-pair GEMM: weights (the 4-D gate/up view, or
+// Tensor maps of the e4m3 CTA-pair GEMM: weights (the 5-D gate/up view, or
 // 128-row boxes for the down pass) and tokens (32 / 64 / 96-row boxes),
-// routed and shared; 128-byte rows of e4m3 codes.
+// routed and shared; two 128-byte K-atoms of e4m3 codes per box.
 struct F8PairMaps {
   CUtensorMap a_r, a_s, b_r32, b_s32, b_r64, b_s64, b_r96, b_s96;
 };
@@ -543,20 +558,20 @@ moe_status f8_pair_maps(const void* w_r, long long w_r_rows, const void* x_r,
   moe_status st;
   auto wmap = [&](CUtensorMap* mm, const void* w, long long rows,
                   long long k) {
-    return a_box == 64 ? make_map_u8_gu4d(mm, w, rows, k)
-                       : make_map_u8(mm, w, rows, k, a_box);
+    return a_box == 64 ? make_map_u8_gu5d(mm, w, rows, k)
+                       : make_map3_u8(mm, w, rows, k, a_box);
   };
   if ((st = wmap(&m.a_r, w_r, w_r_rows, k_r)) != MOE_OK) return st;
   CUtensorMap* br[3] = {&m.b_r32, &m.b_r64, &m.b_r96};
   CUtensorMap* bs[3] = {&m.b_s32, &m.b_s64, &m.b_s96};
   const int boxes[3] = {32, 64, 96};
   for (int i = 0; i < 3; ++i)
-    if ((st = make_map_u8(br[i], x_r, x_r_rows, k_r, boxes[i])) != MOE_OK)
+    if ((st = make_map3_u8(br[i], x_r, x_r_rows, k_r, boxes[i])) != MOE_OK)
       return st;
   if (w_s != nullptr) {
     if ((st = wmap(&m.a_s, w_s, w_s_rows, k_s)) != MOE_OK) return st;
     for (int i = 0; i < 3; ++i)
-      if ((st = make_map_u8(bs[i], x_s, x_s_rows, k_s, boxes[i])) != MOE_OK)
+      if ((st = make_map3_u8(bs[i], x_s, x_s_rows, k_s, boxes[i])) != MOE_OK)
         return st;
   } else {
     m.a_s = m.a_r;

@@ -291,6 +291,18 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
           cluster_addr)
       : "memory");
 }
+// Arrive without release semantics, for hand-offs whose only payload is
+// tensor-memory state that the arriving thread has already waited on
+// (tcgen05.wait::ld / wait::st, then tcgen05.fence::before_thread_sync):
+// the consumer's tcgen05 work is ordered after the phase it observes, and a
+// release here would also wait for the thread's unrelated global stores.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(
+    uint32_t cluster_addr) {
+  asm volatile(
+      "mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(
+          cluster_addr)
+      : "memory");
+}
 __device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr,
                                                uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v)

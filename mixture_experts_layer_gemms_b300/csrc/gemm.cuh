@@ -157,15 +157,30 @@ __device__ __forceinline__ void epilogue_store(uint32_t taddr, int n_valid,
           static_cast<size_t>(b_row + n0) * ld + col0 + q * 32 + lane;
       if (y_fp16) {
         // fp16 keeps 11 significant bits (8x finer than bf16); values
-        // beyond its range are reported, never written silently as inf
-        __half* dst = static_cast<__half*>(out) + off;
+        // beyond its range are reported, never written silently as inf.
+        // The warp's 32 channels x 32 tokens are transposed through its
+        // 2 KB of the exchange buffer (token rows of 64 bytes) and leave as
+        // 16-byte stores, four lanes per token row.
+        __half* tile = reinterpret_cast<__half*>(xchg + q * 32 * 17);
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (j < nleft) {
-            const float v = __uint_as_float(r[j]);
-            overflow |= !(fabsf(v) <= 65504.f);
-            dst[static_cast<size_t>(j) * ld] = __float2half_rn(v);
-          }
+        for (int j = 0; j < 32; ++j) {
+          const float v = __uint_as_float(r[j]);
+          if (j < nleft) overflow |= !(fabsf(v) <= 65504.f);
+          tile[j * 32 + lane] = __float2half_rn(v);
+        }
+        __syncwarp();
+        __half* dst = static_cast<__half*>(out) +
+                      static_cast<size_t>(b_row + n0) * ld + col0 + q * 32;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int piece = lane + 32 * c;        // 16-byte piece of the tile
+          const int j = piece >> 2, part = piece & 3;
+          if (j < nleft)
+            *reinterpret_cast<uint4*>(dst + static_cast<size_t>(j) * ld +
+                                      8 * part) =
+                *reinterpret_cast<const uint4*>(tile + j * 32 + 8 * part);
+        }
+        __syncwarp();
       } else {
         float* dst = static_cast<float*>(out) + off;
 #pragma unroll

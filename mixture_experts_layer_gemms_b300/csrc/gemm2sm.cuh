@@ -423,7 +423,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA_r,
                      stg, q, ep, lane, p.y_fp16 != 0);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(tempty_L + 8 * acc);
+      if (lane == 0) mbar_arrive_cluster_relaxed(tempty_L + 8 * acc);
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1;

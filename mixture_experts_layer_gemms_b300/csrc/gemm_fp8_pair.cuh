@@ -552,7 +552,7 @@ grouped_gemm_fp8_pair_kernel(const __grid_constant__ CUtensorMap tmA_r,
                      stg, q, ep, lane, true, true);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(tempty_L + 8 * acc);
+      if (lane == 0) mbar_arrive_cluster_relaxed(tempty_L + 8 * acc);
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1;
@@ -615,7 +615,7 @@ grouped_gemm_fp8_pair_kernel(const __grid_constant__ CUtensorMap tmA_r,
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(sffull_L + 8 * sfg);
+        if (lane == 0) mbar_arrive_cluster_relaxed(sffull_L + 8 * sfg);
         if (++sfg == kF8PSfGroups) {
           sfg = 0;
           sf_phase ^= 1;

@@ -290,7 +290,7 @@ MOE_API int moe_last_launch_count(void);
  * kept in fp16 between the GEMMs (range checked).  Every call is
  * asynchronous on `stream`; the workspace (moe_backward_workspace_size,
  * 256-byte aligned) holds the per-assignment operands in a layout whose
- * expert segments are padded to 64 rows.
+ * expert segments are padded to 16 rows.
  * Supported: dtype MOE_BF16 and d_ff a multiple of 128 (else
  * MOE_ERR_UNSUPPORTED); every pointer 16-byte aligned (else
  * MOE_ERR_INVALID_ARG).                                                   */

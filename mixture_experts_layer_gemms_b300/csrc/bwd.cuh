@@ -164,8 +164,8 @@ bwd_gather_kernel(const __nv_bfloat16* __restrict__ dh,
 }
 
 // Zero rows offpad[e] + cnt[e] .. offpad[e+1] of the padded operands (X, dY
-// [.., d], H [.., I], dA [.., 2I]) and of dz: the Wgrad GEMMs read whole
-// 64-row blocks.  One CTA per expert.
+// [.., d], H [.., I], dA [.., 2I]) and of dz: the Wgrad GEMMs multiply
+// whole 16-row steps.  One CTA per expert.
 __global__ void __launch_bounds__(256)
 bwd_zero_pad_kernel(const int* __restrict__ offsets,
                     const int* __restrict__ offpad, int d, int I,

@@ -23,8 +23,10 @@
 //
 // Groups: the shared experts (all T tokens, one concatenated group) first,
 // then the routed experts.  Routed token rows live in a padded layout: group
-// e starts at offpad[e] (a multiple of 64) and holds cnt[e] rows, the rest
-// of its 64-row blocks zero, so a Wgrad K block never reaches another group.
+// e starts at offpad[e] (a multiple of 16) and holds cnt[e] rows, the rest
+// of its 16-row blocks zero.  A Wgrad K block (64 rows) may run into the
+// next group, but only its 16-row MMA steps up to the group's padded end
+// are issued, so no product ever takes another group's rows.
 #pragma once
 #include "common.cuh"
 #include "gemm.cuh"
@@ -32,7 +34,7 @@
 namespace moe {
 
 enum BwdKind : int { kDgrad = 0, kRecomp = 1, kWgrad = 2 };
-constexpr int kPadRows = 64;   // routed groups are padded to this many rows
+constexpr int kPadRows = 16;   // routed groups are padded to this many rows
 // epilogue staging: four warps x 32 x 33 floats (the Wgrad transpose; the
 // Recomp exchange uses the first 4 x 32 x 17)
 constexpr int kBwdStgBytes = 4 * 32 * 33 * 4;
@@ -109,9 +111,9 @@ struct BTile {
   int n_valid;   // tokens kinds: tokens; Wgrad: columns
   int n_mma;     // MMA N
   int k_row0;    // first K row of the MN-major operands (Dgrad A, Wgrad A/B)
-  int nk;        // K blocks (64 rows; 128 on CTA pairs)
-  int krows;     // CTA-pair Wgrad: K rows to multiply (the last block may
-                 // hold only 64 of its 128)
+  int nk;        // K blocks (64 rows; 128 for the CTA-pair token kinds)
+  int krows;     // K rows to multiply, a multiple of 16 (a Wgrad group's
+                 // last block may hold fewer rows than the block)
 };
 
 // Item tables in shared memory: offpad, cnt and (tokens kinds) the prefix
@@ -135,6 +137,7 @@ __device__ __forceinline__ BTile bwd_decode(int item, const BwdParams& p,
       ncols = p.n_shared;
       t.k_row0 = 0;
       t.nk = (p.shared_rows + kGemmBK - 1) / kGemmBK;
+      t.krows = t.nk * kGemmBK;       // rows past T read as zero
     } else {
       const int j = item - n_items_s;
       t.shared = 0;
@@ -143,7 +146,8 @@ __device__ __forceinline__ BTile bwd_decode(int item, const BwdParams& p,
       ntn = ntn_r;
       ncols = p.n_routed;
       t.k_row0 = offp[t.e];
-      t.nk = (cnt[t.e] + kGemmBK - 1) / kGemmBK;
+      t.krows = (cnt[t.e] + kPadRows - 1) / kPadRows * kPadRows;
+      t.nk = (t.krows + kGemmBK - 1) / kGemmBK;
     }
     t.wt = local / ntn;
     t.m0 = t.wt * kGemmBM;
@@ -182,6 +186,7 @@ __device__ __forceinline__ BTile bwd_decode(int item, const BwdParams& p,
     }
     t.m0 = t.wt * kGemmBM;
     t.n_mma = (t.n_valid + 15) & ~15;
+    t.krows = t.nk * kGemmBK;
   }
   return t;
 }
@@ -597,8 +602,12 @@ bwd_gemm_kernel(const __grid_constant__ CUtensorMap tmA_r,
           tc_fence_after();
           const uint32_t a0 = sbase + L::a_off + stage * L::a_bytes;
           const uint32_t b0 = sbase + L::b_off + stage * L::b_bytes;
+          // 16-row K steps in this block (a Wgrad group's last block may
+          // end early)
+          const int nkk = min(kGemmBK, t.krows - i * kGemmBK) / 16;
 #pragma unroll
           for (int kk = 0; kk < kGemmBK / 16; ++kk) {
+            if (kk >= nkk) break;
             const uint64_t ad = kAmn ? sdesc_mn128(a0 + kk * 2048, 8192)
                                      : sdesc_k128(a0 + kk * 32);
             const uint64_t bd = kBmn ? sdesc_mn128(b0 + kk * 2048, 8192)

@@ -90,7 +90,8 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a,
 
 // kWgrad epilogue on CTA pairs: one warp's 32 accumulator rows x 128 of
 // the tile's 256 columns (`cbeg` .. +128; two warps share each TMEM lane
-// quarter), 32 columns at a time: TMEM -> registers -> a box in the warp's
+// quarter): TMEM -> registers (all 128 columns, then the accumulator is
+// released), then 32 columns at a time -> a box in the warp's
 // 2 KB of shared memory, laid out as the output map's 64-byte swizzle
 // expects (rows of 64 bytes: 32 bf16 or 16 fp32 columns) -> one TMA store
 // per box, issued by lane 0.  The global writes leave as whole boxes, off
@@ -110,24 +111,37 @@ __device__ __forceinline__ void wgrad_store_box(const CUtensorMap* map, int c,
   bulk_commit();
 }
 
-__device__ __forceinline__ void bwd_ep_wgrad_tma(uint32_t taddr, int cbeg,
-                                                 bool zero,
+// The warp's 128 accumulator columns, read from TMEM into registers in one
+// go (four 32-column loads, one wait) so the accumulator can be handed back
+// to the MMA before any of it is stored; zeros for a group with no rows.
+__device__ __forceinline__ void bwd_ep_wgrad_take(uint32_t taddr, int cbeg,
+                                                  bool zero,
+                                                  uint32_t (&r)[4][32]) {
+  if (!zero) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) tmem_ld32(taddr + cbeg + 32 * j, r[j]);
+    tmem_ld_wait();
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int k = 0; k < 32; ++k) r[j][k] = 0u;
+  }
+}
+
+// Stores what bwd_ep_wgrad_take read: each 32-column chunk becomes one bf16
+// box (or two fp32 boxes) in the warp's ring, then a TMA store.
+__device__ __forceinline__ void bwd_ep_wgrad_put(const uint32_t (&r)[4][32],
+                                                 int cbeg,
                                                  const CUtensorMap* map,
                                                  int n0, int y, int col_split,
                                                  int s_rows, bool bf16,
                                                  uint32_t ring_base,
                                                  int& ring, int lane) {
   const int sw = (lane >> 1) & 3;            // 64-byte swizzle of this row
-#pragma unroll 1
-  for (int c0 = cbeg; c0 < cbeg + 128; c0 += 32) {
-    uint32_t r[32];
-    if (!zero) {
-      tmem_ld32(taddr + c0, r);
-      tmem_ld_wait();
-    } else {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) r[j] = 0u;
-    }
+  for (int j = 0; j < 4; ++j) {
+    const int c0 = cbeg + 32 * j;
     if (bf16) {            // one box of 32 columns
       const uint32_t buf = ring_base + (ring % kWgradBoxes) * 2048u;
       const uint32_t row_addr = buf + lane * 64;
@@ -137,7 +151,7 @@ __device__ __forceinline__ void bwd_ep_wgrad_tma(uint32_t taddr, int cbeg,
       __syncwarp();
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
-#define MOE_F(k) __uint_as_float(r[cc * 8 + (k)])
+#define MOE_F(k) __uint_as_float(r[j][cc * 8 + (k)])
         st_shared_v4(row_addr + ((cc ^ sw) * 16),
                      pack_bf16x2(MOE_F(0), MOE_F(1)),
                      pack_bf16x2(MOE_F(2), MOE_F(3)),
@@ -158,9 +172,9 @@ __device__ __forceinline__ void bwd_ep_wgrad_tma(uint32_t taddr, int cbeg,
         __syncwarp();
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc)
-          st_shared_v4(row_addr + ((cc ^ sw) * 16), r[hb * 16 + cc * 4],
-                       r[hb * 16 + cc * 4 + 1], r[hb * 16 + cc * 4 + 2],
-                       r[hb * 16 + cc * 4 + 3]);
+          st_shared_v4(row_addr + ((cc ^ sw) * 16), r[j][hb * 16 + cc * 4],
+                       r[j][hb * 16 + cc * 4 + 1], r[j][hb * 16 + cc * 4 + 2],
+                       r[j][hb * 16 + cc * 4 + 3]);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0)
@@ -523,7 +537,7 @@ bwd_gemm_pair_kernel(const __grid_constant__ BwdPairMaps maps,
           const uint32_t a0 = sbase + L::a_off + stage * L::a_bytes;
           const uint32_t b0 = sbase + L::b_off + stage * L::b_bytes;
           // 16-row K steps in this stage (a Wgrad group's last block may
-          // hold 64 rows)
+          // end early)
           const int nkk = min(BK, t.krows - i * BK) / 16;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
@@ -621,14 +635,23 @@ bwd_gemm_pair_kernel(const __grid_constant__ BwdPairMaps maps,
             s_rows = p.m_shared;
           }
         }
-        bwd_ep_wgrad_tma(ta, (ep >> 2) * 128, t.nk == 0, om, t.n0, y,
-                         col_split, s_rows, p.out_bf16 != 0,
+        uint32_t r[4][32];
+        bwd_ep_wgrad_take(ta, (ep >> 2) * 128, t.nk == 0, r);
+        // the accumulator is free once its columns are in registers: hand
+        // it back before the stores, so the MMA runs on while they drain
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster_relaxed(tempty_L + 8 * acc);
+        bwd_ep_wgrad_put(r, (ep >> 2) * 128, om, t.n0, y, col_split, s_rows,
+                         p.out_bf16 != 0,
                          smem_u32(stg) + ep * (kWgradBoxes * 2048u), ring,
                          lane);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(tempty_L + 8 * acc);
+      if constexpr (KIND != kWgrad) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(tempty_L + 8 * acc);
+      }
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1;

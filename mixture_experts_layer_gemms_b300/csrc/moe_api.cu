@@ -1490,9 +1490,9 @@ namespace {
 constexpr int kBwdCounters = 8;
 
 // Workspace of moe_backward.  Per-assignment operands live in a padded
-// layout: expert e's rows start at offpad[e] (a multiple of 64) and its
-// segment is a whole number of 64-row blocks, so the layout needs at most
-// A + 63 N rows (A = T K).
+// layout: expert e's rows start at offpad[e] (a multiple of 16) and its
+// segment is a whole number of 16-row blocks, so the layout needs at most
+// A + 15 N rows (A = T K).
 struct BwdLayout {
   long long A_pad;
   size_t ctr, offs, offpad, dz, X, dY, dH, H, dA, dX, dH_s, H_s, dA_s, dX_s,

@@ -489,16 +489,17 @@ def _free():
 
 def time_backward(args, cfg, layer, u, dev, ws, peaks):
     """The layer backward (moe_backward: Dgrad and Wgrad GEMMs, gate and
-    centroid gradients) after a forward on the same batch, timed with CUDA
-    events on the launching stream; and a training step (forward + backward)
-    timed over the same number of steps.  Weight gradients in bf16."""
+    centroid gradients) after a forward on the same batch that saved its
+    gate/up pre-activations, timed with CUDA events on the launching stream;
+    and a training step (that forward + backward) timed over the same number
+    of steps.  Weight gradients in bf16."""
     import mixture_experts_layer_gemms_b300 as moe
     dh = upstream_grad(cfg, dev)
     stream = torch.cuda.current_stream()
     gd = torch.bfloat16
     layer.overlap_shared = False
     for _ in range(max(3, args.warmup)):
-        layer(u)
+        layer(u, save_for_backward=True)
         layer.backward(u, dh, grad_dtype=gd)
     torch.cuda.synchronize()
     moe.get_device_error()
@@ -511,7 +512,7 @@ def time_backward(args, cfg, layer, u, dev, ws, peaks):
     t0.record(stream)
     for i in range(steps):
         ev[i][0].record(stream)
-        layer(u)
+        layer(u, save_for_backward=True)
         ev[i][1].record(stream)
         layer.backward(u, dh, grad_dtype=gd)
         ev[i][2].record(stream)
@@ -521,16 +522,17 @@ def time_backward(args, cfg, layer, u, dev, ws, peaks):
     bw_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
     train_ms = max_over_ranks(t0.elapsed_time(t1), dev) / steps
     rows = cfg.T * cfg.top_k + cfg.n_shared * cfg.T
-    # algorithmic: twice the expert FFNs' forward FLOPs (Dgrad + Wgrad);
-    # executed adds the recomputed gate/up GEMM
+    # algorithmic = executed: twice the expert FFNs' forward FLOPs (Dgrad +
+    # Wgrad); the gate/up pre-activations come from the forward, so no
+    # GEMM is recomputed
     alg = 12.0 * cfg.d * cfg.d_ff * rows
-    exe = 16.0 * cfg.d * cfg.d_ff * rows
+    exe = alg
     pk = peaks["bf16_tflops"]
     ach = alg / (bw_ms / 1e3) / 1e12
     roof = {"bound": "tensor", "achieved": ach, "peak": pk,
             "unit": "TFLOP/s", "frac": ach / pk, "traffic": None,
-            "kernel": "the moe_backward call (Dgrad, recompute and Wgrad "
-                      "CTA-pair GEMMs are 95% of it); algorithmic FLOPs "
+            "kernel": "the moe_backward call (its Dgrad and Wgrad CTA-pair "
+                      "GEMMs are ~95% of it); algorithmic FLOPs "
                       "12 d d_ff per token-expert and per shared-expert "
                       "token",
             "peak_source": f"{peaks['source']} bf16_tflops (burst)"}
@@ -541,10 +543,11 @@ def time_backward(args, cfg, layer, u, dev, ws, peaks):
             "executed_tflops": exe / (bw_ms / 1e3) / 1e12,
             "executed_frac_of_bf16_peak": exe / (bw_ms / 1e3) / 1e12 / pk,
             "grad_dtype": "bf16", "gpu_launches_per_call": n_launch,
-            "note": "moe_backward after a forward of the same batch: "
-                    "gather, Dgrad (down, gate/up), gate/up recompute with "
-                    "the SwiGLU backward, Wgrad (gate/up, down), centroid "
-                    "and input gradients"}
+            "note": "moe_backward after a forward of the same batch that "
+                    "saved its gate/up pre-activations (fp16): gather, Dgrad "
+                    "(down, with the SwiGLU backward in its epilogue; "
+                    "gate/up), Wgrad (gate/up, down), centroid and input "
+                    "gradients"}
 
 
 def forward_block(args, cfg, moe, dev, ws, rank, local, headline):

@@ -221,6 +221,31 @@ MOE_API moe_status moe_expert_ffn_part(const moe_shape* shape, int part,
                                        void* workspace,
                                        size_t workspace_bytes, void* stream);
 
+/* moe_expert_ffn for a training step (bf16 layers only, else
+ * MOE_ERR_UNSUPPORTED): the same outputs, bit for bit, and the gate and up
+ * pre-activations a = W_gate x, c = W_up x of every row, rounded to fp16
+ * (11 significant bits, the precision of the recomputing path to within
+ * its other roundings; a value outside the fp16 range is reported as
+ * MOE_ERR_DEVICE_CHECK by moe_get_device_error), for moe_backward, which
+ * then skips recomputing them.
+ *  act [T*K, 2*d_ff] fp16: row = x_perm slot; act_shared [T, 2*S*d_ff]
+ *  fp16: row = token (may be NULL when n_shared == 0).  Columns are in the
+ *  packed order of moe_pack_weights (blocks of 64 gate then 64 up values);
+ *  the layout is for moe_backward only.  The caller owns both buffers and
+ *  keeps them until the backward has read them.  act NULL ->
+ *  MOE_ERR_INVALID_ARG.                                                   */
+MOE_API moe_status moe_expert_ffn_train(const moe_shape* shape,
+                                        const void* x_perm,
+                                        const int32_t* offsets,
+                                        const void* w_gu_packed,
+                                        const void* w_down, const void* u,
+                                        const void* ws_gu_packed,
+                                        const void* ws_down_packed,
+                                        void* y_perm, void* y_shared,
+                                        void* act, void* act_shared,
+                                        void* workspace,
+                                        size_t workspace_bytes, void* stream);
+
 /* Combine (FFN-output equation):
  *  h[t] = u[t] + y_shared[t] + sum_k topk_gate[t,k] * y_perm[inv[t,k]],
  * accumulated in fp32 in that order; h is written as h_dtype.  y_shared may
@@ -280,14 +305,19 @@ MOE_API int moe_last_launch_count(void);
  * Inputs: the forward's own tensors: u [T, d], centroids [N, d] (bf16),
  * topk_idx / topk_gate [T, K] (moe_route), offsets [N+1] and inv [T, K]
  * (moe_permute), y_perm [T*K, d] fp16 (moe_expert_ffn), the packed weights
- * of moe_pack_weights and w_down; dh [T, d] bf16.
+ * of moe_pack_weights and w_down; dh [T, d] bf16.  act / act_shared: the
+ * pre-activations saved by moe_expert_ffn_train on the same batch, or both
+ * NULL; with them the SwiGLU backward runs in the epilogue of the dH GEMM
+ * from the saved a, c (and dH in fp32), without them a and c are recomputed
+ * by a third gate/up GEMM.
  * Outputs (overwritten, not accumulated): du [T, d] fp32, dE [N, d] fp32;
  * dw_gate / dw_up [N, d_ff, d], dw_down [N, d, d_ff] and, when
  * n_shared > 0, dws_gate / dws_up [S, d_ff, d], dws_down [S, d, d_ff] in
  * the canonical (unpacked) layouts, as grad_dtype (MOE_F32 or MOE_BF16).
  * Arithmetic: bf16 GEMM operands (x, dY, H, dA rounded to bf16; a, c
- * recomputed), fp32 accumulation in TMEM; dH and the input-side products
- * kept in fp16 between the GEMMs (range checked).  Every call is
+ * saved in fp16 or recomputed in fp32), fp32 accumulation in TMEM; the
+ * recomputing path keeps dH in fp16 between its GEMMs, and both keep the
+ * input-side products in fp16 (range checked).  Every call is
  * asynchronous on `stream`; the workspace (moe_backward_workspace_size,
  * 256-byte aligned) holds the per-assignment operands in a layout whose
  * expert segments are padded to 16 rows.
@@ -300,6 +330,7 @@ MOE_API moe_status moe_backward(
     const moe_shape* shape, const void* dh, const void* u,
     const void* centroids, const int32_t* topk_idx, const float* topk_gate,
     const int32_t* offsets, const int32_t* inv, const void* y_perm,
+    const void* act, const void* act_shared,
     const void* w_gu_packed, const void* w_down, const void* ws_gu_packed,
     const void* ws_down_packed, float* du, float* dE, void* dw_gate,
     void* dw_up, void* dw_down, void* dws_gate, void* dws_up, void* dws_down,

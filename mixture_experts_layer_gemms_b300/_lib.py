@@ -29,7 +29,8 @@ EXPORTED = ("moe_workspace_size", "moe_pack_weights", "moe_route",
             "moe_route_noalloc", "moe_selftest_wait_timeout",
             "moe_route_grouped", "moe_fp8_weight_bytes",
             "moe_pack_weights_fp8", "moe_x_perm_bytes", "moe_expert_ffn_part",
-            "moe_backward_workspace_size", "moe_backward")
+            "moe_backward_workspace_size", "moe_backward",
+            "moe_expert_ffn_train")
 
 
 class MoEError(RuntimeError):
@@ -73,7 +74,8 @@ def _load() -> ctypes.CDLL:
         "moe_x_perm_bytes": [SP, ctypes.POINTER(ctypes.c_size_t)],
         "moe_expert_ffn_part": [SP, I, P, P, P, P, P, P, P, P, P, P, Z, V],
         "moe_backward_workspace_size": [SP, ctypes.POINTER(ctypes.c_size_t)],
-        "moe_backward": [SP] + [P] * 20 + [I, P, Z, V],
+        "moe_backward": [SP] + [P] * 22 + [I, P, Z, V],
+        "moe_expert_ffn_train": [SP] + [P] * 12 + [Z, V],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -213,6 +215,19 @@ def expert_ffn(shape, x_perm, offsets, w_gu_packed, w_down, u, ws_gu_packed,
                               _stream(stream)), "moe_expert_ffn")
 
 
+def expert_ffn_train(shape, x_perm, offsets, w_gu_packed, w_down, u,
+                     ws_gu_packed, ws_down_packed, y_perm, y_shared, act,
+                     act_shared, workspace, stream=None) -> None:
+    """expert_ffn that also stores the gate/up pre-activations (fp16) in act
+    [T*K, 2*d_ff] and act_shared [T, 2*S*d_ff] for backward()."""
+    _check(LIB.moe_expert_ffn_train(
+        ctypes.byref(shape), _ptr(x_perm), _ptr(offsets), _ptr(w_gu_packed),
+        _ptr(w_down), _ptr(u), _ptr(ws_gu_packed), _ptr(ws_down_packed),
+        _ptr(y_perm), _ptr(y_shared), _ptr(act), _ptr(act_shared),
+        _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)), "moe_expert_ffn_train")
+
+
 def expert_ffn_part(shape, part, x_perm, offsets, w_gu_packed, w_down, u,
                     ws_gu_packed, ws_down_packed, y_perm, y_shared, workspace,
                     stream=None) -> None:
@@ -236,14 +251,16 @@ def backward_workspace_size(shape: MoeShape) -> int:
 def backward(shape, dh, u, centroids, topk_idx, topk_gate, offsets, inv,
              y_perm, w_gu_packed, w_down, ws_gu_packed, ws_down_packed, du, dE,
              dw_gate, dw_up, dw_down, dws_gate, dws_up, dws_down, workspace,
-             stream=None) -> None:
+             stream=None, act=None, act_shared=None) -> None:
     """Gradients of the layer for dh; the weight gradients' dtype (fp32 or
-    bf16) is taken from dw_gate."""
+    bf16) is taken from dw_gate.  act / act_shared: the pre-activations of
+    expert_ffn_train on the same batch (else they are recomputed)."""
     gd = MOE_BF16 if dw_gate.dtype == torch.bfloat16 else MOE_F32
     _check(LIB.moe_backward(
         ctypes.byref(shape), _ptr(dh), _ptr(u), _ptr(centroids),
         _ptr(topk_idx), _ptr(topk_gate), _ptr(offsets), _ptr(inv),
-        _ptr(y_perm), _ptr(w_gu_packed), _ptr(w_down), _ptr(ws_gu_packed),
+        _ptr(y_perm), _ptr(act), _ptr(act_shared), _ptr(w_gu_packed),
+        _ptr(w_down), _ptr(ws_gu_packed),
         _ptr(ws_down_packed), _ptr(du), _ptr(dE), _ptr(dw_gate), _ptr(dw_up),
         _ptr(dw_down), _ptr(dws_gate), _ptr(dws_up), _ptr(dws_down), gd,
         _ptr(workspace), workspace.numel() * workspace.element_size(),

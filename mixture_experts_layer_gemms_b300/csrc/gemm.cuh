@@ -55,6 +55,13 @@ struct GemmParams {
   int swiglu;
   int y_fp16;           // down pass: store Y as fp16 (else fp32)
   int* item_counter;    // zeroed before the launch; CTAs claim items from it
+  // bf16 gate/up pass: when not null, the gate and up pre-activations are
+  // also stored (fp16, range checked; packed column order, the row of H)
+  // for the backward
+  __half* act_routed;
+  long long ld_act_routed;
+  __half* act_shared;
+  long long ld_act_shared;
 };
 
 template <int BN, int STAGES>
@@ -144,7 +151,9 @@ __device__ __forceinline__ void epilogue_store(uint32_t taddr, int n_valid,
                                                bool swiglu, float* xchg, int q,
                                                int ep, int lane,
                                                bool y_fp16 = false,
-                                               bool h_fp32 = false) {
+                                               bool h_fp32 = false,
+                                               __half* act = nullptr,
+                                               long long ld_act = 0) {
   (void)ep;
   bool overflow = false;
   for (int n0 = 0; n0 < n_valid; n0 += 32) {
@@ -188,6 +197,21 @@ __device__ __forceinline__ void epilogue_store(uint32_t taddr, int n_valid,
           if (j < nleft) dst[static_cast<size_t>(j) * ld] = __uint_as_float(r[j]);
       }
       continue;
+    }
+    if (act != nullptr) {
+      // the pre-activation of packed row q*32 + lane (gate rows 0..63, up
+      // rows 64..127 of H columns col0 ..) for the backward, in fp16 (11
+      // significant bits; out of range is reported like y); a warp's 32
+      // lanes write 64 contiguous bytes of each token row
+      __half* ad = act + static_cast<size_t>(b_row + n0) * ld_act +
+                   2 * col0 + q * 32 + lane;
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < nleft) {
+          const float v = __uint_as_float(r[j]);
+          overflow |= !(fabsf(v) <= 65504.f);
+          ad[static_cast<size_t>(j) * ld_act] = __float2half_rn(v);
+        }
     }
     const bool gate_warp = q < 2;
     const int pair_q = q & 1;               // warps q and q+2 form a pair
@@ -503,7 +527,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA_r,
       epilogue_store(tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * BN,
                      t.n_valid, t.b_row, out, ld,
                      p.swiglu ? t.wt * 64 : t.wt * 128, p.swiglu != 0, stg,
-                     q, ep, lane, p.y_fp16 != 0);
+                     q, ep, lane, p.y_fp16 != 0, false,
+                     t.shared ? p.act_shared : p.act_routed,
+                     t.shared ? p.ld_act_shared : p.ld_act_routed);
       tc_fence_before();
       mbar_arrive(bar_tempty + 8 * acc);
       if (++acc == 2) {

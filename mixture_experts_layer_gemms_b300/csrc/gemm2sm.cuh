@@ -420,7 +420,9 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA_r,
                          acc * kPairBN,
                      t.n_valid, t.b_row, out, ld,
                      p.swiglu ? tile128 * 64 : tile128 * 128, p.swiglu != 0,
-                     stg, q, ep, lane, p.y_fp16 != 0);
+                     stg, q, ep, lane, p.y_fp16 != 0, false,
+                     t.shared ? p.act_shared : p.act_routed,
+                     t.shared ? p.ld_act_shared : p.ld_act_routed);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster_relaxed(tempty_L + 8 * acc);

@@ -77,6 +77,11 @@ struct BwdParams {
   void* out2_r; long long ld2_r;     // Recomp: dA;   Wgrad gate/up: W_up grad
   void* out2_s; long long ld2_s;
   const __half* dh_r;  const __half* dh_s;   // Recomp: dH [token][i]
+  // Dgrad of the down projection: when not null, the forward's saved
+  // pre-activations [forward row][2I] (fp16, packed order); the epilogue
+  // then writes H to out and dA to out2 instead of dH (no recompute pass)
+  const __half* act_r;  long long ld_act_r;
+  const __half* act_s;  long long ld_act_s;
   int wgrad_gu;          // Wgrad: 1 gate/up (unpack rows), 0 down
   int out_bf16;          // Wgrad: gradients stored as bf16 (else fp32)
   int* item_counter;
@@ -211,6 +216,57 @@ __device__ __forceinline__ void bwd_ep_dgrad(uint32_t taddr, int n_valid,
         ovf |= !(fabsf(v) <= 65504.f);
         dst[static_cast<size_t>(j) * ld] = __float2half_rn(v);
       }
+  }
+}
+
+// kDgrad of the down projection with the SwiGLU backward taken from the
+// forward's saved pre-activations.  The thread's M row is intermediate
+// column i = `col`; the accumulator holds dH (fp32) for 32 tokens per load.
+// a and c of padded row `row` are at act[row + shift][ca] and [ca + 64]
+// (fp16, packed order: ca = 128 (i / 64) + i % 64; shift maps the padded
+// row to the forward's row), and
+//   H[row][i]        = SiLU(a) c                                (bf16)
+//   dA[row][ca]      = dH c SiLU'(a)   (gate half)              (bf16)
+//   dA[row][ca + 64] = dH SiLU(a)      (up half)                (bf16)
+// dH stays fp32 here (the recompute path rounds it to fp16 in between).
+__device__ __forceinline__ void bwd_ep_dgrad_act(
+    uint32_t taddr, int n_valid, int b_row, int col, long long shift,
+    const __half* __restrict__ act, long long ld_act,
+    __nv_bfloat16* H, long long ld_h, __nv_bfloat16* dA, long long ld_a) {
+  const int ca = (col >> 6) * 128 + (col & 63);
+  for (int n0 = 0; n0 < n_valid; n0 += 32) {
+    const int nleft = n_valid - n0;
+    // the chunk's a and c, loaded before the TMEM read so that their
+    // latency overlaps it
+    const __half* src =
+        act + static_cast<size_t>(b_row + n0 + shift) * ld_act + ca;
+    __half av[32], cv[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if (j < nleft) {
+        av[j] = src[static_cast<size_t>(j) * ld_act];
+        cv[j] = src[static_cast<size_t>(j) * ld_act + 64];
+      } else {
+        av[j] = cv[j] = __float2half_rn(0.f);
+      }
+    }
+    uint32_t r[32];
+    tmem_ld32(taddr + n0, r);
+    tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if (j >= nleft) continue;
+      const float a = __half2float(av[j]);
+      const float c = __half2float(cv[j]);
+      const float g = __uint_as_float(r[j]);
+      const float sg = 1.0f / (1.0f + expf(-a));
+      const float si = a * sg;
+      const size_t row = static_cast<size_t>(b_row + n0 + j);
+      H[row * ld_h + col] = __float2bfloat16_rn(si * c);
+      dA[row * ld_a + ca] =
+          __float2bfloat16_rn(g * c * (sg * (1.0f + a * (1.0f - sg))));
+      dA[row * ld_a + ca + 64] = __float2bfloat16_rn(g * si);
+    }
   }
 }
 
@@ -665,9 +721,22 @@ bwd_gemm_kernel(const __grid_constant__ CUtensorMap tmA_r,
           tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
       const int row = q * 32 + lane;   // M row of the tile
       if constexpr (KIND == kDgrad) {
-        __half* out = static_cast<__half*>(t.shared ? p.out_s : p.out_r);
-        const long long ld = t.shared ? p.ld_s : p.ld_r;
-        bwd_ep_dgrad(ta, t.n_valid, t.n0, out, ld, t.m0 + row, ovf);
+        const __half* act = t.shared ? p.act_s : p.act_r;
+        if (act != nullptr) {
+          const long long shift =
+              t.shared ? 0 : static_cast<long long>(p.offsets[t.e]) - offp[t.e];
+          bwd_ep_dgrad_act(
+              ta, t.n_valid, t.n0, t.m0 + row, shift, act,
+              t.shared ? p.ld_act_s : p.ld_act_r,
+              static_cast<__nv_bfloat16*>(t.shared ? p.out_s : p.out_r),
+              t.shared ? p.ld_s : p.ld_r,
+              static_cast<__nv_bfloat16*>(t.shared ? p.out2_s : p.out2_r),
+              t.shared ? p.ld2_s : p.ld2_r);
+        } else {
+          __half* out = static_cast<__half*>(t.shared ? p.out_s : p.out_r);
+          const long long ld = t.shared ? p.ld_s : p.ld_r;
+          bwd_ep_dgrad(ta, t.n_valid, t.n0, out, ld, t.m0 + row, ovf);
+        }
       } else if constexpr (KIND == kRecomp) {
         bwd_ep_recomp(ta, t.n_valid, t.n0, t.wt,
                       t.shared ? p.dh_s : p.dh_r,

@@ -604,9 +604,23 @@ bwd_gemm_pair_kernel(const __grid_constant__ BwdPairMaps maps,
           tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * kBwdPairBN;
       const int m_cta = t.m0 + static_cast<int>(rank) * 128;  // CTA's rows
       if constexpr (KIND == kDgrad) {
-        __half* out = static_cast<__half*>(t.shared ? p.out_s : p.out_r);
-        const long long ld = t.shared ? p.ld_s : p.ld_r;
-        bwd_ep_dgrad(ta, t.n_valid, t.n0, out, ld, m_cta + q * 32 + lane, ovf);
+        const __half* act = t.shared ? p.act_s : p.act_r;
+        if (act != nullptr) {
+          const long long shift =
+              t.shared ? 0 : static_cast<long long>(p.offsets[t.e]) - offp[t.e];
+          bwd_ep_dgrad_act(
+              ta, t.n_valid, t.n0, m_cta + q * 32 + lane, shift, act,
+              t.shared ? p.ld_act_s : p.ld_act_r,
+              static_cast<__nv_bfloat16*>(t.shared ? p.out_s : p.out_r),
+              t.shared ? p.ld_s : p.ld_r,
+              static_cast<__nv_bfloat16*>(t.shared ? p.out2_s : p.out2_r),
+              t.shared ? p.ld2_s : p.ld2_r);
+        } else {
+          __half* out = static_cast<__half*>(t.shared ? p.out_s : p.out_r);
+          const long long ld = t.shared ? p.ld_s : p.ld_r;
+          bwd_ep_dgrad(ta, t.n_valid, t.n0, out, ld, m_cta + q * 32 + lane,
+                       ovf);
+        }
       } else if constexpr (KIND == kRecomp) {
         const int grp = ep >> 2;            // exchange group of 4 warps
         bwd_ep_recomp(ta, t.n_valid, t.n0, m_cta / 128,

@@ -1115,10 +1115,20 @@ static moe_status expert_ffn_impl(const moe_shape* s, int part,
                                   const void* u, const void* ws_gu_packed,
                                   const void* ws_down_packed, void* y_perm,
                                   void* y_shared, void* ws, size_t ws_bytes,
-                                  void* stream) {
+                                  void* stream, void* act = nullptr,
+                                  void* act_shared = nullptr) {
   g_launches = 0;
   moe_status st = check_shape(s);
   if (st != MOE_OK) return st;
+  const bool save = act != nullptr || act_shared != nullptr;
+  if (save) {
+    if (s->dtype != MOE_BF16)
+      return fail(MOE_ERR_UNSUPPORTED,
+                  "saved pre-activations: bf16 layers only (dtype %d)",
+                  static_cast<int>(s->dtype));
+    if (s->T > 0) NEED_PTR(act);
+    if (s->T > 0 && s->n_shared > 0) NEED_PTR(act_shared);
+  }
   if (part < 0 || part > 2)
     return fail(MOE_ERR_INVALID_ARG, "part=%d (0 both, 1 routed, 2 shared)",
                 part);
@@ -1235,6 +1245,12 @@ static moe_status expert_ffn_impl(const moe_shape* s, int part,
   p.ld_shared = SI;
   p.swiglu = 1;
   p.item_counter = ctr;
+  if (save) {   // rows as H's: x_perm slots (routed), tokens (shared)
+    p.act_routed = static_cast<__half*>(act);
+    p.ld_act_routed = 2LL * I;
+    p.act_shared = static_cast<__half*>(act_shared);
+    p.ld_act_shared = 2LL * SI;
+  }
   if (pair) {
     if ((st = pair_maps(wgu_r, rows_gu_r, xr, rows_x_r, d,
                         has_shared ? ws_gu_packed : nullptr, 2LL * SI,
@@ -1273,6 +1289,7 @@ static moe_status expert_ffn_impl(const moe_shape* s, int part,
   p.swiglu = 0;
   p.y_fp16 = 1;
   p.item_counter = ctr + 1;
+  p.act_routed = p.act_shared = nullptr;
   if (pair) {
     if ((st = pair_maps(wd_r, rows_d_r, hr_, rows_x_r, k_r2,
                         has_shared ? ws_down_packed : nullptr, d, h_s, s->T,
@@ -1305,6 +1322,19 @@ moe_status moe_expert_ffn_part(const moe_shape* s, int part,
   return expert_ffn_impl(s, part, x_perm, offsets, w_gu_packed, w_down, u,
                          ws_gu_packed, ws_down_packed, y_perm, y_shared, ws,
                          ws_bytes, stream);
+}
+
+moe_status moe_expert_ffn_train(const moe_shape* s, const void* x_perm,
+                                const int32_t* offsets,
+                                const void* w_gu_packed, const void* w_down,
+                                const void* u, const void* ws_gu_packed,
+                                const void* ws_down_packed, void* y_perm,
+                                void* y_shared, void* act, void* act_shared,
+                                void* ws, size_t ws_bytes, void* stream) {
+  if (act == nullptr) return fail(MOE_ERR_INVALID_ARG, "act is NULL");
+  return expert_ffn_impl(s, 0, x_perm, offsets, w_gu_packed, w_down, u,
+                         ws_gu_packed, ws_down_packed, y_perm, y_shared, ws,
+                         ws_bytes, stream, act, act_shared);
 }
 
 moe_status moe_combine(const moe_shape* s, const void* u, const void* y_perm,
@@ -1622,6 +1652,31 @@ moe_status make_map_grad(CUtensorMap* m, const void* ptr, long long rows,
   return MOE_OK;
 }
 
+// Outputs of the Dgrad (down) launch: dH (fp16) for the recompute pass, or,
+// with the forward's saved pre-activations, H and dA straight from its
+// epilogue (the SwiGLU backward fused, no recompute pass).
+void set_dgrad_down_outputs(BwdParams& p, bool saved, const void* act,
+                            const void* act_shared, int I, int SI, void* dH,
+                            void* dH_s, void* H, void* H_s, void* dA,
+                            void* dA_s) {
+  p.ld_r = I;
+  p.ld_s = SI;
+  if (!saved) {
+    p.out_r = dH;
+    p.out_s = dH_s;
+    p.act_r = p.act_s = nullptr;
+    return;
+  }
+  p.out_r = H;
+  p.out_s = H_s;
+  p.out2_r = dA;    p.ld2_r = 2LL * I;
+  p.out2_s = dA_s;  p.ld2_s = 2LL * SI;
+  p.act_r = static_cast<const __half*>(act);
+  p.ld_act_r = 2LL * I;
+  p.act_s = static_cast<const __half*>(act_shared);
+  p.ld_act_s = 2LL * SI;
+}
+
 template <int KIND>
 moe_status launch_bwd_pair(const BwdPairMaps& m, const BwdParams& p,
                            long long max_items, cudaStream_t cs) {
@@ -1654,6 +1709,7 @@ moe_status moe_backward(const moe_shape* s, const void* dh, const void* u,
                         const void* centroids, const int32_t* topk_idx,
                         const float* topk_gate, const int32_t* offsets,
                         const int32_t* inv, const void* y_perm,
+                        const void* act, const void* act_shared,
                         const void* w_gu_packed, const void* w_down,
                         const void* ws_gu_packed, const void* ws_down_packed,
                         float* du, float* dE, void* dw_gate, void* dw_up,
@@ -1692,6 +1748,14 @@ moe_status moe_backward(const moe_shape* s, const void* dh, const void* u,
     NEED_PTR(dws_gate);
     NEED_PTR(dws_up);
     NEED_PTR(dws_down);
+  }
+  // saved pre-activations (moe_expert_ffn_train): both or neither
+  const bool saved = act != nullptr;
+  if (saved && T > 0) {
+    NEED_PTR(act);
+    if (S > 0) NEED_PTR(act_shared);
+  } else if (act_shared != nullptr) {
+    return fail(MOE_ERR_INVALID_ARG, "act_shared given without act");
   }
   const BwdLayout w = bwd_layout(s);
   if (ws == nullptr) return fail(MOE_ERR_WORKSPACE, "workspace is NULL");
@@ -1776,28 +1840,33 @@ moe_status moe_backward(const moe_shape* s, const void* dh, const void* u,
       return st;
     p.m_routed = I;  p.m_shared = SI;
     p.k_routed = d;  p.k_shared = d;
-    p.out_r = dH;    p.ld_r = I;
-    p.out_s = dH_s;  p.ld_s = SI;
+    set_dgrad_down_outputs(p, saved, act, act_shared, I, SI, dH, dH_s, H, H_s,
+                           dA, dA_s);
     p.item_counter = ctr + 0;
     if ((st = launch_bwd_pair<kDgrad>(m, p, ti_r * (I / 256) +
                                                 ti_s * (SI / 256), cs)))
       return st;
-    // 4. gate/up recomputed with the SwiGLU backward: H, dA
-    if ((st = bwd_pair_maps({w_gu_packed, 2 * NI, d}, {X, R, d},
-                            {ws_gu_packed, 2LL * SI, d}, {u, T, d}, sh, true,
-                            m)))
-      return st;
-    p.m_routed = 2 * I;  p.m_shared = 2 * SI;
-    p.k_routed = d;      p.k_shared = d;
-    p.dh_r = dH;         p.dh_s = dH_s;
-    p.out_r = H;         p.ld_r = I;
-    p.out_s = H_s;       p.ld_s = SI;
-    p.out2_r = dA;       p.ld2_r = 2LL * I;
-    p.out2_s = dA_s;     p.ld2_s = 2LL * SI;
-    p.item_counter = ctr + 1;
-    if ((st = launch_bwd_pair<kRecomp>(m, p, ti_r * (2 * I / 256) +
-                                                 ti_s * (2 * SI / 256), cs)))
-      return st;
+    p.act_r = p.act_s = nullptr;
+    // 4. gate/up recomputed with the SwiGLU backward: H, dA (only without
+    // the forward's saved pre-activations)
+    if (!saved) {
+      if ((st = bwd_pair_maps({w_gu_packed, 2 * NI, d}, {X, R, d},
+                              {ws_gu_packed, 2LL * SI, d}, {u, T, d}, sh,
+                              true, m)))
+        return st;
+      p.m_routed = 2 * I;  p.m_shared = 2 * SI;
+      p.k_routed = d;      p.k_shared = d;
+      p.dh_r = dH;         p.dh_s = dH_s;
+      p.out_r = H;         p.ld_r = I;
+      p.out_s = H_s;       p.ld_s = SI;
+      p.out2_r = dA;       p.ld2_r = 2LL * I;
+      p.out2_s = dA_s;     p.ld2_s = 2LL * SI;
+      p.item_counter = ctr + 1;
+      if ((st = launch_bwd_pair<kRecomp>(m, p, ti_r * (2 * I / 256) +
+                                                   ti_s * (2 * SI / 256),
+                                         cs)))
+        return st;
+    }
     // 5. Dgrad (gate/up): dX = dA W_gu, dX_s = dA_s Ws_gu
     if ((st = bwd_pair_maps({w_gu_packed, 2 * NI, d}, {dA, R, 2LL * I},
                             {ws_gu_packed, 2LL * SI, d}, {dA_s, T, 2LL * SI},
@@ -1886,15 +1955,18 @@ moe_status moe_backward(const moe_shape* s, const void* dh, const void* u,
     }
     p.m_routed = I;  p.m_shared = SI;
     p.k_routed = d;  p.k_shared = d;
-    p.out_r = dH;    p.ld_r = I;
-    p.out_s = dH_s;  p.ld_s = SI;
+    set_dgrad_down_outputs(p, saved, act, act_shared, I, SI, dH, dH_s, H, H_s,
+                           dA, dA_s);
     p.item_counter = ctr + 0;
     if ((st = launch_bwd_gemm<kDgrad, 256, 4>(
              a_r, b_r, a_s, b_s, p,
              tok_items_r * (I / 128) + tok_items_s * (SI / 128), sms, cs)))
       return st;
+    p.act_r = p.act_s = nullptr;
 
-    // 4. gate/up recomputed with the SwiGLU backward: H, dA (and shared)
+    // 4. gate/up recomputed with the SwiGLU backward: H, dA (and shared),
+    // only without the forward's saved pre-activations
+    if (!saved) {
     if ((st = make_map(&a_r, w_gu_packed, 2LL * N * I, d, kGemmBM))) return st;
     if ((st = make_map(&b_r, X, R, d, kBoxRows))) return st;
     if (S > 0) {
@@ -1917,6 +1989,7 @@ moe_status moe_backward(const moe_shape* s, const void* dh, const void* u,
              tok_items_r * (2 * I / 128) + tok_items_s * (2 * SI / 128), sms,
              cs)))
       return st;
+    }
 
     // 5. Dgrad (gate/up): dX = dA W_gu, dX_s = dA_s Ws_gu
     if ((st = make_map(&a_r, w_gu_packed, 2LL * N * I, d, 64))) return st;

@@ -33,6 +33,11 @@ class Buffers:
     y_shared: Optional[torch.Tensor]
     h: torch.Tensor
     workspace: torch.Tensor
+    # gate/up pre-activations of the last forward on this batch size when it
+    # ran with save_for_backward (bf16 layers), for backward()
+    act: Optional[torch.Tensor] = None
+    act_shared: Optional[torch.Tensor] = None
+    saved: bool = False
 
 
 class MoELayer:
@@ -147,16 +152,32 @@ class MoELayer:
 
     def forward(self, u: torch.Tensor, update_bias: bool = False,
                 gamma: float = 1e-3, stream=None,
-                out: Optional[torch.Tensor] = None) -> torch.Tensor:
+                out: Optional[torch.Tensor] = None,
+                save_for_backward: bool = False) -> torch.Tensor:
         """h for u[T, d]; the result lives in this layer's buffer for T, or
-        in ``out`` ([T, d], the layer's output dtype) when given."""
+        in ``out`` ([T, d], the layer's output dtype) when given.  With
+        ``save_for_backward`` (bf16 layers) the expert FFNs also store their
+        gate/up pre-activations, and the next backward() on this batch uses
+        them instead of recomputing them."""
         T = u.shape[0]
         b = self.buffers(T)
         sh = self.shape(T)
+        if save_for_backward:
+            if self.code != torch.bfloat16:
+                raise ValueError("save_for_backward: bf16 layers only")
+            if b.act is None:
+                dev = self.E.device
+                b.act = torch.empty((max(T * self.K, 1), 2 * self.I),
+                                    dtype=torch.float16, device=dev)
+                b.act_shared = (torch.empty((T, 2 * self.S * self.I),
+                                            dtype=torch.float16, device=dev)
+                                if self.S else None)
+        b.saved = False
         _lib.route_grouped(sh, self.n_groups, self.topk_groups, u, self.E,
                            self.bias, b.topk_idx, b.topk_gate, b.counts,
                            b.workspace, stream)
-        side = self._shared_side_stream(u) if stream is None else None
+        side = (self._shared_side_stream(u)
+                if stream is None and not save_for_backward else None)
         if side is not None:
             # the shared experts need no routing: they run on a side stream
             # beside the permute and join before the routed experts' output
@@ -174,6 +195,12 @@ class MoELayer:
                                  self.w_down, u, None, None, b.y_perm, None,
                                  b.workspace)
             main.wait_stream(side)
+        elif save_for_backward:
+            _lib.expert_ffn_train(sh, b.x_perm, b.offsets, self.w_gu,
+                                  self.w_down, u, self.ws_gu, self.ws_down,
+                                  b.y_perm, b.y_shared, b.act, b.act_shared,
+                                  b.workspace, stream)
+            b.saved = True
         else:
             _lib.expert_ffn(sh, b.x_perm, b.offsets, self.w_gu, self.w_down,
                             u, self.ws_gu, self.ws_down, b.y_perm, b.y_shared,
@@ -194,7 +221,8 @@ class MoELayer:
                  grad_dtype: torch.dtype = torch.float32, stream=None):
         """Gradients of the layer for the upstream gradient dh [T, d] (bf16),
         after a forward on the same u (its routing, slots and expert outputs
-        are reused).  Returns a dict: du [T, d] and dE [N, d] fp32; dw_gate,
+        are reused, and its gate/up pre-activations when it ran with
+        save_for_backward).  Returns a dict: du [T, d] and dE [N, d] fp32; dw_gate,
         dw_up [N, I, d], dw_down [N, d, I] and, with shared experts, dws_gate,
         dws_up [S, I, d], dws_down [S, d, I] as grad_dtype.  The tensors are
         this layer's buffers for (T, grad_dtype), overwritten by the next
@@ -231,7 +259,9 @@ class MoELayer:
                       b.inv, b.y_perm, self.w_gu, self.w_down, self.ws_gu,
                       self.ws_down, g["du"], g["dE"], g["dw_gate"],
                       g["dw_up"], g["dw_down"], g.get("dws_gate"),
-                      g.get("dws_up"), g.get("dws_down"), g["_ws"], stream)
+                      g.get("dws_up"), g.get("dws_down"), g["_ws"], stream,
+                      act=b.act if b.saved else None,
+                      act_shared=b.act_shared if b.saved else None)
         return {k: v for k, v in g.items() if not k.startswith("_")}
 
     def forward_host(self, u_host, h_host, update_bias: bool = False,
@@ -303,21 +333,24 @@ class MoELayer:
         replays; the result is this layer's buffer for ``u.shape[0]``.  With
         ``update_bias`` every replay moves the bias once.  With ``dh`` (a
         fixed device buffer of upstream gradients) the backward pass is
-        captured after the forward, and a replay returns (h, gradients) --
-        one training step per graph launch."""
+        captured after the forward (which, for bf16 layers, saves its gate/up
+        pre-activations for it), and a replay returns (h, gradients) -- one
+        training step per graph launch."""
         T = u.shape[0]
         self.buffers(T)
         side = torch.cuda.Stream(device=u.device)
         side.wait_stream(torch.cuda.current_stream(u.device))
+        train = dh is not None and self.code == torch.bfloat16
         with torch.cuda.stream(side):      # first-use set-up outside capture
-            self.forward(u)
+            self.forward(u, save_for_backward=train)
             if dh is not None:
                 self.backward(u, dh, grad_dtype=grad_dtype)
         torch.cuda.current_stream(u.device).wait_stream(side)
         torch.cuda.synchronize(u.device)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            h = self.forward(u, update_bias=update_bias, gamma=gamma)
+            h = self.forward(u, update_bias=update_bias, gamma=gamma,
+                             save_for_backward=train)
             grads = (self.backward(u, dh, grad_dtype=grad_dtype)
                      if dh is not None else None)
 

@@ -196,9 +196,14 @@ def test_expert_ffn_part_validation(moe, dtype_name, part, code, detail):
     assert detail in moe.LIB.moe_last_error_detail()
 
 
+# moe_backward's 22 pointer arguments, in order (8, 9: the saved
+# pre-activations, which may both be NULL)
+ACT, ACT_S = 8, 9
+
+
 def _bwd_call(moe, sh, ptrs=None, grad=1, ws=None, nbytes=1 << 40):
     P = ctypes.c_void_p
-    p = [P(256 * (i + 1)) for i in range(20)] if ptrs is None else ptrs
+    p = [P(256 * (i + 1)) for i in range(22)] if ptrs is None else ptrs
     return moe.LIB.moe_backward(ctypes.byref(sh), *p, grad,
                                 P(1 << 20) if ws is None else ws, nbytes, None)
 
@@ -229,21 +234,55 @@ def test_backward_argument_checks(moe):
     assert n.value >= A_pad * 256 * 2 * 4 and n.value % 256 == 0
     P = ctypes.c_void_p
     assert _bwd_call(moe, sh, grad=2) == 1                   # e4m3 grads
-    for i in range(20):
-        ptrs = [P(256 * (k + 1)) for k in range(20)]
+    for i in range(22):
+        if i == ACT:
+            continue               # act NULL: the recomputing path
+        ptrs = [P(256 * (k + 1)) for k in range(22)]
         ptrs[i] = None
         assert _bwd_call(moe, sh, ptrs) == 1, i
         assert b"NULL" in moe.LIB.moe_last_error_detail()
-    ptrs = [P(256 * (k + 1)) for k in range(20)]
-    ptrs[0] = P(258)                                          # dh misaligned
+    for i in (0, ACT, ACT_S):                                 # misaligned
+        ptrs = [P(256 * (k + 1)) for k in range(22)]
+        ptrs[i] = P(258)
+        assert _bwd_call(moe, sh, ptrs) == 1, i
+        assert b"aligned" in moe.LIB.moe_last_error_detail()
+    # act and act_shared come together (or not at all)
+    ptrs = [P(256 * (k + 1)) for k in range(22)]
+    ptrs[ACT] = None
     assert _bwd_call(moe, sh, ptrs) == 1
-    assert b"aligned" in moe.LIB.moe_last_error_detail()
+    assert b"act_shared given without act" in moe.LIB.moe_last_error_detail()
+    ptrs[ACT_S] = None                       # neither: only the workspace
+    assert _bwd_call(moe, sh, ptrs, nbytes=n.value - 1) == 3
     assert _bwd_call(moe, sh, nbytes=n.value - 1) == 3       # too small
     assert _bwd_call(moe, sh, ws=P(1 << 20 | 8), nbytes=n.value) == 1
     # without shared experts their weights and gradients may be NULL, so
     # the first refusal is the workspace's
     sh0 = _shape(moe, dtype=moe.MOE_BF16, n_shared=0)
-    ptrs = [P(256 * (k + 1)) for k in range(20)]
-    for i in (10, 11, 17, 18, 19):
+    ptrs = [P(256 * (k + 1)) for k in range(22)]
+    for i in (ACT_S, 12, 13, 19, 20, 21):
         ptrs[i] = None
     assert _bwd_call(moe, sh0, ptrs, nbytes=0) == 3
+
+
+def test_expert_ffn_train_validation(moe):
+    """The training forward stores pre-activations for bf16 layers only and
+    needs act (and act_shared with shared experts); refused before a
+    launch."""
+    P = ctypes.c_void_p
+
+    def call(sh, act, act_s):
+        _, n = _ws(moe, sh)
+        p = [P(256 * (k + 1)) for k in range(9)]
+        return moe.LIB.moe_expert_ffn_train(ctypes.byref(sh), *p, act, act_s,
+                                            P(1 << 20), n, None)
+
+    bf = _shape(moe, dtype=moe.MOE_BF16)
+    assert call(bf, None, P(4096)) == 1
+    assert b"act is NULL" in moe.LIB.moe_last_error_detail()
+    assert call(bf, P(4096), None) == 1
+    assert b"act_shared is NULL" in moe.LIB.moe_last_error_detail()
+    assert call(bf, P(4100), P(4096)) == 1
+    assert b"aligned" in moe.LIB.moe_last_error_detail()
+    for dt in (moe.MOE_F32, moe.MOE_FP8):
+        assert call(_shape(moe, dtype=dt, d_ff=256), P(4096), P(8192)) == 2
+        assert b"bf16 layers only" in moe.LIB.moe_last_error_detail()

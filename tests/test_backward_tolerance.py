@@ -13,7 +13,9 @@ Rounding points modelled (per selected expert e, rows of its tokens):
   y  = fp16(bf16(SiLU(a) c) W_d^T)      forward output, read by the gate term
   dY = bf16(g dh)                        Dgrad/Wgrad operand
   dH = fp16(dY W_d)
-  a, c = fp32(x W_g^T), fp32(x W_u^T)    recomputed
+  a, c = fp32(x W_g^T), fp32(x W_u^T)    recomputed, or
+  a, c = fp16(fp32(x W_g^T)), ...        saved by the forward (then dH is
+                                         the fp32 accumulator, not fp16)
   H = bf16(SiLU(a) c), da = bf16(dH c SiLU'(a)), dc = bf16(dH SiLU(a))
   dX = fp16(da W_g + dc W_u)
   dz = fp32(dh . y) g (1 - g)
@@ -39,14 +41,18 @@ hf = lambda x: _r(x, torch.float16)
 f32 = lambda x: _r(x, torch.float32)
 
 
-def _model_ffn(x, wg, wu, wd, g, dh_rows):
+def _model_ffn(x, wg, wu, wd, g, dh_rows, saved=False):
     a, c = f32(x @ wg.T), f32(x @ wu.T)
+    # the forward's y comes from the fp32 a, c either way
     sg = 1.0 / (1.0 + np.exp(-a))
+    y = hf(bf(a * sg * c) @ wd.T)
+    if saved:
+        a, c = hf(a), hf(c)
+        sg = 1.0 / (1.0 + np.exp(-a))
     si = a * sg
     H = bf(si * c)
-    y = hf(H @ wd.T)
     dY = bf(g[:, None] * dh_rows)
-    dH = hf(dY @ wd)
+    dH = f32(dY @ wd) if saved else hf(dY @ wd)
     da = bf(dH * c * sg * (1.0 + a * (1.0 - sg)))
     dc = bf(dH * si)
     dX = hf(da @ wg + dc @ wu)
@@ -59,9 +65,10 @@ BASE = dict(T=64, d=256, n_routed=16, top_k=4, n_shared=1, d_ff=128,
             dtype="bf16")
 
 
+@pytest.mark.parametrize("saved", [False, True], ids=["recompute", "saved"])
 @pytest.mark.parametrize("over", [dict(BASE), dict(BASE, T=300, d=384),
                                   dict(BASE, T=200, n_shared=2, d_ff=256)])
-def test_gradient_bar_has_margin_over_rounding_model(over):
+def test_gradient_bar_has_margin_over_rounding_model(over, saved):
     cfg = get_config("tiny").with_(**over)
     t = generate(cfg, "cpu")
     u, E, b = as_f64(t["u"]), as_f64(t["E"]), as_f64(t["b"])
@@ -81,14 +88,14 @@ def test_gradient_bar_has_margin_over_rounding_model(over):
         rows, ks = np.nonzero(idx == e)
         if rows.size == 0:
             continue
-        m = _model_ffn(u[rows], *W(e), f32(gate[rows, ks]), dh[rows])
+        m = _model_ffn(u[rows], *W(e), f32(gate[rows, ks]), dh[rows], saved)
         du[rows] += m["dX"] + m["dz"][:, None] * E[e]
         dE[e] = m["dz"] @ u[rows]
         for j, k in enumerate(("dWg", "dWu", "dWd")):
             got[k].append(m[k])
             want[k].append(ref["dW"][e][j])
     for s, w in enumerate(Ws):
-        m = _model_ffn(u, *w, np.ones(cfg.T), dh)
+        m = _model_ffn(u, *w, np.ones(cfg.T), dh, saved)
         du += m["dX"]
         for j, k in enumerate(("dWg", "dWu", "dWd")):
             got[k].append(m[k])

@@ -48,11 +48,11 @@ def _layer(moe, g, cfg):
                         top_k=cfg.top_k, h_dtype=torch.float32)
 
 
-def _run(moe, cfg, grad_dtype=torch.float32):
+def _run(moe, cfg, grad_dtype=torch.float32, saved=False):
     g = make_inputs(cfg)
     dh = upstream_grad(cfg, "cpu").to("cuda")
     layer = _layer(moe, g, cfg)
-    layer(g["u"])
+    layer(g["u"], save_for_backward=saved)
     gr = layer.backward(g["u"], dh, grad_dtype=grad_dtype)
     torch.cuda.synchronize()
     moe.get_device_error()
@@ -78,11 +78,15 @@ CASES = {
 }
 
 
+@pytest.mark.parametrize("saved", [False, True], ids=["recompute", "saved"])
 @pytest.mark.parametrize("case", sorted(CASES))
-def test_backward_parity(moe, case):
+def test_backward_parity(moe, case, saved):
+    """Both ways to the SwiGLU backward: a and c recomputed by a gate/up
+    GEMM, or saved (bf16) by the forward and used in the dH GEMM's
+    epilogue."""
     name, over = CASES[case]
     cfg = get_config(name).with_(**over)
-    g, dh, layer, gr = _run(moe, cfg)
+    g, dh, layer, gr = _run(moe, cfg, saved=saved)
     b = layer.buffers(cfg.T)
     idx = b.topk_idx.cpu().numpy()
     u64, E64, b64 = as_f64(g["u"]), as_f64(g["E"]), as_f64(g["b"])
@@ -107,7 +111,58 @@ def test_backward_parity(moe, case):
             out[k] = grad_close(gr[k].float().cpu().numpy(), want, k)
         else:
             assert k not in gr
-    print(case, out)
+    print(case, saved, out)
+
+
+@pytest.mark.parametrize("over", [dict(BASE, T=64),
+                                  dict(BASE, T=300, d=384, n_shared=2),
+                                  dict(BASE, T=300, d=512, d_ff=256)],
+                         ids=["small_groups", "single_sm", "cta_pair"])
+def test_forward_saves_preactivations(moe, over):
+    """save_for_backward leaves the forward's outputs bit for bit unchanged
+    and stores a = x W_gate^T, c = x W_up^T of every slot (and of every
+    token for the shared experts) as fp16, in the packed column order
+    (blocks of 64 gate then 64 up values), within fp16 rounding (2^-11
+    relative) of the fp64 products of the bf16 operands, plus the fp32
+    accumulation's share."""
+    cfg = get_config("tiny").with_(**over)
+    g = make_inputs(cfg)
+    plain, saving = _layer(moe, g, cfg), _layer(moe, g, cfg)
+    h0 = plain(g["u"]).clone()
+    h1 = saving(g["u"], save_for_backward=True)
+    torch.cuda.synchronize()
+    moe.get_device_error()
+    assert torch.equal(h0, h1)
+    b0, b1 = plain.buffers(cfg.T), saving.buffers(cfg.T)
+    assert torch.equal(b0.y_perm, b1.y_perm)
+    assert b1.saved
+    I, S = cfg.d_ff, cfg.n_shared
+
+    def unpack(act, n_units):
+        a = act.float().cpu().numpy().reshape(act.shape[0], n_units // 64, 2,
+                                              64)
+        return (a[:, :, 0, :].reshape(act.shape[0], n_units),
+                a[:, :, 1, :].reshape(act.shape[0], n_units))
+
+    u64 = as_f64(g["u"])
+    offs = b1.offsets.cpu().numpy()
+    perm = b1.perm.cpu().numpy()
+    ga, gc = unpack(b1.act[:offs[-1]], I)
+    for e in range(cfg.n_routed):
+        sl = slice(offs[e], offs[e + 1])
+        x = u64[perm[sl]]
+        for got, w in ((ga[sl], g["w_gate"][e]), (gc[sl], g["w_up"][e])):
+            ref = x @ as_f64(w).T
+            assert np.all(np.abs(got - ref) <= 2.0 ** -11 * np.abs(ref) + 1e-4)
+    if S:
+        sa, sc = unpack(b1.act_shared, S * I)
+        for s_ in range(S):
+            cols = slice(s_ * I, (s_ + 1) * I)
+            for got, w in ((sa[:, cols], g["ws_gate"][s_]),
+                           (sc[:, cols], g["ws_up"][s_])):
+                ref = u64 @ as_f64(w).T
+                assert np.all(np.abs(got - ref) <=
+                              2.0 ** -11 * np.abs(ref) + 1e-4)
 
 
 @pytest.mark.parametrize("over", [dict(BASE, T=200),
@@ -177,7 +232,8 @@ def test_backward_unused_experts_zero(moe):
     assert torch.any(gr["dw_down"][4:] != 0)
 
 
-def test_backward_full_v3_prefill_sampled(moe):
+@pytest.mark.parametrize("saved", [False, True], ids=["recompute", "saved"])
+def test_backward_full_v3_prefill_sampled(moe, saved):
     """V3 prefill shapes: du of sampled tokens, every weight and centroid
     gradient of two sampled experts, and sampled intermediate rows of the
     shared expert's gradients, each against the oracle."""
@@ -185,7 +241,7 @@ def test_backward_full_v3_prefill_sampled(moe):
     g = generate(cfg, "cuda")
     dh = upstream_grad(cfg, "cuda")
     layer = _layer(moe, g, cfg)
-    layer(g["u"])
+    layer(g["u"], save_for_backward=saved)
     gr = layer.backward(g["u"], dh)
     torch.cuda.synchronize()
     moe.get_device_error()
@@ -232,9 +288,9 @@ def test_backward_full_v3_prefill_sampled(moe):
 
 
 def test_training_step_graph(moe):
-    """Forward + bias update + backward captured as one CUDA graph replay
-    the eager step bit for bit, on new tokens and gradients written into the
-    captured buffers."""
+    """Forward (saving its pre-activations) + bias update + backward captured
+    as one CUDA graph replay the eager step bit for bit, on new tokens and
+    gradients written into the captured buffers."""
     cfg = get_config("tiny").with_(**dict(BASE, T=300, d=512, d_ff=256))
     g = make_inputs(cfg)
     mk = lambda: _layer(moe, g, cfg)
@@ -249,7 +305,7 @@ def test_training_step_graph(moe):
                     .to(u.dtype))
             dh.copy_(torch.randn(dh.shape, generator=gen, device="cuda")
                      .to(dh.dtype))
-        want_h = eager(u, update_bias=True).clone()
+        want_h = eager(u, update_bias=True, save_for_backward=True).clone()
         want = {k: v.clone() for k, v in
                 eager.backward(u, dh, grad_dtype=torch.bfloat16).items()}
         h, grads = run()

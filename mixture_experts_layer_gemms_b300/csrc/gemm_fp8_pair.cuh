@@ -23,9 +23,13 @@
 // three stages (each K-atom is a 128-byte-swizzled block of its rows).
 // Gate/up items load each CTA's weight half as one 5-D box (per K-atom the
 // CTA's 64 gate rows and the 64 up rows of the same intermediates), so SwiGLU pairs
-// TMEM lanes l and l + 64 as in the bf16 kernel, and H leaves as fp32 (the
-// host requantizes it to e4m3 1 x 128 blocks for the down pass, from the
-// same fp32 values as the other e4m3 kernels; a bf16 H would round twice).
+// TMEM lanes l and l + 64 as in the bf16 kernel.  An item's 128 H columns
+// (64 per CTA) are exactly one 1 x 128 quantization block of the down pass,
+// so the epilogue requantizes H to e4m3 itself: per token, the block's
+// largest |H| from both CTAs (exchanged through distributed shared memory),
+// its exponent, the codes and the scales, from the same fp32 values the
+// other e4m3 kernels quantize (a bf16 H would round twice).  Without the
+// q8 outputs H leaves as fp32 instead.
 //
 // TMEM (512 columns per CTA): accumulators at columns 0 and 256 (192
 // columns each), four scale groups at columns 192, 224, 448 and 480 (A
@@ -50,9 +54,13 @@
 //   isempty[j] (both)   : the 4 scale warps are done with item slot j
 //   sffull[g]  (L only) : one arrival per scale warp of both CTAs
 //   sfempty[g] (both)   : MMA commit multicast (group g's MMAs are done)
+//   amx[c]     (both)   : the other CTA's 4 epilogue warps' token maxima of
+//                         chunk parity c landed (st.async transaction bytes;
+//                         fused requantization)
 #pragma once
 #include "common.cuh"
 #include "gemm.cuh"
+#include "quant.cuh"
 
 namespace moe {
 
@@ -96,6 +104,18 @@ struct F8PairParams {
   void* out_shared;
   long long ld_shared;
   int* item_counter;         // zeroed before the launch
+  // gate/up pass: when q8_routed is not null, H is requantized in the
+  // epilogue instead of stored as fp32: e4m3 codes [rows][ld_*], fp32
+  // scales [ld_* / 128][rows] (column = row) and the UE8M0 table
+  // [rows][qpitch_*], the layout the activation quantizer writes
+  uint8_t* q8_routed;
+  float* qs_routed;
+  uint8_t* qe_routed;
+  int qpitch_routed;
+  uint8_t* q8_shared;
+  float* qs_shared;
+  uint8_t* qe_shared;
+  int qpitch_shared;
 };
 
 struct F8PairSmem {
@@ -118,12 +138,135 @@ struct F8PairSmem {
   static constexpr int epok_off = misc_off + 16;
   static constexpr int sched_off = epok_off + 16;
   static constexpr int tab_off = sched_off + 4 * kSchedDepth;
-  static constexpr int total = tab_off + 2 * (kMaxGroups + 1) * 4;
+  // fused requantization of H: per chunk parity, 4 warps x 16 token maxima,
+  // this CTA's own and the peer CTA's; and two barriers the peer arrives on
+  static constexpr int amx_off =
+      (tab_off + 2 * (kMaxGroups + 1) * 4 + 15) / 16 * 16;   // float4 rows
+  static constexpr int amx_bytes = 2 * 2 * 4 * 16 * 4;
+  static constexpr int amxbar_off = amx_off + amx_bytes;
+  static constexpr int total = amxbar_off + 16;
   static constexpr int alloc = total + 1024;
   static constexpr int tmem_cols = 512;
   static_assert(alloc <= 227 * 1024, "shared memory");
   static_assert(kF8PBN <= 192 && f8p_sf_col(3) + 24 <= 512, "TMEM map");
 };
+
+// The pair's two CTAs hold the 128 H columns of one 1 x 128 quantization
+// block (64 each).  Hand-off of the per-token block maxima between them:
+// each CTA's four epilogue warps write their 16 token maxima into their own
+// `amx` slot of the chunk's parity and, by st.async, into the peer's; the
+// st.async completes its bytes on the peer's barrier of that parity, where
+// the peer's warp 0 expects 4 x 64 bytes per chunk.  No release fence is
+// taken (one would wait for the epilogue's earlier global stores).  The
+// slot of parity c is written again only after this CTA has received the
+// peer's maxima of chunk c + 1, which the peer sends after its reads of
+// chunk c.
+struct F8Amx {
+  float* own;            // [2][4][16]
+  float* rem;            // [2][4][16], written by the peer
+  uint32_t rem_peer;     // cluster address of the peer's `rem`
+  uint32_t bar;          // this CTA's barriers [2]
+  uint32_t bar_peer;     // cluster address of the peer's barriers
+  int par;               // parity of the next chunk
+  uint32_t ph;           // bit c: phase of barrier c
+};
+
+// 16 bytes into the peer CTA's shared memory, counted as transaction bytes
+// on the peer's barrier `cluster_bar`.
+__device__ __forceinline__ void st_async_v4f(uint32_t cluster_addr, float a,
+                                             float b, float c, float d,
+                                             uint32_t cluster_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], "
+      "{%1, %2, %3, %4}, [%5];" ::"r"(cluster_addr),
+      "f"(a), "f"(b), "f"(c), "f"(d), "r"(cluster_bar)
+      : "memory");
+}
+
+// Gate/up epilogue of the e4m3 CTA-pair GEMM with H requantized in place:
+// SwiGLU as in epilogue_store (warps q and q+2 swap token halves so each
+// thread holds H of one column, 16 tokens), then per token the largest |H|
+// of the 128-column block (warp maximum, the partner warp's, the peer
+// CTA's), the block exponent e and the e4m3 codes of H 2^-e; the rank-0
+// CTA also writes the block's fp32 scale and UE8M0 byte.  H is the same
+// fp32 value the separate quantizer would read, so the codes and scales are
+// the same bit for bit.
+__device__ __forceinline__ bool f8p_epilogue_swiglu_q8(
+    uint32_t taddr, int n_valid, int b_row, int col0, long long ld,
+    long long rows, uint8_t* q8, float* qs, uint8_t* qe, int qpitch,
+    bool write_scales, float* xchg, F8Amx& am, int q, int lane,
+    volatile int* abort_flag) {
+  const bool gate_warp = q < 2;
+  const int pair_q = q & 1;
+  const int jbase = gate_warp ? 0 : 16;
+  const int col = col0 + pair_q * 32 + lane;      // H column of the thread
+  const int blk = col0 >> 7;                       // quantization block
+  bool ok = true;
+  for (int n0 = 0; n0 < n_valid; n0 += 32) {
+    uint32_t r[32];
+    tmem_ld32(taddr + n0, r);
+    tmem_ld_wait();
+    const int nleft = n_valid - n0;
+    float* mine = xchg + ((q * 32) + lane) * 17;
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      mine[j] = __uint_as_float(r[gate_warp ? 16 + j : j]);
+    named_bar_sync(1, 128);
+    const float* theirs =
+        xchg + (((gate_warp ? q + 2 : q - 2) * 32) + lane) * 17;
+    float h[16], mx[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float g = gate_warp ? __uint_as_float(r[j]) : theirs[j];
+      const float u = gate_warp ? theirs[j] : __uint_as_float(r[16 + j]);
+      h[j] = jbase + j < nleft ? silu_f32(g) * u : 0.f;
+      mx[j] = warp_amax(h[j]);
+    }
+    const int sl = am.par;
+    if (lane == 0) {
+      float* o = am.own + (sl * 4 + q) * 16;
+      const uint32_t rp = am.rem_peer + ((sl * 4 + q) * 16) * 4;
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        reinterpret_cast<float4*>(o)[v] =
+            make_float4(mx[4 * v], mx[4 * v + 1], mx[4 * v + 2], mx[4 * v + 3]);
+        st_async_v4f(rp + 16 * v, mx[4 * v], mx[4 * v + 1], mx[4 * v + 2],
+                     mx[4 * v + 3], am.bar_peer + 8 * sl);
+      }
+      // this CTA's barrier: the peer's four warps' 64 bytes each
+      if (q == 0) mbar_arrive_expect_tx(am.bar + 8 * sl, 4 * 64);
+    }
+    named_bar_sync(1, 128);          // the partner warp's maxima are in own
+    if (!mbar_wait_cl(am.bar + 8 * sl, (am.ph >> sl) & 1u, abort_flag,
+                      KID_GEMM_FP8, 120))
+      ok = false;
+    am.ph ^= 1u << sl;
+    am.par ^= 1;
+    const int qp = q ^ 1;
+    const float* o1 = am.own + (sl * 4 + q) * 16;
+    const float* o2 = am.own + (sl * 4 + qp) * 16;
+    const float* r1 = am.rem + (sl * 4 + q) * 16;
+    const float* r2 = am.rem + (sl * 4 + qp) * 16;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      if (jbase + j >= nleft) continue;
+      const float a = fmaxf(fmaxf(o1[j], o2[j]), fmaxf(r1[j], r2[j]));
+      const int e = e4m3_scale_exp(a);
+      const bool bad_e = e < -126 || e > 126;
+      const long long row = b_row + n0 + jbase + j;
+      q8[row * ld + col] = bad_e ? 0 : static_cast<uint8_t>(
+                                           e4m3_code(h[j], pow2f(-e)));
+      if (write_scales && pair_q == 0 && lane == 0) {
+        const float sc = bad_e ? 0.f : pow2f(e);
+        if (bad_e) report_error(ERR_CHECK, KID_QUANT, 1);
+        qs[static_cast<long long>(blk) * rows + row] = sc;
+        qe[row * qpitch + blk] = ue8_of(sc);
+      }
+    }
+    named_bar_sync(1, 128);
+  }
+  return ok;
+}
 
 // Rows of the TMA box of a CTA's token half-tile: the smallest of 32, 64,
 // 96 covering it (96 = 192 / 2).
@@ -244,6 +387,8 @@ grouped_gemm_fp8_pair_kernel(const __grid_constant__ CUtensorMap tmA_r,
       mbar_init(bar_sfull + 8 * i, 1);
       mbar_init(bar_sempty + 8 * i, 18);      // 9 consumers x 2 CTAs
     }
+    for (int j = 0; j < 2; ++j)   // own expect-tx; the peer's st.async bytes
+      mbar_init(sbase + L::amxbar_off + 8 * j, 1);
     *abort_flag = 0;
     *bad_flag = 0;
     fence_mbar_init();
@@ -526,6 +671,15 @@ grouped_gemm_fp8_pair_kernel(const __grid_constant__ CUtensorMap tmA_r,
     const int q = warp & 3;
     int acc = 0;
     uint32_t acc_phase = 0;
+    F8Amx amx;
+    amx.own = reinterpret_cast<float*>(smem + L::amx_off);
+    amx.rem = amx.own + 2 * 4 * 16;
+    const uint32_t other = leader ? peer : lead;   // the pair's other CTA
+    amx.rem_peer = mapa_shared(smem_u32(amx.rem), other);
+    amx.bar = sbase + L::amxbar_off;
+    amx.bar_peer = mapa_shared(amx.bar, other);
+    amx.par = 0;
+    amx.ph = 0;
     while (true) {
       int item = next_item(108);
       const bool got = item >= 0;
@@ -545,11 +699,23 @@ grouped_gemm_fp8_pair_kernel(const __grid_constant__ CUtensorMap tmA_r,
       void* out = t.shared ? p.out_shared : p.out_routed;
       const long long ld = t.shared ? p.ld_shared : p.ld_routed;
       const int tile128 = t.wt * 2 + static_cast<int>(rank);
-      epilogue_store(tmem + (static_cast<uint32_t>(q * 32) << 16) +
-                         f8p_acc_col(acc),
-                     t.n_valid, t.b_row, out, ld,
-                     p.gate_up ? tile128 * 64 : tile128 * 128, p.gate_up != 0,
-                     stg, q, ep, lane, true, true);
+      const uint32_t ta = tmem + (static_cast<uint32_t>(q * 32) << 16) +
+                          f8p_acc_col(acc);
+      bool eok = true;
+      if (p.gate_up && p.q8_routed != nullptr) {
+        eok = f8p_epilogue_swiglu_q8(
+            ta, t.n_valid, t.b_row, tile128 * 64, ld,
+            t.shared ? p.shared_rows : p.max_routed_rows,
+            t.shared ? p.q8_shared : p.q8_routed,
+            t.shared ? p.qs_shared : p.qs_routed,
+            t.shared ? p.qe_shared : p.qe_routed,
+            t.shared ? p.qpitch_shared : p.qpitch_routed, leader, stg, amx,
+            q, lane, abort_flag);
+      } else {
+        epilogue_store(ta, t.n_valid, t.b_row, out, ld,
+                       p.gate_up ? tile128 * 64 : tile128 * 128,
+                       p.gate_up != 0, stg, q, ep, lane, true, true);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster_relaxed(tempty_L + 8 * acc);
@@ -557,6 +723,7 @@ grouped_gemm_fp8_pair_kernel(const __grid_constant__ CUtensorMap tmA_r,
         acc = 0;
         acc_phase ^= 1;
       }
+      if (!__all_sync(0xffffffffu, eok)) *abort_flag = 1;
     }
   } else {
     // ------------- scale warps (warps 6..9 of both CTAs) -------------------

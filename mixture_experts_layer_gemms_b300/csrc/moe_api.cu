@@ -637,13 +637,22 @@ moe_status expert_ffn_fp8(const moe_shape* s, const void* x_perm,
   if (!small && d % 256 == 0 && ue8_pitch(d) <= kF8PMaxPitch &&
       ue8_pitch(I) <= kF8PMaxPitch && ue8_pitch(SI) <= kF8PMaxPitch) {
     // Prefill-sized groups: e4m3 CTA pairs with the block scales applied in
-    // the tensor core.  H leaves the gate/up pass as fp32 and is requantized
-    // to e4m3 1 x 128 blocks (the same rule as every activation) for the
+    // the tensor core.  The gate/up pass requantizes H to e4m3 1 x 128
+    // blocks (the same rule as every activation) in its epilogue, for the
     // down pass.
     float* hb = reinterpret_cast<float*>(wsb + w.h_routed);
     float* hbs = reinterpret_cast<float*>(wsb + w.h_shared);
     uint8_t* q8 = reinterpret_cast<uint8_t*>(wsb + w.h8_routed);
     uint8_t* q8s = reinterpret_cast<uint8_t*>(wsb + w.h8_shared);
+    // padding bytes of the H tables' rows (no block writes them)
+    if (ue8_pitch(I) * kQBlock > I && A > 0)
+      MOE_CHECK_CUDA(cudaMemsetAsync(fp8_ue8(q8, A, I, false), 127,
+                                     static_cast<size_t>(A) * ue8_pitch(I),
+                                     cs));
+    if (has_shared && ue8_pitch(SI) * kQBlock > SI)
+      MOE_CHECK_CUDA(cudaMemsetAsync(fp8_ue8(q8s, T, SI, false), 127,
+                                     static_cast<size_t>(T) * ue8_pitch(SI),
+                                     cs));
     F8PairMaps m;
     F8PairParams q{};
     if ((st = f8_pair_maps(w_gu8, 2LL * N * I, x_perm, A, d,
@@ -670,22 +679,17 @@ moe_status expert_ffn_fp8(const moe_shape* s, const void* x_perm,
     q.out_shared = hbs;
     q.ld_shared = SI;
     q.item_counter = ctr;
-    if ((st = launch_gemm_fp8_pair(m, q, cs)) != MOE_OK) return st;
-    if (A > 0) {
-      const long long warps = A * (I / kQBlock);
-      quantize_rows_kernel<<<static_cast<unsigned>(cdiv(warps, 8)), 256, 0,
-                             cs>>>(hb, static_cast<int>(A), I, q8,
-                                   scales(q8, A, I), A,
-                                   fp8_ue8(q8, A, I, false));
-      MOE_CHECK_LAUNCH();
-    }
+    q.q8_routed = q8;
+    q.qs_routed = scales(q8, A, I);
+    q.qe_routed = fp8_ue8(q8, A, I, false);
+    q.qpitch_routed = ue8_pitch(I);
     if (has_shared) {
-      const long long warps = T * (SI / kQBlock);
-      quantize_rows_kernel<<<static_cast<unsigned>(cdiv(warps, 8)), 256, 0,
-                             cs>>>(hbs, s->T, SI, q8s, scales(q8s, T, SI), T,
-                                   fp8_ue8(q8s, T, SI, false));
-      MOE_CHECK_LAUNCH();
+      q.q8_shared = q8s;
+      q.qs_shared = scales(q8s, T, SI);
+      q.qe_shared = fp8_ue8(q8s, T, SI, false);
+      q.qpitch_shared = ue8_pitch(SI);
     }
+    if ((st = launch_gemm_fp8_pair(m, q, cs)) != MOE_OK) return st;
     if ((st = f8_pair_maps(w_down8, static_cast<long long>(N) * d, q8, A, I,
                            has_shared ? ws_down8 : nullptr, d, q8s, T, SI, 128,
                            m)) != MOE_OK)
@@ -706,6 +710,7 @@ moe_status expert_ffn_fp8(const moe_shape* s, const void* x_perm,
     q.out_shared = y_shared;
     q.ld_shared = d;
     q.item_counter = ctr + 1;
+    q.q8_routed = q.q8_shared = nullptr;
     return launch_gemm_fp8_pair(m, q, cs);
   }
   const int bn = small ? 32 : 128;

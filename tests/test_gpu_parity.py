@@ -84,6 +84,20 @@ def test_route_full_v3_prefill(moe):
     assert counts.sum() == cfg.T * cfg.top_k
 
 
+def test_route_full_unsplit_v3_dims(moe):
+    """V3 dimensions with T = 16384 (the skewed-bias loop's batch): 128
+    token tiles x 2 would exceed one wave of the GPU's SMs, so the router
+    runs unsplit (one CTA per tile over all of d = 7168, sigmoid in its
+    first epilogue branch).  All tokens checked, as at T = 8192."""
+    cfg = get_config("v3_prefill").with_(T=16384)
+    t = generate(cfg, "cuda", experts=False)
+    idx, gate, counts = _route_gpu(moe, cfg, t["u"], t["E"], t["b"])
+    b64 = as_f64(t["b"])
+    r = om.route(as_f64(t["u"]), as_f64(t["E"]), b64, cfg.top_k)
+    check_routing(r, b64, idx, counts, cfg.top_k)
+    assert counts.sum() == cfg.T * cfg.top_k
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_route_ties_lowest_index(moe, dtype):
     """E = 0 makes every affinity exactly 1/2: selection follows the bias,

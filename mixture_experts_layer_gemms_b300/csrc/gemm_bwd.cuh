@@ -11,11 +11,14 @@
 //           MN-major (W stored [K rows, M contiguous]), tokens on N.
 //           dH = dY W_down (W_down [d, I]: K = d, M = I) and
 //           dX = dA W_gu   (packed W_gu [2I, d]: K = 2I, M = d).
-//           Output fp16 [token][m].
+//           Output fp16 [token][m]; or, for dH with the forward's saved
+//           pre-activations a, c, the SwiGLU backward in the epilogue
+//           (H and dA written instead of dH, as kRecomp writes them).
 //  kRecomp  the forward's gate/up GEMM again (both operands K-major), with
 //           the SwiGLU backward in the epilogue: from a, c (fp32, TMEM) and
 //           dH it writes H = SiLU(a) c and dA = [dH c SiLU'(a) | dH SiLU(a)]
-//           in the packed gate/up column order.
+//           in the packed gate/up column order.  Only when the forward saved
+//           no pre-activations.
 //  kWgrad   D[m, n] = sum_k A[k, m] B[k, n] over the tokens of one group:
 //           both operands MN-major (token rows, M or N contiguous); output
 //           row-major per expert.  dW_gu = dA^T X  (gate/up rows unpacked to

@@ -1,8 +1,9 @@
 // The layer backward's grouped GEMMs on CTA pairs (tcgen05.mma.cta_group::2):
 // the same three kinds of work as bwd_gemm_kernel (gemm_bwd.cuh) -- Dgrad
-// with an MN-major weight operand, the gate/up recompute with the SwiGLU
-// backward epilogue, Wgrad with both operands MN-major -- on 256-row M tiles
-// split over two SMs, as the forward's grouped_gemm_pair_kernel does
+// with an MN-major weight operand (for dH optionally with the SwiGLU
+// backward from saved pre-activations), the gate/up recompute with the
+// SwiGLU backward epilogue, Wgrad with both operands MN-major -- on 256-row
+// M tiles split over two SMs, as the forward's grouped_gemm_pair_kernel does
 // ("AI新顶流-DeepSeek 技术大揭秘", section "FP8混合精度训练框架": the Dgrad and
 // Wgrad GEMMs of each linear operator).
 //
@@ -10,9 +11,10 @@
 // half of the B operand (tokens kinds: token rows n0 + r N/2 .. + N/2; Wgrad:
 // columns n0 + 128 r .. +128) in its own shared memory; the even CTA issues
 // M = 256 MMAs reading both halves, each CTA's TMEM receives its 128 rows x
-// all N columns.  A stage is 128 of K: every operand half is one 3-D TMA box
-// of two 64-element swizzle atoms (K-major: {64 K, rows, 2 K-atoms};
-// MN-major: {64 MN, 128 K rows, 2 MN-atoms}), 32 KB.  Per SM and stage this
+// all N columns.  A stage of the token kinds is 128 of K: every operand
+// half is one 3-D TMA box of two 64-element swizzle atoms (K-major: {64 K,
+// rows, 2 K-atoms}; MN-major: {64 MN, 128 K rows, 2 MN-atoms}), 32 KB;
+// Wgrad stages are 64 of K (16 KB per operand half), five of them.  Per SM and stage this
 // moves 32 KB of A and at most 32 KB of B, where a 128 x 256 tile on one SM
 // moves 16 + 32 KB per 64 of K: the shared-memory traffic of TMA fills plus
 // MMA operand reads fits the SM's bandwidth at full tensor rate.

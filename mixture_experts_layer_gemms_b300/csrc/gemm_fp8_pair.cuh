@@ -199,7 +199,6 @@ __device__ __forceinline__ bool f8p_epilogue_swiglu_q8(
   const bool gate_warp = q < 2;
   const int pair_q = q & 1;
   const int jbase = gate_warp ? 0 : 16;
-  const int col = col0 + pair_q * 32 + lane;      // H column of the thread
   const int blk = col0 >> 7;                       // quantization block
   bool ok = true;
   for (int n0 = 0; n0 < n_valid; n0 += 32) {
@@ -247,20 +246,33 @@ __device__ __forceinline__ bool f8p_epilogue_swiglu_q8(
     const float* o2 = am.own + (sl * 4 + qp) * 16;
     const float* r1 = am.rem + (sl * 4 + q) * 16;
     const float* r2 = am.rem + (sl * 4 + qp) * 16;
+    // the warp's 16 tokens x 32 columns of codes, transposed through its own
+    // (now free) 2 KB of the exchange buffer: lane pairs then store one
+    // token's 32 codes as two 16-byte vectors
+    uint8_t* tile = reinterpret_cast<uint8_t*>(xchg + q * 32 * 17);
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-      if (jbase + j >= nleft) continue;
       const float a = fmaxf(fmaxf(o1[j], o2[j]), fmaxf(r1[j], r2[j]));
       const int e = e4m3_scale_exp(a);
       const bool bad_e = e < -126 || e > 126;
-      const long long row = b_row + n0 + jbase + j;
-      q8[row * ld + col] = bad_e ? 0 : static_cast<uint8_t>(
-                                           e4m3_code(h[j], pow2f(-e)));
-      if (write_scales && pair_q == 0 && lane == 0) {
+      tile[j * 32 + lane] = bad_e ? 0 : static_cast<uint8_t>(
+                                            e4m3_code(h[j], pow2f(-e)));
+      if (jbase + j < nleft && write_scales && pair_q == 0 && lane == 0) {
+        const long long row = b_row + n0 + jbase + j;
         const float sc = bad_e ? 0.f : pow2f(e);
         if (bad_e) report_error(ERR_CHECK, KID_QUANT, 1);
         qs[static_cast<long long>(blk) * rows + row] = sc;
         qe[row * qpitch + blk] = ue8_of(sc);
+      }
+    }
+    __syncwarp();
+    {
+      const int j = lane >> 1, part = lane & 1;
+      if (jbase + j < nleft) {
+        const long long row = b_row + n0 + jbase + j;
+        *reinterpret_cast<uint4*>(q8 + row * ld + col0 + pair_q * 32 +
+                                  part * 16) =
+            *reinterpret_cast<const uint4*>(tile + j * 32 + part * 16);
       }
     }
     named_bar_sync(1, 128);

@@ -218,7 +218,10 @@ __device__ __forceinline__ bool f8p_epilogue_swiglu_q8(
     for (int j = 0; j < 16; ++j) {
       const float g = gate_warp ? __uint_as_float(r[j]) : theirs[j];
       const float u = gate_warp ? theirs[j] : __uint_as_float(r[16 + j]);
-      h[j] = jbase + j < nleft ? silu_f32(g) * u : 0.f;
+      // SiLU with the fast exponential and division intrinsics: H is
+      // about to be rounded to 3 mantissa bits, so their few-ulp error
+      // decides a code only at a rounding boundary (one e4m3 step)
+      h[j] = jbase + j < nleft ? __fdividef(g, 1.0f + __expf(-g)) * u : 0.f;
       mx[j] = warp_amax(h[j]);
     }
     const int sl = am.par;

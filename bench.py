@@ -51,7 +51,7 @@ METRIC = "MoE-layer tokens/s at V3 shape"
 # over to the full size.  None where no capture of the current kernel
 # exists.
 TRAFFIC_RATIO = {"v3_prefill": 3.276123 / 3.246,
-                 "v3_prefill_fp8": 1.676476 / 1.653926,
+                 "v3_prefill_fp8": 1.677290 / 1.653926,
                  "v3_decode": 2.918043 / 2.910781, "skew": None}
 L2_NOTE = "inputs larger than L2 (22.5 GB of expert weights read per step)"
 CPU_TOKENS = 16     # tokens in the oracle's timed sample

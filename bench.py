@@ -449,7 +449,7 @@ def ffn_roofline(cfg, counts, ffn_ms, peaks, traffic_key):
                 "unit": "GB/s", "frac": ach / peaks["hbm_gbs"],
                 "traffic": traffic,
                 "algorithmic_bytes": alg_bytes,
-                "kernel": ("grouped_gemm_fp8_kernel<32,1,*>" if fp8 else
+                "kernel": ("grouped_gemm_fp8_pair_kernel" if fp8 else
                            "grouped_gemm_kernel<32,10>") +
                           " (gate/up + down launches of one expert-FFN call)",
                 "peak_source": f"{peaks['source']} hbm_gbs (copy)"}

@@ -634,12 +634,14 @@ moe_status expert_ffn_fp8(const moe_shape* s, const void* x_perm,
   zero_i32_kernel<<<1, 32, 0, cs>>>(ctr, 2);
   MOE_CHECK_LAUNCH();
   const bool small = A <= 48LL * N;
-  if (!small && d % 256 == 0 && ue8_pitch(d) <= kF8PMaxPitch &&
+  if (d % 256 == 0 && ue8_pitch(d) <= kF8PMaxPitch &&
       ue8_pitch(I) <= kF8PMaxPitch && ue8_pitch(SI) <= kF8PMaxPitch) {
-    // Prefill-sized groups: e4m3 CTA pairs with the block scales applied in
-    // the tensor core.  The gate/up pass requantizes H to e4m3 1 x 128
-    // blocks (the same rule as every activation) in its epilogue, for the
-    // down pass.
+    // e4m3 CTA pairs with the block scales applied in the tensor core, for
+    // prefill- and decode-sized groups alike (a decode item's few tokens
+    // cost the MMA about as much per instruction as a prefill item's, and
+    // the weight stream bounds it).  The gate/up pass requantizes H to e4m3
+    // 1 x 128 blocks (the same rule as every activation) in its epilogue,
+    // for the down pass.
     float* hb = reinterpret_cast<float*>(wsb + w.h_routed);
     float* hbs = reinterpret_cast<float*>(wsb + w.h_shared);
     uint8_t* q8 = reinterpret_cast<uint8_t*>(wsb + w.h8_routed);

@@ -168,8 +168,9 @@ FP8_CASES = {
     # the block-scaled CTA-pair kernel with reductions of 6 and 3 128-blocks
     # (scale groups of four stages, the last one partly used)
     "pair_d768_I384_T1200": ("tiny", dict(SMALL, T=1200, d=768, d_ff=384)),
-    # d % 256 != 0: prefill-sized groups on the weights-on-M kernels
+    # d % 256 != 0: the single-SM kernels, prefill- and decode-sized groups
     "fallback_d384_T1200": ("tiny", dict(SMALL, T=1200, d=384, d_ff=256)),
+    "fallback_small_d384_T64": ("tiny", dict(SMALL, d=384, d_ff=256)),
     "no_shared_T1": ("tiny", dict(SMALL, T=1, n_shared=0)),
     "no_shared_T900": ("tiny", dict(SMALL, T=900, n_shared=0, d=512)),
 }

@@ -346,17 +346,22 @@ WsLayout ws_layout(const moe_shape* s) {
   w.perm_hist = off;
   off = round256(off + static_cast<size_t>(cdiv(s->T, kPermChunk)) *
                            s->n_routed * 4);
-  // H between the passes (MOE_FP8: fp32, requantized to e4m3 below)
-  const size_t hs = s->dtype == MOE_FP8 ? 4 : es;
+  // H between the passes (MOE_FP8: the single-SM kernels' e4m3 codes and
+  // scales of H)
+  const long long SI = static_cast<long long>(s->n_shared) * s->d_ff;
   w.h_routed = off;
-  off = round256(off + static_cast<size_t>(A) * s->d_ff * hs);
+  off = round256(off + (s->dtype == MOE_FP8
+                            ? fp8_buf_bytes(A, s->d_ff, false)
+                            : static_cast<size_t>(A) * s->d_ff * es));
   w.h_shared = off;
-  off = round256(off + static_cast<size_t>(s->T) * s->n_shared * s->d_ff * hs);
+  off = round256(off + (s->dtype == MOE_FP8
+                            ? (SI > 0 ? fp8_buf_bytes(s->T, SI, false) : 0)
+                            : static_cast<size_t>(s->T) * SI * es));
   w.u_q = off;          // MOE_FP8: e4m3 codes of u and their block scales
   if (s->dtype == MOE_FP8 && s->n_shared > 0)
     off += fp8_buf_bytes(s->T, s->d, false);
-  // MOE_FP8 prefill path: H as e4m3 codes and scales (requantized from the
-  // fp32 H that the gate/up pass leaves in h_routed / h_shared)
+  // MOE_FP8 CTA-pair path: H as e4m3 codes, scales and UE8M0 tables, written
+  // by the gate/up pass's epilogue
   w.h8_routed = off;
   if (s->dtype == MOE_FP8) off += fp8_buf_bytes(A, s->d_ff, false);
   w.h8_shared = off;
@@ -642,11 +647,10 @@ moe_status expert_ffn_fp8(const moe_shape* s, const void* x_perm,
     // the weight stream bounds it).  The gate/up pass requantizes H to e4m3
     // 1 x 128 blocks (the same rule as every activation) in its epilogue,
     // for the down pass.
-    float* hb = reinterpret_cast<float*>(wsb + w.h_routed);
-    float* hbs = reinterpret_cast<float*>(wsb + w.h_shared);
     uint8_t* q8 = reinterpret_cast<uint8_t*>(wsb + w.h8_routed);
     uint8_t* q8s = reinterpret_cast<uint8_t*>(wsb + w.h8_shared);
-    // padding bytes of the H tables' rows (no block writes them)
+    // padding bytes of the H tables' rows (no block writes them); the gate/up
+    // pass writes H's codes and scales only (its `out` is not used)
     if (ue8_pitch(I) * kQBlock > I && A > 0)
       MOE_CHECK_CUDA(cudaMemsetAsync(fp8_ue8(q8, A, I, false), 127,
                                      static_cast<size_t>(A) * ue8_pitch(I),
@@ -676,9 +680,9 @@ moe_status expert_ffn_fp8(const moe_shape* s, const void* x_perm,
     q.sx_shared = has_shared ? fp8_ue8(u8, T, d, false) : nullptr;
     q.pitch_routed = ue8_pitch(d);
     q.pitch_shared = ue8_pitch(d);
-    q.out_routed = hb;
+    q.out_routed = nullptr;
     q.ld_routed = I;
-    q.out_shared = hbs;
+    q.out_shared = nullptr;
     q.ld_shared = SI;
     q.item_counter = ctr;
     q.q8_routed = q8;

@@ -1,5 +1,7 @@
 // Grouped expert GEMMs in e4m3 with block scales and promotion of the
-// partial sums to fp32 every 128 elements of the reduction.
+// partial sums to fp32 every 128 elements of the reduction, on the CUDA
+// cores: the kernels for shapes whose d is not a multiple of 256 (the
+// others run on the block-scaled CTA-pair kernel, gemm_fp8_pair.cuh).
 // (DeepSeek-V3 report commentary, cooktownmusic.com, FP8 training-framework
 // part: FP8 GEMM inputs, fine-grained block scaling (Fig. 7a), partial
 // results promoted to FP32 on the CUDA cores at N_C = 128 (Fig. 7b);

@@ -606,8 +606,10 @@ moe_status launch_gemm_fp8_pair(const F8PairMaps& m, const F8PairParams& p,
 }
 
 // MOE_FP8 expert FFNs: quantize u for the shared experts, gate/up (+ SwiGLU
-// + requantization of H), down.  Small average group size -> 32-token
-// chunks (weight streaming); else 128-token chunks.
+// + requantization of H), down.  d a multiple of 256: the block-scaled
+// CTA-pair kernel for every group size.  Otherwise the single-SM kernels:
+// 32-token chunks for a small average group size (weight streaming), else
+// 128-token chunks.
 moe_status expert_ffn_fp8(const moe_shape* s, const void* x_perm,
                           const int32_t* offsets, const void* w_gu8,
                           const void* w_down8, const void* u,

@@ -1764,11 +1764,11 @@ moe_status moe_backward(const moe_shape* s, const void* dh, const void* u,
   }
   // saved pre-activations (moe_expert_ffn_train): both or neither
   const bool saved = act != nullptr;
+  if (!saved && act_shared != nullptr)
+    return fail(MOE_ERR_INVALID_ARG, "act_shared given without act");
   if (saved && T > 0) {
     NEED_PTR(act);
     if (S > 0) NEED_PTR(act_shared);
-  } else if (act_shared != nullptr) {
-    return fail(MOE_ERR_INVALID_ARG, "act_shared given without act");
   }
   const BwdLayout w = bwd_layout(s);
   if (ws == nullptr) return fail(MOE_ERR_WORKSPACE, "workspace is NULL");

@@ -197,12 +197,13 @@ def test_backward_deterministic(moe):
         assert torch.equal(first[k], again[k]), k
 
 
-def test_backward_empty_batch(moe):
+@pytest.mark.parametrize("saved", [False, True], ids=["recompute", "saved"])
+def test_backward_empty_batch(moe, saved):
     cfg = get_config("tiny").with_(**dict(BASE, T=0))
     g = make_inputs(cfg.with_(T=4))
     layer = _layer(moe, g, cfg)
     u = g["u"][:0]
-    layer(u)
+    layer(u, save_for_backward=saved)
     gr = layer.backward(u, torch.empty((0, cfg.d), dtype=torch.bfloat16,
                                        device="cuda"))
     torch.cuda.synchronize()
